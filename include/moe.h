@@ -1,0 +1,176 @@
+/*
+ * moe.h -- C ABI of the single-GPU mixture-of-experts FFN layer forward (sm_103a).
+ *
+ * The layer, as the expert-parallelism pages state it ("Expert Parallelism (MoE)",
+ * section "MoE Layer Structure"; "Expert Parallelism (EP)", section "Key math / How
+ * it works"):
+ *
+ *   1. router: logits = X . W_r^T (+ b_r), softmax over the E experts, top-K per token;
+ *   2. dispatch: every token goes to each of its K experts; on one GPU this is a
+ *      permutation that packs each expert's rows contiguously (the all-to-all of
+ *      "The All-to-All Communication"), after a per-expert capacity
+ *      C = floor((T / E) * capacity_factor) drops the assignments that arrive when their
+ *      expert is full ("Top-K Routing and Capacity Factor");
+ *   3. experts: Linear(d -> F) -> GELU -> Linear(F -> d) on each expert's rows;
+ *   4. combine: Y[t] = sum over t's kept assignments of routing_weight * expert_output;
+ *   5. aux statistics f_i, P_i and L_aux = alpha * sum_i f_i P_i ("Load Balancing: The
+ *      Auxiliary Loss"), reported and never added to Y.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor pointers are DEVICE pointers, row-major, 16-byte aligned, owned by the
+ *   caller.  The library never allocates or frees device memory.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Every
+ *   call only enqueues work on it and returns without synchronising the host.
+ * - The returned status covers argument validation and kernel-launch errors.  Errors
+ *   that arise on the device (an expert id out of range, a bounded wait that gave up,
+ *   packed rows exceeding the buffer) are recorded in a status word inside `ws`;
+ *   moe_sync_status() synchronises the stream, returns and clears it.
+ * - Activations and weights have the config's dtype (fp32 or bf16); logits, routing
+ *   weights, biases, expert outputs (y_perm, y_shared) and statistics are fp32;
+ *   indices are int32.
+ * - Weights use the Linear layout [out, in]: W_r [E, d], W1 [G, F, d], W2 [G, d, F].
+ * - Flat assignment index a = t*K + k.  Routing ties: logits compare as fp32, higher
+ *   first, equal values -> lower expert id.  Routing weights are the softmax
+ *   probabilities (cfg.renormalize = 1 divides them by their sum over the K picks).
+ * - Drop order: an assignment is dropped iff its expert already holds C assignments
+ *   earlier in flat order.  Rows inside an expert's packed block are in ascending
+ *   flat order.  Routing, counts, offsets, slot and src are deterministic.
+ * - Limits: 1 <= K <= min(E, 32), E <= 256, T >= 0 with T*K < 2^31; d and F multiples
+ *   of 8 (bf16) or 4 (fp32).  Violations return MOE_ERR_INVALID / MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,      /* bad argument: null / misaligned pointer, bad sizes */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_TIMEOUT = 4,      /* (device) a bounded spin-wait gave up */
+  MOE_ERR_DEVICE = 5        /* (device) out-of-range expert id or packed-row overflow */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+typedef struct {
+  int32_t T;            /* tokens */
+  int32_t d;            /* hidden size */
+  int32_t E;            /* routed experts */
+  int32_t K;            /* experts per token */
+  int32_t F;            /* expert width (the "4d" of the FFN) */
+  int32_t dtype;        /* moe_dtype_t of activations and weights */
+  int32_t capacity;     /* C per expert; < 0 means no dropping */
+  int32_t renormalize;  /* 0: w = softmax prob (default); 1: w / sum_k w */
+  float alpha;          /* aux-loss weight */
+} moe_config;
+
+/* Bytes of device workspace `ws` the calls below need for this config.  The caller
+ * allocates it and ZERO-FILLS it once before first use; the library keeps it
+ * consistent afterwards.  One workspace must not be used by two calls that can run
+ * concurrently. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Rows the packed buffers (src, x_perm, h, y_perm) must hold:
+ * min(T*K, E*C) with dropping, T*K without. */
+int64_t moe_rows_capacity(const moe_config* cfg);
+
+/* Step 1 -- router Linear, softmax over E, top-K ("MoE Layer Structure").
+ *   x        [T, d]  dtype, or NULL: then `logits` is an INPUT holding fp32 logits
+ *   w_r      [E, d]  dtype (ignored when x == NULL)
+ *   b_r      [E]     fp32, nullable (added to the logits before softmax)
+ *   logits   [T, E]  fp32, written (or read when x == NULL)
+ *   topk_ids [T, K]  int32 out, sorted by logit descending
+ *   topk_w   [T, K]  fp32 out, routing weights
+ *   ws       workspace; receives per-block partial sums of the softmax probabilities
+ *            that moe_aux_stats reduces. */
+moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
+                       float* logits, int32_t* topk_ids, float* topk_w, void* ws, void* stream);
+
+/* Step 2 -- histogram, capacity, drop mask and dispatch permutation
+ * ("The All-to-All Communication", "Top-K Routing and Capacity Factor").
+ *   x        [T, d] dtype (nullable together with x_perm: routing only, no row copy)
+ *   topk_ids [T, K] int32 in
+ *   counts   [E]    int32 out: assignments per expert before dropping
+ *   offsets  [E+1]  int32 out: exclusive scan of kept counts; offsets[E] = R rows kept
+ *   slot     [T, K] int32 out: packed row of assignment (t,k), or -1 if dropped
+ *   src      [moe_rows_capacity] int32 out: packed row -> flat assignment t*K+k
+ *   x_perm   [moe_rows_capacity, d] dtype out: x_perm[r] = x[src[r] / K]
+ * Rows at and beyond offsets[E] are left untouched. */
+moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                          int32_t* counts, int32_t* offsets, int32_t* slot, int32_t* src,
+                          void* x_perm, void* ws, void* stream);
+
+/* Step 3a -- grouped first expert Linear with GELU fused in its epilogue
+ * ("Each expert applies: Linear(d -> 4d) -> GELU -> Linear(4d -> d)").
+ *   x_perm   [rows_cap, d] dtype in; group g owns rows [offsets[g], offsets[g+1])
+ *   offsets  [n_groups+1] int32 DEVICE pointer (read on the device; no host sync)
+ *   w1       [n_groups, F, d] dtype
+ *   h        [rows_cap, F] dtype out: h = GELU(x_perm . W1[g]^T), exact erf form,
+ *            fp32 accumulation, rounded once to dtype.
+ * n_groups = E for the routed experts; n_groups = 1 with offsets {0, T} and x in place
+ * of x_perm runs a shared (always-on) expert over all tokens. */
+moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                           int32_t n_groups, int64_t rows_cap, const void* w1, void* h,
+                           void* ws, void* stream);
+
+/* Step 3b -- grouped second expert Linear: y_perm = h . W2[g]^T.
+ *   h [rows_cap, F] dtype; w2 [n_groups, d, F] dtype;
+ *   y_perm [rows_cap, d] FP32 out (expert outputs stay fp32 until the combine rounds
+ *   the layer output once). */
+moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t* offsets,
+                             int32_t n_groups, int64_t rows_cap, const void* w2, void* y_perm,
+                             void* ws, void* stream);
+
+/* Step 3 -- both expert Linears (moe_expert_up then moe_expert_down). */
+moe_status_t moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                             int32_t n_groups, int64_t rows_cap, const void* w1, const void* w2,
+                             void* h, void* y_perm, void* ws, void* stream);
+
+/* Step 4 -- combine back to token order ("Y = sum over selected experts of
+ * expert_output[token] * routing_weight[token]").  Gather-side, no atomics:
+ *   Y[t] = sum_{k ascending, slot[t,k] >= 0} topk_w[t,k] * y_perm[slot[t,k]]
+ *          (+ y_shared[t]), accumulated in fp32 and rounded once.
+ *   y_perm [rows_cap, d] fp32, slot [T, K], topk_w [T, K], y_shared [T, d] fp32
+ *   nullable, y [T, d] dtype out.  A dropped assignment contributes exactly 0. */
+moe_status_t moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot,
+                         const float* topk_w, const void* y_shared, void* y, void* stream);
+
+/* Step 5 -- auxiliary load-balancing statistics ("Load Balancing: The Auxiliary Loss"):
+ *   f[i] = counts[i] / (T*K)          (pre-drop assignment fraction)
+ *   P[i] = mean_t softmax(logits)[t,i] (from the partial sums moe_route left in ws)
+ *   l_aux[0] = alpha * sum_i f[i] * P[i]
+ * All outputs fp32 device pointers; with T = 0 all are 0.  Must follow the moe_route
+ * call that used the same ws. */
+moe_status_t moe_aux_stats(const moe_config* cfg, const int32_t* counts, const void* ws,
+                           float* f, float* P, float* l_aux, void* stream);
+
+/* Synchronise `stream`, then return and clear the device status word in `ws`
+ * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE), or MOE_ERR_CUDA if a kernel failed. */
+moe_status_t moe_sync_status(void* ws, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status_t status);
+
+/* Number of kernels this library has launched in this process (host-side counter). */
+uint64_t moe_launch_count(void);
+
+/* Test hook for the bounded wait of the dispatch scan.  When skip_block >= 0, the next
+ * moe_dispatch call makes scan block `skip_block` withhold its published counts, so its
+ * successor's wait runs out after `spin_limit` polls and records MOE_ERR_TIMEOUT in
+ * the device status word; every block still terminates.  Results of that call are
+ * invalid.  The hook disarms itself after one call; skip_block < 0 disarms it. */
+void moe_test_arm_scan_timeout(int32_t skip_block, int32_t spin_limit);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -220,8 +220,12 @@ def combine(y_perm, slot, w, T: int, y_shared=None) -> np.ndarray:
 # Auxiliary statistics: [EPM] "Load Balancing: The Auxiliary Loss".
 # --------------------------------------------------------------------------------------
 def aux_stats(ids, p, E: int, alpha: float):
-    """f_i = count_i / (T*K) (pre-drop), P_i = mean_t p[t,i], L_aux = alpha * sum f_i P_i."""
+    """f_i = count_i / (T*K) (pre-drop), P_i = mean_t p[t,i], L_aux = alpha * sum f_i P_i.
+
+    With no tokens the fractions and means are empty sums: all statistics are 0."""
     ids = np.asarray(ids, dtype=np.int64)
+    if ids.size == 0:
+        return np.zeros(E), np.zeros(E), 0.0
     counts = np.bincount(ids.reshape(-1), minlength=E).astype(np.float64)
     f = counts / ids.size
     P = widen(p).mean(axis=0)

@@ -1,0 +1,250 @@
+// C-ABI entry points: argument validation, workspace carving and kernel launches.
+// Every call only enqueues work on the caller's stream; nothing here synchronises the
+// host except moe_sync_status.
+#include <atomic>
+#include <stdio.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+cudaError_t launch_softmax_topk(const float* logits, int T, int E, int K, int renorm, int32_t* ids,
+                                float* w, float* ppart, int nblk, cudaStream_t st);
+cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsigned long long* desc,
+                        int32_t* pos, int32_t* counts, int32_t* offsets, uint32_t* hdr,
+                        int skip_block, int spin_limit, cudaStream_t st);
+cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const int32_t* pos,
+                            const int32_t* offsets, int Tn, int d, int E, int K, int C,
+                            int32_t* slot, int32_t* src, void* xp, int64_t rows_cap, uint32_t* hdr,
+                            int num_sms, cudaStream_t st);
+cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const float* w,
+                           const void* ys, void* y, int Tn, int d, int K, int num_sms,
+                           cudaStream_t st);
+cudaError_t launch_aux(const int32_t* counts, const float* ppart, int nblk, int E, int Tn, int K,
+                       float alpha, float* f, float* P, float* l_aux, cudaStream_t st);
+cudaError_t launch_simt_grouped(int dtype, const void* A, const void* B, void* C,
+                                const int32_t* offsets, int G, int N, int Kd, int64_t rows_cap,
+                                bool gelu, uint32_t* hdr, cudaStream_t st);
+cudaError_t launch_simt_router(int dtype, const void* x, const void* w_r, const float* b_r,
+                               float* logits, int T, int E, int d, uint32_t* hdr, cudaStream_t st);
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static std::atomic<int> g_skip_block{-1};
+static std::atomic<int> g_spin_limit{1 << 21};
+
+static int num_sms() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static moe_status_t check_cfg(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID;
+  if (c->T < 0 || c->d <= 0 || c->E <= 0 || c->K <= 0 || c->F <= 0) return MOE_ERR_INVALID;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID;
+  if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID;
+  if (c->K > c->E) return MOE_ERR_INVALID;
+  if (c->E > 256 || c->K > 32) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->K >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  const int vec = c->dtype == MOE_BF16 ? 8 : 4;
+  if (c->d % vec != 0 || c->F % vec != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static moe_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  fprintf(stderr, "moe: CUDA error: %s\n", cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+static int64_t rows_capacity(const moe_config& c) {
+  const int64_t A = (int64_t)c.T * c.K;
+  if (c.capacity < 0) return A;
+  const int64_t ec = (int64_t)c.E * c.capacity;
+  return A < ec ? A : ec;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return ws_layout(*cfg).total;
+}
+
+int64_t moe_rows_capacity(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return -1;
+  return rows_capacity(*cfg);
+}
+
+moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
+                       float* logits, int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!logits || !topk_ids || !topk_w || !ws) return MOE_ERR_INVALID;
+  if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(ws))
+    return MOE_ERR_INVALID;
+  if (x != nullptr && (w_r == nullptr || !aligned16(x) || !aligned16(w_r))) return MOE_ERR_INVALID;
+  if (b_r != nullptr && !aligned16(b_r)) return MOE_ERR_INVALID;
+  if (c.T == 0) return MOE_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(c);
+  uint32_t* hdr = (uint32_t*)ws;
+  if (x != nullptr) {
+    s = cuda_status(launch_simt_router(c.dtype, x, w_r, b_r, logits, c.T, c.E, c.d, hdr, st));
+    if (s != MOE_OK) return s;
+  }
+  return cuda_status(launch_softmax_topk(logits, c.T, c.E, c.K, c.renormalize, topk_ids, topk_w,
+                                         (float*)((char*)ws + L.ppart), L.nblk_route, st));
+}
+
+moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                          int32_t* counts, int32_t* offsets, int32_t* slot, int32_t* src,
+                          void* x_perm, void* ws, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!topk_ids || !counts || !offsets || !slot || !src || !ws) return MOE_ERR_INVALID;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID;
+  if (!aligned16(topk_ids) || !aligned16(counts) || !aligned16(offsets) || !aligned16(slot) ||
+      !aligned16(src) || !aligned16(ws))
+    return MOE_ERR_INVALID;
+  if (x != nullptr && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int A = c.T * c.K;
+  if (A == 0) {
+    s = cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st));
+    if (s != MOE_OK) return s;
+    return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1), st));
+  }
+  const WsLayout L = ws_layout(c);
+  uint32_t* hdr = (uint32_t*)ws;
+  // reset the scan ticket and descriptors (the status word at offset 0 is kept)
+  s = cuda_status(cudaMemsetAsync((char*)ws + 4, 0, L.desc + (size_t)L.nblk_scan * c.E * 8 - 4, st));
+  if (s != MOE_OK) return s;
+  const int skip = g_skip_block.exchange(-1);
+  const int spin = skip >= 0 ? g_spin_limit.load() : (1 << 21);
+  int32_t* pos = (int32_t*)((char*)ws + L.pos);
+  s = cuda_status(launch_scan(topk_ids, A, c.E, c.capacity, L.nblk_scan,
+                              (unsigned long long*)((char*)ws + L.desc), pos, counts, offsets, hdr,
+                              skip, spin, st));
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_dispatch(c.dtype, x, topk_ids, pos, offsets, c.T, c.d, c.E, c.K,
+                                     c.capacity, slot, src, x_perm, rows_capacity(c), hdr,
+                                     num_sms(), st));
+}
+
+static moe_status_t check_ffn_args(const moe_config* cfg, const void* in, const int32_t* offsets,
+                                   int32_t n_groups, int64_t rows_cap, const void* w,
+                                   const void* out, const void* ws) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!in || !offsets || !w || !out || !ws) return MOE_ERR_INVALID;
+  if (!aligned16(in) || !aligned16(w) || !aligned16(out) || !aligned16(ws) || ((uintptr_t)offsets & 3))
+    return MOE_ERR_INVALID;
+  if (n_groups < 1 || n_groups > 256 || rows_cap < 0) return MOE_ERR_INVALID;
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                           int32_t n_groups, int64_t rows_cap, const void* w1, void* h, void* ws,
+                           void* stream) {
+  moe_status_t s = check_ffn_args(cfg, x_perm, offsets, n_groups, rows_cap, w1, h, ws);
+  if (s != MOE_OK) return s;
+  if (rows_cap == 0) return MOE_OK;
+  const moe_config& c = *cfg;
+  return cuda_status(launch_simt_grouped(c.dtype, x_perm, w1, h, offsets, n_groups, c.F, c.d,
+                                         rows_cap, true, (uint32_t*)ws, (cudaStream_t)stream));
+}
+
+moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t* offsets,
+                             int32_t n_groups, int64_t rows_cap, const void* w2, void* y_perm,
+                             void* ws, void* stream) {
+  moe_status_t s = check_ffn_args(cfg, h, offsets, n_groups, rows_cap, w2, y_perm, ws);
+  if (s != MOE_OK) return s;
+  if (rows_cap == 0) return MOE_OK;
+  const moe_config& c = *cfg;
+  return cuda_status(launch_simt_grouped(c.dtype, h, w2, y_perm, offsets, n_groups, c.d, c.F,
+                                         rows_cap, false, (uint32_t*)ws, (cudaStream_t)stream));
+}
+
+moe_status_t moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                             int32_t n_groups, int64_t rows_cap, const void* w1, const void* w2,
+                             void* h, void* y_perm, void* ws, void* stream) {
+  moe_status_t s = moe_expert_up(cfg, x_perm, offsets, n_groups, rows_cap, w1, h, ws, stream);
+  if (s != MOE_OK) return s;
+  return moe_expert_down(cfg, h, offsets, n_groups, rows_cap, w2, y_perm, ws, stream);
+}
+
+moe_status_t moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot,
+                         const float* topk_w, const void* y_shared, void* y, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!y_perm || !slot || !topk_w || !y) return MOE_ERR_INVALID;
+  if (!aligned16(y_perm) || !aligned16(slot) || !aligned16(topk_w) || !aligned16(y)) return MOE_ERR_INVALID;
+  if (y_shared != nullptr && !aligned16(y_shared)) return MOE_ERR_INVALID;
+  if (c.T == 0) return MOE_OK;
+  return cuda_status(launch_combine(c.dtype, y_perm, slot, topk_w, y_shared, y, c.T, c.d, c.K,
+                                    num_sms(), (cudaStream_t)stream));
+}
+
+moe_status_t moe_aux_stats(const moe_config* cfg, const int32_t* counts, const void* ws, float* f,
+                           float* P, float* l_aux, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!counts || !ws || !f || !P || !l_aux) return MOE_ERR_INVALID;
+  if (!aligned16(ws) || ((uintptr_t)counts & 3) || ((uintptr_t)f & 3) || ((uintptr_t)P & 3) ||
+      ((uintptr_t)l_aux & 3))
+    return MOE_ERR_INVALID;
+  const WsLayout L = ws_layout(c);
+  return cuda_status(launch_aux(counts, (const float*)((const char*)ws + L.ppart), L.nblk_route,
+                                c.E, c.T, c.K, c.alpha, f, P, l_aux, (cudaStream_t)stream));
+}
+
+moe_status_t moe_sync_status(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  moe_status_t s = cuda_status(cudaStreamSynchronize(st));
+  if (s != MOE_OK) return s;
+  uint32_t word = 0;
+  s = cuda_status(cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost));
+  if (s != MOE_OK) return s;
+  if (word != 0) {
+    s = cuda_status(cudaMemset(ws, 0, sizeof(word)));
+    if (s != MOE_OK) return s;
+  }
+  if (word & DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (word & (DEV_ERR_BAD_ID | DEV_ERR_OVERFLOW)) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID: return "MOE_ERR_INVALID";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+void moe_test_arm_scan_timeout(int32_t skip_block, int32_t spin_limit) {
+  g_spin_limit.store(spin_limit > 0 ? spin_limit : 1);
+  g_skip_block.store(skip_block);
+}
+
+}  // extern "C"

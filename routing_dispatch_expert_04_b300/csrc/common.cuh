@@ -1,0 +1,109 @@
+// Shared device helpers, workspace layout and launch bookkeeping of the MoE layer library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ device status word
+// Bits OR-ed into ws header word 0 by kernels; moe_sync_status maps them to a status.
+constexpr uint32_t DEV_ERR_TIMEOUT = 1u;   // a bounded spin-wait gave up
+constexpr uint32_t DEV_ERR_BAD_ID = 2u;    // expert id outside [0, E)
+constexpr uint32_t DEV_ERR_OVERFLOW = 4u;  // offsets[G] larger than the row buffer
+
+__device__ __forceinline__ void raise_error(uint32_t* status, uint32_t bit) {
+  atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------------ workspace layout
+// [0, 256)        header: u32 status, u32 scan ticket
+// desc            scan descriptors, nblk_scan * E * u64 (flag << 32 | value)
+// pos             A * i32, position of each assignment inside its expert (pre-drop)
+// ppart           nblk_route * E * f32, per-block sums of softmax probabilities
+constexpr int SCAN_THREADS = 256;
+constexpr int SCAN_IPT = 16;
+constexpr int SCAN_ITEMS = SCAN_THREADS * SCAN_IPT;  // assignments per scan block
+constexpr int ROUTE_WARPS = 8;
+constexpr int ROUTE_TPW = 4;                          // tokens per warp
+constexpr int ROUTE_TOKENS = ROUTE_WARPS * ROUTE_TPW; // tokens per route block
+
+struct WsLayout {
+  size_t desc, pos, ppart, total;
+  int nblk_scan, nblk_route;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(const moe_config& c) {
+  WsLayout L;
+  int64_t A = (int64_t)c.T * c.K;
+  L.nblk_scan = (int)((A + SCAN_ITEMS - 1) / SCAN_ITEMS);
+  L.nblk_route = (int)(((int64_t)c.T + ROUTE_TOKENS - 1) / ROUTE_TOKENS);
+  size_t off = 256;
+  L.desc = off;
+  off = align_up(off + (size_t)L.nblk_scan * c.E * 8, 256);
+  L.pos = off;
+  off = align_up(off + (size_t)A * 4, 256);
+  L.ppart = off;
+  off = align_up(off + (size_t)L.nblk_route * c.E * 4, 256);
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------------ launch bookkeeping
+void count_launch();
+
+// ------------------------------------------------------------------ element helpers
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int PER16 = 4;  // elements per 16-byte vector
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+  __device__ __forceinline__ static float to_f(float x) { return x; }
+  __device__ __forceinline__ static float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int PER16 = 8;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);  // .x = low half
+      w[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ __forceinline__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ __forceinline__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_v4(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+}  // namespace moe

@@ -1,0 +1,127 @@
+// Softmax over the experts and top-K selection, one warp per token.
+//
+// "Expert Parallelism (MoE)", section "MoE Layer Structure": for each token the
+// top-K experts are activated; the routing weight is the softmax probability of the
+// chosen expert ("Load Balancing: The Auxiliary Loss" speaks of the probability after
+// softmax).  Selection compares the fp32 logits: higher first, equal values go to the
+// lower expert id, so the picks are a deterministic function of the fp32 logits.
+//
+// The kernel also leaves, per block, the sum over its tokens of every expert's
+// probability; the aux-statistics kernel reduces those partial sums in a fixed order
+// to P_i, so the result is deterministic without floating-point atomics.
+#include <math.h>
+#include <limits.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+template <int VPT>
+__global__ void __launch_bounds__(ROUTE_WARPS * 32)
+softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renorm,
+                    int32_t* __restrict__ ids, float* __restrict__ wout,
+                    float* __restrict__ ppart) {
+  __shared__ float s_p[ROUTE_WARPS][VPT * 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float pacc[VPT];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) pacc[j] = 0.f;
+
+  const int t0 = blockIdx.x * ROUTE_TOKENS + warp * ROUTE_TPW;
+  for (int i = 0; i < ROUTE_TPW; ++i) {
+    const int t = t0 + i;
+    if (t >= T) break;  // warp-uniform
+    const float* row = logits + (size_t)t * E;
+    float v[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = (e < E) ? row[e] : -INFINITY;
+    }
+    // softmax: max, sum of exp, normalise
+    float m = v[0];
+#pragma unroll
+    for (int j = 1; j < VPT; ++j) m = fmaxf(m, v[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float p[VPT];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int e = lane + 32 * j;
+      p[j] = (e < E) ? expf(v[j] - m) : 0.f;
+      s += p[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      p[j] = p[j] / s;
+      pacc[j] += p[j];
+    }
+    // top-K: K rounds of a warp arg-max under (value desc, id asc)
+    uint32_t taken = 0;
+    int my_id = 0;
+    float my_w = 0.f, wsum = 0.f;
+    for (int k = 0; k < K; ++k) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < bi))) {
+          bv = v[j];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      const int owner = bi & 31, jw = bi >> 5;
+      float mine = 0.f;
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+        if (j == jw) mine = p[j];
+      if (lane == owner) taken |= 1u << jw;
+      const float pw = __shfl_sync(0xffffffffu, mine, owner);
+      if (lane == k) {
+        my_id = bi;
+        my_w = pw;
+      }
+      wsum += pw;
+    }
+    if (renorm) my_w = my_w / wsum;
+    if (lane < K) {
+      ids[(size_t)t * K + lane] = my_id;
+      wout[(size_t)t * K + lane] = my_w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) s_p[warp][lane + 32 * j] = pacc[j];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < ROUTE_WARPS; ++w) acc += s_p[w][e];
+    ppart[(size_t)blockIdx.x * E + e] = acc;
+  }
+}
+
+cudaError_t launch_softmax_topk(const float* logits, int T, int E, int K, int renorm, int32_t* ids,
+                                float* w, float* ppart, int nblk, cudaStream_t st) {
+  const dim3 grid(nblk), block(ROUTE_WARPS * 32);
+  if (E <= 32) softmax_topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart);
+  else if (E <= 64) softmax_topk_kernel<2><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart);
+  else if (E <= 128) softmax_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart);
+  else softmax_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,235 @@
+// Per-expert histogram, capacity, drop mask and the dispatch permutation.
+//
+// "Expert Parallelism (MoE)", "Top-K Routing and Capacity Factor": each expert accepts
+// at most C assignments; assignments that would push an expert over capacity are
+// dropped and their routing weight is zeroed.  "The All-to-All Communication": after
+// routing, every token is sent to the holder of each chosen expert; on one GPU the
+// all-to-all becomes a permutation that packs each expert's rows contiguously.
+//
+// Order fixed here: assignments are taken in flat order a = t*K + k.  An assignment's
+// position in its expert is the number of earlier assignments to the same expert; it
+// is kept iff that position is below C, and kept rows of expert e are packed at
+// offsets[e] + position.  The result is unique, so it can be compared bit for bit.
+//
+// scan_kernel -- one pass over the flat id stream.  Each block takes a chunk of
+// SCAN_ITEMS assignments (chunk index drawn from an atomic ticket, so every block it
+// waits for has already started), ranks its assignments per expert with warp
+// match/popc and a per-expert running count in shared memory, publishes its per-expert
+// totals, and obtains the totals of all earlier chunks by a decoupled look-back with
+// one descriptor per (chunk, expert).  Every wait is bounded: past `spin_limit` polls
+// the block records a timeout in the status word and carries on, so the kernel always
+// terminates.  The last chunk knows the grand totals and writes counts and offsets.
+//
+// dispatch_kernel -- one warp per token: turns positions into packed rows (slot, src)
+// and copies the token's row once from HBM into each of its kept packed rows with
+// 16-byte loads and stores.
+#include "common.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+constexpr unsigned long long FLAG_AGG = 1ull << 32;   // this chunk's own totals
+constexpr unsigned long long FLAG_INCL = 2ull << 32;  // totals of chunks 0..this one
+
+__global__ void __launch_bounds__(SCAN_THREADS)
+scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
+            unsigned long long* desc, int32_t* __restrict__ pos, int32_t* __restrict__ counts,
+            int32_t* __restrict__ offsets, uint32_t* hdr, int skip_block, int spin_limit) {
+  constexpr int NW = SCAN_THREADS / 32;
+  __shared__ uint32_t s_wcnt[NW][256];  // (round stamp << 8) | count of e in warp
+  __shared__ int s_run[256];            // running count of e inside this chunk
+  __shared__ int s_excl[256];           // count of e in all earlier chunks
+  __shared__ int s_b;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) s_b = (int)atomicAdd(&hdr[1], 1u);
+  for (int i = tid; i < NW * 256; i += SCAN_THREADS) (&s_wcnt[0][0])[i] = 0u;
+  for (int e = tid; e < 256; e += SCAN_THREADS) s_run[e] = 0;
+  __syncthreads();
+  const int b = s_b;
+  const int64_t base = (int64_t)b * SCAN_ITEMS;
+  uint32_t lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+
+  int my_e[SCAN_IPT], my_r[SCAN_IPT];
+#pragma unroll
+  for (int r = 0; r < SCAN_IPT; ++r) {
+    const int64_t a = base + (int64_t)r * SCAN_THREADS + tid;
+    int e = -1;
+    if (a < A) {
+      e = ids[a];
+      if (e < 0 || e >= E) {
+        raise_error(hdr, DEV_ERR_BAD_ID);
+        e = -1;
+      }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int wrank = __popc(peers & lt);
+    const bool leader = (31 - __clz(peers)) == lane;
+    const uint32_t stamp = (uint32_t)(r + 1) << 8;
+    if (e >= 0 && leader) s_wcnt[warp][e] = stamp | (uint32_t)__popc(peers);
+    __syncthreads();
+    bool last = false;
+    int rank = 0;
+    if (e >= 0) {
+      int pre = 0;
+      for (int w = 0; w < warp; ++w) {
+        const uint32_t v = s_wcnt[w][e];
+        if ((v & ~0xffu) == stamp) pre += (int)(v & 0xffu);
+      }
+      last = leader;
+      for (int w = warp + 1; w < NW; ++w)
+        if ((s_wcnt[w][e] & ~0xffu) == stamp) last = false;
+      rank = s_run[e] + pre + wrank;
+    }
+    my_e[r] = e;
+    my_r[r] = rank;
+    __syncthreads();
+    if (last) s_run[e] = rank + 1;
+  }
+  __syncthreads();
+
+  // decoupled look-back, one thread per expert
+  const bool publish = (b != skip_block);
+  if (tid < E) {
+    const int agg = s_run[tid];
+    unsigned long long* mine = desc + (size_t)b * E + tid;
+    int excl = 0;
+    if (b == 0) {
+      if (publish) st_release_u64(mine, FLAG_INCL | (uint32_t)agg);
+    } else {
+      if (publish) st_release_u64(mine, FLAG_AGG | (uint32_t)agg);
+      int j = b - 1, spins = 0;
+      while (j >= 0) {
+        const unsigned long long v = ld_acquire_u64(desc + (size_t)j * E + tid);
+        const unsigned long long flag = v & ~0xffffffffull;
+        if (flag == 0) {
+          if (++spins > spin_limit) {
+            raise_error(hdr, DEV_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(64);
+          continue;
+        }
+        excl += (int)(uint32_t)v;
+        if (flag == FLAG_INCL) break;
+        --j;
+      }
+      if (publish) st_release_u64(mine, FLAG_INCL | (uint32_t)(excl + agg));
+    }
+    s_excl[tid] = excl;
+  }
+  __syncthreads();
+
+#pragma unroll
+  for (int r = 0; r < SCAN_IPT; ++r) {
+    if (my_e[r] >= 0) pos[base + (int64_t)r * SCAN_THREADS + tid] = s_excl[my_e[r]] + my_r[r];
+  }
+
+  if (b == nblk - 1) {  // block-uniform
+    if (tid < E) {
+      const int tot = s_excl[tid] + s_run[tid];
+      counts[tid] = tot;
+      s_run[tid] = (C < 0) ? tot : min(tot, C);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int acc = 0;
+      offsets[0] = 0;
+      for (int e = 0; e < E; ++e) {
+        acc += s_run[e];
+        offsets[e + 1] = acc;
+      }
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids,
+                const int32_t* __restrict__ pos, const int32_t* __restrict__ offsets, int Tn, int d,
+                int E, int K, int C, int32_t* __restrict__ slot, int32_t* __restrict__ src,
+                T* __restrict__ xp, int64_t rows_cap, uint32_t* hdr) {
+  __shared__ int s_slot[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = d / Elem<T>::PER16;
+  for (int t = blockIdx.x * 8 + warp; t < Tn; t += gridDim.x * 8) {
+    if (lane < K) {
+      const int64_t a = (int64_t)t * K + lane;
+      const int e = ids[a];
+      int s = -1;
+      if (e >= 0 && e < E) {
+        const int p = pos[a];
+        if (C < 0 || p < C) s = offsets[e] + p;
+      }
+      if (s >= rows_cap) {
+        raise_error(hdr, DEV_ERR_OVERFLOW);
+        s = -1;
+      }
+      slot[a] = s;
+      if (s >= 0) src[s] = (int32_t)a;
+      s_slot[warp][lane] = s;
+    }
+    __syncwarp();
+    if (xp != nullptr) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+      int j = lane;
+      for (; j + 96 < nvec; j += 128) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = ld_nc_v4(xr + j + 32 * u);
+        for (int k = 0; k < K; ++k) {
+          const int s = s_slot[warp][k];
+          if (s < 0) continue;
+          uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)s * d) + j;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) st_v4(dst + 32 * u, v[u]);
+        }
+      }
+      for (; j < nvec; j += 32) {
+        const uint4 v = ld_nc_v4(xr + j);
+        for (int k = 0; k < K; ++k) {
+          const int s = s_slot[warp][k];
+          if (s >= 0) st_v4(reinterpret_cast<uint4*>(xp + (size_t)s * d) + j, v);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsigned long long* desc,
+                        int32_t* pos, int32_t* counts, int32_t* offsets, uint32_t* hdr,
+                        int skip_block, int spin_limit, cudaStream_t st) {
+  scan_kernel<<<nblk, SCAN_THREADS, 0, st>>>(ids, A, E, C, nblk, desc, pos, counts, offsets, hdr,
+                                              skip_block, spin_limit);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const int32_t* pos,
+                            const int32_t* offsets, int Tn, int d, int E, int K, int C,
+                            int32_t* slot, int32_t* src, void* xp, int64_t rows_cap, uint32_t* hdr,
+                            int num_sms, cudaStream_t st) {
+  const int want = (Tn + 7) / 8;
+  const int grid = want < num_sms * 16 ? want : num_sms * 16;
+  if (dtype == MOE_BF16)
+    dispatch_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+        (const __nv_bfloat16*)x, ids, pos, offsets, Tn, d, E, K, C, slot, src, (__nv_bfloat16*)xp,
+        rows_cap, hdr);
+  else
+    dispatch_kernel<float><<<grid, 256, 0, st>>>((const float*)x, ids, pos, offsets, Tn, d, E, K, C,
+                                                 slot, src, (float*)xp, rows_cap, hdr);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,324 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the fp64 oracle.
+
+Tolerances: routing ids, counts, offsets, slot, src and the drop mask are compared bit
+for bit when the routing kernels are fed the oracle's fp32 logits; routing weights and
+P_i within 1e-6 relative (fp32 softmax against fp64); layer output
+max|GPU - oracle| / RMS(oracle) <= 1e-4 (fp32) or 2e-2 (bf16), over the tokens a
+near-tie cannot flip (logit gap of the K-th and (K+1)-th expert >= 1e-4, plus the
+capacity cascade those tokens can cause).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from routing_dispatch_expert_04_b300 import build as B
+from routing_dispatch_expert_04_b300 import native as N
+from routing_dispatch_expert_04_b300.layer import MoELayer
+from routing_dispatch_expert_04_b300.workloads import WORKLOADS, Workload, make_inputs, make_logits
+from parity_helpers import assert_rounded_to, comparable_tokens, rel_rms_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    B.build()
+    N.lib()
+
+
+def _routing_only(T, E, K, C, L32, renorm=False):
+    """Drive moe_route (logits given) + moe_dispatch (no row copy) + moe_aux_stats."""
+    cfg = N.make_config(T, 8, E, K, 8, "bf16", C, renorm, 0.01)
+    dev = "cuda"
+    R = max(N.rows_capacity(cfg), 1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device=dev)
+    logits = torch.from_numpy(np.ascontiguousarray(L32)).to(dev)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    slot = torch.empty((T, K), dtype=torch.int32, device=dev)
+    src = torch.full((R,), -7, dtype=torch.int32, device=dev)
+    f = torch.empty(E, dtype=torch.float32, device=dev)
+    P = torch.empty(E, dtype=torch.float32, device=dev)
+    l = torch.empty(1, dtype=torch.float32, device=dev)
+    N.route(cfg, None, None, None, logits, ids, w, ws)
+    N.dispatch(cfg, None, ids, counts, offsets, slot, src, None, ws)
+    N.aux_stats(cfg, counts, ws, f, P, l)
+    assert N.sync_status(ws) == 0
+    return dict(ids=to_np(ids), w=to_np(w), counts=to_np(counts), offsets=to_np(offsets),
+                slot=to_np(slot), src=to_np(src), f=to_np(f), P=to_np(P), l_aux=float(l.item()))
+
+
+def _check_routing(g, L32, K, C, E, renorm=False, alpha=0.01):
+    ids = O.top_k(L32, K)
+    p = O.softmax(L32)
+    w = O.routing_weights(p, ids, renorm)
+    plan = O.dispatch_plan(ids, E, C)
+    assert np.array_equal(g["ids"], ids)
+    assert np.max(np.abs(g["w"] - w) / np.abs(w)) <= 1e-6
+    assert np.array_equal(g["counts"], plan["counts"])
+    assert np.array_equal(g["offsets"], plan["offsets"])
+    assert np.array_equal(g["slot"], plan["slot"].reshape(-1, K))
+    R = plan["R"]
+    assert np.array_equal(g["src"][:R], plan["src"])
+    f, P, l_aux = O.aux_stats(ids, p, E, alpha)
+    assert np.array_equal(g["f"], f.astype(np.float32))
+    assert np.max(np.abs(g["P"] - P) / np.maximum(P, 1e-30)) <= 1e-5
+    assert abs(g["l_aux"] - l_aux) <= 1e-5 * l_aux
+    return plan
+
+
+# ------------------------------------------------------------------ routing, bit-exact
+@pytest.mark.parametrize("T,E,K,cf,ties,renorm", [
+    (256, 8, 2, 1.25, False, False),
+    (4096, 8, 2, 1.25, True, False),
+    (8192, 256, 8, None, False, False),
+    (16384, 128, 8, 1.5, True, False),
+    (65536, 8, 2, 1.0, False, False),
+    (5000, 64, 4, 0.9, True, True),
+    (4097, 33, 5, 2.0, True, False),
+    (1, 1, 1, 1.0, False, False),
+    (37, 5, 5, 0.5, True, False),
+])
+def test_routing_bit_exact_random_logits(T, E, K, cf, ties, renorm):
+    L32 = make_logits(T, E, seed=T + E, ties=ties).numpy()
+    C = O.capacity(T, E, cf)
+    g = _routing_only(T, E, K, C, L32, renorm)
+    _check_routing(g, L32, K, C, E, renorm)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "dsv3", "qwen3", "long"])
+def test_routing_bit_exact_workload_logits(name):
+    """Full-size workloads: the oracle computes the fp32 logits in fp64 from the seeded
+    X, W_r and b_r; the GPU routing kernels are fed those logits."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, "cuda", weights=False)
+    _, L32 = O.router_logits(to_np(inp["x"]), to_np(inp["w_r"]),
+                             None if inp["b_r"] is None else to_np(inp["b_r"]))
+    C = O.capacity(wl.T, wl.E, wl.capacity_factor)
+    g = _routing_only(wl.T, wl.E, wl.K, C, L32)
+    plan = _check_routing(g, L32, wl.K, C, wl.E, alpha=wl.alpha)
+    if C >= 0:
+        assert (plan["kept"] <= C).all()
+    if name == "long":
+        share = float(plan["counts"].max()) / (wl.T * wl.K)
+        assert 0.37 <= share <= 0.43, share
+
+
+def test_scan_spans_many_blocks_all_one_expert():
+    """Every assignment to one expert (collapsed router): the look-back carries one
+    expert's running count across all scan blocks."""
+    T, E, K = 20000, 16, 2
+    L32 = np.zeros((T, E), dtype=np.float32)
+    L32[:, 3] = 5.0
+    L32[:, 7] = 4.0
+    C = 1000
+    g = _routing_only(T, E, K, C, L32)
+    _check_routing(g, L32, K, C, E)
+    assert g["offsets"].tolist()[-1] == 2 * C
+
+
+def test_scan_timeout_is_reported_and_recovers():
+    """A scan block withholds its published counts (test hook); its successor's bounded
+    wait runs out, the kernel still terminates, and the status word says so.  The next
+    call is unaffected."""
+    T, E, K = 6000, 8, 2            # 12000 assignments -> 3 scan blocks
+    L32 = make_logits(T, E, seed=3).numpy()
+    N.arm_scan_timeout(0, 2000)
+    cfg = N.make_config(T, 8, E, K, 8, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    logits = torch.from_numpy(L32).cuda()
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    slot = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    src = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    N.route(cfg, None, None, None, logits, ids, w, ws)
+    N.dispatch(cfg, None, ids, counts, offsets, slot, src, None, ws)
+    assert N.sync_status(ws) == 4  # MOE_ERR_TIMEOUT
+    assert N.sync_status(ws) == 0  # cleared
+    g = _routing_only(T, E, K, -1, L32)
+    _check_routing(g, L32, K, -1, E)
+
+
+def test_out_of_range_expert_id_reported():
+    T, E, K = 100, 8, 2
+    cfg = N.make_config(T, 8, E, K, 8, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    ids = torch.randint(0, E, (T, K), dtype=torch.int32, device="cuda")
+    ids[5, 1] = E
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    slot = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    src = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    N.dispatch(cfg, None, ids, counts, offsets, slot, src, None, ws)
+    assert N.sync_status(ws) == 5  # MOE_ERR_DEVICE
+    assert int(slot[5, 1].item()) == -1
+    assert int(counts.sum().item()) == T * K - 1
+
+
+# ------------------------------------------------------------------ whole layer
+def _layer_case(wl: Workload, seed=0, logits_from_oracle=False, renorm=False):
+    inp = make_inputs(wl, "cuda", seed=seed)
+    layer = MoELayer.from_workload(wl, inp, renormalize=renorm)
+    x_np = to_np(inp["x"])
+    b_np = None if inp["b_r"] is None else to_np(inp["b_r"])
+    _, L32 = O.router_logits(x_np, to_np(inp["w_r"]), b_np)
+    layer.forward(inp["x"], logits_in=torch.from_numpy(L32).cuda() if logits_from_oracle else None)
+    layer.check_device_status()
+    torch.cuda.synchronize()
+    shared = (to_np(inp["w1s"])[0], to_np(inp["w2s"])[0]) if wl.shared else None
+    C = O.capacity(wl.T, wl.E, wl.capacity_factor)
+    ref = O.moe_forward(x_np, to_np(inp["w_r"]), b_np, to_np(inp["w1"]), to_np(inp["w2"]),
+                        wl.K, C, wl.alpha, renormalize=renorm, shared=shared,
+                        logits32=L32 if logits_from_oracle else None)
+    return layer, ref, L32, C
+
+
+SMALL = [
+    Workload("tiny", 256, 128, 8, 2, 512, "f32", 1.25),
+    Workload("f32_ragged", 203, 36, 5, 3, 92, "f32", 1.1),
+    Workload("bf16_small", 300, 256, 8, 2, 384, "bf16", 1.25),
+    Workload("bf16_ragged", 517, 136, 16, 4, 200, "bf16", 0.8),
+    Workload("bf16_bias_shared", 333, 128, 32, 8, 96, "bf16", None, bias="normal", shared=True),
+    Workload("bf16_zipf", 1000, 192, 8, 2, 256, "bf16", 1.0, bias="zipf"),
+    Workload("bf16_single_expert", 130, 64, 1, 1, 64, "bf16", None),
+    Workload("bf16_k_eq_e", 90, 64, 4, 4, 128, "bf16", 1.0),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_layer_end_to_end_small(wl):
+    layer, ref, L32, C = _layer_case(wl)
+    # router logits themselves
+    Lg = to_np(layer.logits)
+    assert np.max(np.abs(Lg - L32) / (1 + np.abs(L32))) <= (1e-5 if wl.dtype == "bf16" else 1e-5)
+    keep = comparable_tokens(L32, ref["ids"], wl.K, C)
+    assert keep.mean() > 0.5
+    y = to_np(layer.y)
+    err = rel_rms_err(y[keep], ref["y"][keep])
+    assert err <= TOL[wl.dtype], err
+    assert np.array_equal(to_np(layer.ids)[keep], ref["ids"][keep])
+
+
+@pytest.mark.parametrize("wl", SMALL[:6], ids=[w.name for w in SMALL[:6]])
+def test_layer_stages_with_oracle_logits(wl):
+    """Fed the oracle's logits, every stage matches: routing bit-exact, packed rows
+    exact, h and y_perm within tolerance, combine within tolerance, aux stats."""
+    layer, ref, L32, C = _layer_case(wl, logits_from_oracle=True)
+    R = ref["R"]
+    assert np.array_equal(to_np(layer.ids), ref["ids"])
+    assert np.array_equal(to_np(layer.offsets), ref["offsets"])
+    assert np.array_equal(to_np(layer.slot), ref["slot"].reshape(wl.T, wl.K))
+    assert np.array_equal(to_np(layer.src)[:R], ref["src"])
+    assert np.array_equal(to_np(layer.x_perm)[:R], ref["x_perm"])
+    tol = TOL[wl.dtype]
+    assert_rounded_to(to_np(layer.h)[:R], ref["h"], wl.dtype)
+    assert rel_rms_err(to_np(layer.y_perm)[:R], ref["y_perm"]) <= tol
+    assert rel_rms_err(to_np(layer.y), ref["y"]) <= tol
+    assert np.max(np.abs(to_np(layer.P) - ref["P"]) / ref["P"]) <= 1e-5
+    assert abs(layer.l_aux.item() - ref["l_aux"]) <= 1e-5 * ref["l_aux"]
+
+
+def test_capacity_zero_drops_everything():
+    wl = Workload("cap0", 64, 64, 8, 2, 64, "bf16", 0.1)  # C = floor(64*0.1/8) = 0
+    layer, ref, L32, C = _layer_case(wl)
+    assert C == 0
+    assert int(layer.offsets[-1].item()) == 0
+    assert (to_np(layer.slot) == -1).all()
+    assert (to_np(layer.y) == 0).all()
+
+
+def test_empty_batch():
+    wl = Workload("empty", 0, 64, 8, 2, 64, "bf16", 1.0)
+    inp = make_inputs(wl, "cuda")
+    layer = MoELayer.from_workload(wl, inp)
+    layer.forward(inp["x"])
+    layer.check_device_status()
+    assert (to_np(layer.counts) == 0).all() and (to_np(layer.offsets) == 0).all()
+    assert (to_np(layer.f) == 0).all() and layer.l_aux.item() == 0.0
+
+
+def test_determinism_two_runs():
+    wl = SMALL[3]
+    inp = make_inputs(wl, "cuda")
+    layer = MoELayer.from_workload(wl, inp)
+    layer.forward(inp["x"])
+    y1 = layer.y.clone()
+    p1 = layer.P.clone()
+    layer.forward(inp["x"])
+    assert torch.equal(y1, layer.y) and torch.equal(p1, layer.P)
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _sampled_full_check(name, n_tokens=48, seed=0):
+    """Full-size workload in the bench's launch configuration: routing in full against
+    the oracle's own logits (near ties excluded), the expert FFN on every row of two
+    experts and the layer output on a token sample."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, "cuda")
+    layer = MoELayer.from_workload(wl, inp)
+    layer.forward(inp["x"])
+    layer.check_device_status()
+    torch.cuda.synchronize()
+    x_np = to_np(inp["x"])
+    b_np = None if inp["b_r"] is None else to_np(inp["b_r"])
+    _, L32 = O.router_logits(x_np, to_np(inp["w_r"]), b_np)
+    C = O.capacity(wl.T, wl.E, wl.capacity_factor)
+    ids = O.top_k(L32, wl.K)
+    plan = O.dispatch_plan(ids, wl.E, C)
+    keep = comparable_tokens(L32, ids, wl.K, C)
+    g_ids = to_np(layer.ids)
+    assert np.array_equal(g_ids[keep], ids[keep])
+    if keep.all():
+        assert np.array_equal(to_np(layer.offsets), plan["offsets"])
+        assert np.array_equal(to_np(layer.slot), plan["slot"].reshape(wl.T, wl.K))
+    tol = TOL[wl.dtype]
+    # two experts' packed rows in full (GPU rows of those experts are the oracle's rows
+    # whenever routing agrees; compare via the oracle's own packing)
+    offs = plan["offsets"]
+    g_offs = to_np(layer.offsets)
+    for e in (0, wl.E - 1):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi == lo or not np.array_equal(g_offs[e:e + 2], offs[e:e + 2]):
+            continue
+        rows = plan["src"][lo:hi] // wl.K
+        y_ref, h_ref = O.expert_ffn(x_np[rows], to_np(inp["w1"][e]), to_np(inp["w2"][e]))
+        glo, ghi = int(g_offs[e]), int(g_offs[e + 1])
+        assert np.array_equal(to_np(layer.src)[glo:ghi] // wl.K, rows)
+        assert_rounded_to(to_np(layer.h[glo:ghi]), h_ref, wl.dtype)
+        assert rel_rms_err(to_np(layer.y_perm[glo:ghi]), y_ref) <= tol
+    # token sample: the oracle evaluates each sampled token's kept experts one by one
+    rng = np.random.default_rng(seed)
+    cand = np.nonzero(keep)[0]
+    toks = rng.choice(cand, size=min(n_tokens, cand.size), replace=False)
+    w = O.routing_weights(O.softmax(L32[toks]), ids[toks])
+    keepmask = plan["keep"].reshape(wl.T, wl.K)[toks]
+    need = sorted({int(e) for t_i in range(len(toks)) for k, e in enumerate(ids[toks[t_i]])
+                   if keepmask[t_i, k]})
+    Y = np.zeros((len(toks), wl.d))
+    for e in need:
+        sel = [(t_i, k) for t_i in range(len(toks)) for k in range(wl.K)
+               if ids[toks[t_i], k] == e and keepmask[t_i, k]]
+        rows = np.array([toks[t_i] for t_i, _ in sel])
+        ye, _ = O.expert_ffn(x_np[rows], to_np(inp["w1"][e]), to_np(inp["w2"][e]))
+        for j, (t_i, k) in enumerate(sel):
+            Y[t_i] += w[t_i, k] * ye[j]
+    if wl.shared:
+        Y += O.dense_ffn(x_np[toks], to_np(inp["w1s"][0]), to_np(inp["w2s"][0]))
+    err = rel_rms_err(to_np(layer.y)[toks], Y)
+    assert err <= tol, err
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3"])
+def test_full_size_sampled(name):
+    _sampled_full_check(name)

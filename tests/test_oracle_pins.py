@@ -329,3 +329,8 @@ def test_all_subsets_topk_small():
                        key=lambda s: (sum(vals[i] for i in s), [-i for i in s]))
             assert sorted(got) == list(best)
             assert [vals[i] for i in got] == sorted([vals[i] for i in got], reverse=True)
+
+
+def test_aux_empty_batch_is_zero():
+    f, P, L = O.aux_stats(np.zeros((0, 2), np.int32), np.zeros((0, 4)), 4, 0.01)
+    assert f.tolist() == [0.0] * 4 and P.tolist() == [0.0] * 4 and L == 0.0
