@@ -24,7 +24,7 @@
  *   call only enqueues work on it and returns without synchronising the host.
  * - The returned status covers argument validation and kernel-launch errors.  Errors
  *   that arise on the device (an expert id out of range, a bounded wait that gave up,
- *   packed rows exceeding the buffer) are recorded in a status word inside `ws`;
+ *   packed rows exceeding the buffer, an fp16 overflow) are recorded in a status word inside `ws`;
  *   moe_sync_status() synchronises the stream, returns and clears it.
  * - Activations and weights have the config's dtype (fp32 or bf16); logits, routing
  *   weights, biases, expert outputs (y_perm, y_shared) and statistics are fp32;
@@ -55,7 +55,7 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement */
   MOE_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
   MOE_ERR_TIMEOUT = 4,      /* (device) a bounded spin-wait gave up */
-  MOE_ERR_DEVICE = 5        /* (device) out-of-range expert id or packed-row overflow */
+  MOE_ERR_DEVICE = 5        /* (device) bad expert id, packed-row or fp16 overflow */
 } moe_status_t;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
@@ -113,8 +113,13 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
  *   x_perm   [rows_cap, d] dtype in; group g owns rows [offsets[g], offsets[g+1])
  *   offsets  [n_groups+1] int32 DEVICE pointer (read on the device; no host sync)
  *   w1       [n_groups, F, d] dtype
- *   h        [rows_cap, F] dtype out: h = GELU(x_perm . W1[g]^T), exact erf form,
- *            fp32 accumulation, rounded once to dtype.
+ *   h        [rows_cap, F] out: h = GELU(x_perm . W1[g]^T), exact erf form, fp32
+ *            accumulation, rounded once -- to fp32 for MOE_F32 layers and to FP16 for
+ *            MOE_BF16 layers (11 significant bits instead of bf16's 8, which keeps the
+ *            layer output within its error bound; |h| > 65504 is reported as
+ *            MOE_ERR_DEVICE by moe_sync_status).
+ * MOE_BF16 runs on the tcgen05 tensor cores (TMA-fed, TMEM accumulators); MOE_F32 on
+ * the CUDA cores (fp32 products).
  * n_groups = E for the routed experts; n_groups = 1 with offsets {0, T} and x in place
  * of x_perm runs a shared (always-on) expert over all tokens. */
 moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
@@ -122,7 +127,9 @@ moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int3
                            void* ws, void* stream);
 
 /* Step 3b -- grouped second expert Linear: y_perm = h . W2[g]^T.
- *   h [rows_cap, F] dtype; w2 [n_groups, d, F] dtype;
+ *   h [rows_cap, F] as written by moe_expert_up (fp32, or fp16 for MOE_BF16 layers);
+ *   w2 [n_groups, d, F]: fp32 for MOE_F32 layers; FP16 for MOE_BF16 layers (convert the
+ *   bf16 weights once with moe_bf16_to_f16);
  *   y_perm [rows_cap, d] FP32 out (expert outputs stay fp32 until the combine rounds
  *   the layer output once). */
 moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t* offsets,
@@ -151,6 +158,12 @@ moe_status_t moe_combine(const moe_config* cfg, const void* y_perm, const int32_
  * call that used the same ws. */
 moe_status_t moe_aux_stats(const moe_config* cfg, const int32_t* counts, const void* ws,
                            float* f, float* P, float* l_aux, void* stream);
+
+/* Convert n bf16 values to fp16 (n a multiple of 8), e.g. the second expert Linear's
+ * weights of a MOE_BF16 layer.  Magnitudes in [2^-17, 65504] convert exactly, smaller
+ * ones round at 2^-25; larger ones are reported as MOE_ERR_DEVICE in the status word
+ * of `ws` (any workspace of this library). */
+moe_status_t moe_bf16_to_f16(const void* src, void* dst, int64_t n, void* ws, void* stream);
 
 /* Synchronise `stream`, then return and clear the device status word in `ws`
  * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE), or MOE_ERR_CUDA if a kernel failed. */

@@ -65,6 +65,11 @@ def widen(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
 
 
+def linear(x, w) -> np.ndarray:
+    """A Linear layer without bias in fp64, weights stored [out, in]: x . W^T."""
+    return widen(x) @ widen(w).T
+
+
 # --------------------------------------------------------------------------------------
 # Router: [EPM] "MoE Layer Structure" -- Router (Linear d -> N_experts).
 # --------------------------------------------------------------------------------------
@@ -73,7 +78,7 @@ def router_logits(x, w_r, b_r=None):
 
     x: [T, d]; w_r: [E, d] (Linear layout, out x in); b_r: [E] or None.
     """
-    L = widen(x) @ widen(w_r).T
+    L = linear(x, w_r)
     if b_r is not None:
         L = L + widen(b_r)[None, :]
     return L, L.astype(np.float32)
@@ -184,8 +189,8 @@ def expert_ffn(x_rows, w1, w2):
 
     x_rows: [n, d]; w1: [F, d]; w2: [d, F] (Linear layouts).  Returns (y [n,d], h [n,F]).
     """
-    h = gelu(widen(x_rows) @ widen(w1).T)
-    y = h @ widen(w2).T
+    h = gelu(linear(x_rows, w1))
+    y = linear(h, w2)
     return y, h
 
 

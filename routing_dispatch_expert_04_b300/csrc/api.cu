@@ -27,6 +27,16 @@ cudaError_t launch_simt_grouped(int dtype, const void* A, const void* B, void* C
                                 bool gelu, uint32_t* hdr, cudaStream_t st);
 cudaError_t launch_simt_router(int dtype, const void* x, const void* w_r, const float* b_r,
                                float* logits, int T, int E, int d, uint32_t* hdr, cudaStream_t st);
+cudaError_t launch_tc_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets, int G,
+                         int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                         cudaStream_t st);
+cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
+                           int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                           cudaStream_t st);
+cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, float* logits, int T,
+                             int E, int d, uint32_t* hdr, int num_sms, cudaStream_t st);
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, int64_t n, uint32_t* hdr, int num_sms,
+                               cudaStream_t st);
 
 static std::atomic<uint64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -35,9 +45,15 @@ static std::atomic<int> g_skip_block{-1};
 static std::atomic<int> g_spin_limit{1 << 21};
 
 static int num_sms() {
-  int dev = 0, n = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 148;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -89,17 +105,20 @@ moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, co
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
+  if (c.T == 0) return MOE_OK;  // nothing is read or written
   if (!logits || !topk_ids || !topk_w || !ws) return MOE_ERR_INVALID;
   if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(ws))
     return MOE_ERR_INVALID;
   if (x != nullptr && (w_r == nullptr || !aligned16(x) || !aligned16(w_r))) return MOE_ERR_INVALID;
   if (b_r != nullptr && !aligned16(b_r)) return MOE_ERR_INVALID;
-  if (c.T == 0) return MOE_OK;
   cudaStream_t st = (cudaStream_t)stream;
   const WsLayout L = ws_layout(c);
   uint32_t* hdr = (uint32_t*)ws;
   if (x != nullptr) {
-    s = cuda_status(launch_simt_router(c.dtype, x, w_r, b_r, logits, c.T, c.E, c.d, hdr, st));
+    if (c.dtype == MOE_BF16)
+      s = cuda_status(launch_tc_router(x, w_r, b_r, logits, c.T, c.E, c.d, hdr, num_sms(), st));
+    else
+      s = cuda_status(launch_simt_router(c.dtype, x, w_r, b_r, logits, c.T, c.E, c.d, hdr, st));
     if (s != MOE_OK) return s;
   }
   return cuda_status(launch_softmax_topk(logits, c.T, c.E, c.K, c.renormalize, topk_ids, topk_w,
@@ -112,14 +131,16 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
-  if (!topk_ids || !counts || !offsets || !slot || !src || !ws) return MOE_ERR_INVALID;
-  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID;
-  if (!aligned16(topk_ids) || !aligned16(counts) || !aligned16(offsets) || !aligned16(slot) ||
-      !aligned16(src) || !aligned16(ws))
-    return MOE_ERR_INVALID;
-  if (x != nullptr && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
   const int A = c.T * c.K;
+  if (!counts || !offsets || !aligned16(counts) || !aligned16(offsets)) return MOE_ERR_INVALID;
+  if (A > 0) {
+    if (!topk_ids || !slot || !src || !ws) return MOE_ERR_INVALID;
+    if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID;
+    if (!aligned16(topk_ids) || !aligned16(slot) || !aligned16(src) || !aligned16(ws))
+      return MOE_ERR_INVALID;
+    if (x != nullptr && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID;
+  }
   if (A == 0) {
     s = cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, st));
     if (s != MOE_OK) return s;
@@ -147,10 +168,12 @@ static moe_status_t check_ffn_args(const moe_config* cfg, const void* in, const 
                                    const void* out, const void* ws) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
+  if (n_groups < 1 || n_groups > 256 || rows_cap < 0) return MOE_ERR_INVALID;
+  if (rows_cap == 0) return MOE_OK;  // nothing is read or written
+  if (rows_cap >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
   if (!in || !offsets || !w || !out || !ws) return MOE_ERR_INVALID;
   if (!aligned16(in) || !aligned16(w) || !aligned16(out) || !aligned16(ws) || ((uintptr_t)offsets & 3))
     return MOE_ERR_INVALID;
-  if (n_groups < 1 || n_groups > 256 || rows_cap < 0) return MOE_ERR_INVALID;
   return MOE_OK;
 }
 
@@ -161,6 +184,9 @@ moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int3
   if (s != MOE_OK) return s;
   if (rows_cap == 0) return MOE_OK;
   const moe_config& c = *cfg;
+  if (c.dtype == MOE_BF16)
+    return cuda_status(launch_tc_up(x_perm, w1, h, offsets, n_groups, c.F, c.d, rows_cap,
+                                    (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
   return cuda_status(launch_simt_grouped(c.dtype, x_perm, w1, h, offsets, n_groups, c.F, c.d,
                                          rows_cap, true, (uint32_t*)ws, (cudaStream_t)stream));
 }
@@ -172,6 +198,9 @@ moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t
   if (s != MOE_OK) return s;
   if (rows_cap == 0) return MOE_OK;
   const moe_config& c = *cfg;
+  if (c.dtype == MOE_BF16)
+    return cuda_status(launch_tc_down(h, w2, y_perm, offsets, n_groups, c.d, c.F, rows_cap,
+                                      (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
   return cuda_status(launch_simt_grouped(c.dtype, h, w2, y_perm, offsets, n_groups, c.d, c.F,
                                          rows_cap, false, (uint32_t*)ws, (cudaStream_t)stream));
 }
@@ -189,10 +218,10 @@ moe_status_t moe_combine(const moe_config* cfg, const void* y_perm, const int32_
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
+  if (c.T == 0) return MOE_OK;  // nothing is read or written
   if (!y_perm || !slot || !topk_w || !y) return MOE_ERR_INVALID;
   if (!aligned16(y_perm) || !aligned16(slot) || !aligned16(topk_w) || !aligned16(y)) return MOE_ERR_INVALID;
   if (y_shared != nullptr && !aligned16(y_shared)) return MOE_ERR_INVALID;
-  if (c.T == 0) return MOE_OK;
   return cuda_status(launch_combine(c.dtype, y_perm, slot, topk_w, y_shared, y, c.T, c.d, c.K,
                                     num_sms(), (cudaStream_t)stream));
 }
@@ -211,6 +240,13 @@ moe_status_t moe_aux_stats(const moe_config* cfg, const int32_t* counts, const v
                                 c.E, c.T, c.K, c.alpha, f, P, l_aux, (cudaStream_t)stream));
 }
 
+moe_status_t moe_bf16_to_f16(const void* src, void* dst, int64_t n, void* ws, void* stream) {
+  if (n < 0 || (n % 8) != 0) return MOE_ERR_INVALID;
+  if (n == 0) return MOE_OK;
+  if (!src || !dst || !ws || !aligned16(src) || !aligned16(dst) || !aligned16(ws)) return MOE_ERR_INVALID;
+  return cuda_status(launch_bf16_to_f16(src, dst, n, (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
+}
+
 moe_status_t moe_sync_status(void* ws, void* stream) {
   if (ws == nullptr) return MOE_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
@@ -224,7 +260,7 @@ moe_status_t moe_sync_status(void* ws, void* stream) {
     if (s != MOE_OK) return s;
   }
   if (word & DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
-  if (word & (DEV_ERR_BAD_ID | DEV_ERR_OVERFLOW)) return MOE_ERR_DEVICE;
+  if (word & (DEV_ERR_BAD_ID | DEV_ERR_OVERFLOW | DEV_ERR_RANGE)) return MOE_ERR_DEVICE;
   return MOE_OK;
 }
 

@@ -14,6 +14,7 @@ namespace moe {
 constexpr uint32_t DEV_ERR_TIMEOUT = 1u;   // a bounded spin-wait gave up
 constexpr uint32_t DEV_ERR_BAD_ID = 2u;    // expert id outside [0, E)
 constexpr uint32_t DEV_ERR_OVERFLOW = 4u;  // offsets[G] larger than the row buffer
+constexpr uint32_t DEV_ERR_RANGE = 8u;     // a value outside the fp16 range was stored
 
 __device__ __forceinline__ void raise_error(uint32_t* status, uint32_t bit) {
   atomicOr(status, bit);

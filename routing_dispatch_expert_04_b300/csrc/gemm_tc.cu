@@ -1,0 +1,438 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// C[r, n] = epi( sum_k A[r, k] * B[g*N + n, k] ) for the rows r of group g,
+// r in [offsets[g], offsets[g+1]).  A is the packed expert input (K-major, row pitch Kd),
+// B the stacked expert weights in Linear layout [G*N, Kd].  This is the expert FFN of
+// "Expert Parallelism (MoE)", "MoE Layer Structure" (each expert applies Linear(d -> 4d)
+// -> GELU -> Linear(4d -> d)) run for all experts in one launch ("Expert Parallelism
+// (EP)", step 3: expert GEMMs compute locally).
+//
+// Design (one CTA per SM, persistent):
+//   warp 0      TMA producer: per k-block, one 128x64 A box and one BNx64 B box into a
+//               STAGES-deep ring of 128-byte-swizzled shared-memory stages;
+//   warp 1      owns TMEM (2 x BN fp32 columns: double-buffered accumulators) and one
+//               elected thread issues tcgen05.mma (M=128, N=BN, K=16) and commits;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused GELU (exact erf) or
+//               plain/bias, conversion and masked stores.  Overlaps the next tile's
+//               main loop through the second accumulator.
+// Tiles are (group, n-tile, m-tile) with m fastest, so CTAs running at the same time
+// share one weight box through L2.  The per-group row ranges are read from `offsets` on
+// the device (no host synchronisation); the last m-tile of a group may run past the
+// group's rows (those rows are loaded but never stored) and past the buffer (TMA fills
+// zeros).  Every mbarrier wait is bounded: after WAIT_LIMIT_NS the CTA records a timeout
+// in the status word, every role leaves its loop, in-flight copies and MMAs are awaited
+// (bounded), TMEM is freed and the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+using namespace tc;
+
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 64;            // 64 bf16/fp16 = one 128-byte swizzle row
+constexpr int TC_THREADS = 192;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
+
+enum { TC_EPI_GELU_F16 = 0, TC_EPI_F32 = 1, TC_EPI_BIAS_F32 = 2 };
+
+struct TcArgs {
+  const int32_t* offsets;  // [G+1] device, or nullptr: one group of M rows
+  int G, M, N, Kd;
+  int64_t rows_cap;
+  void* out;               // [rows_cap, ldo]
+  int ldo;
+  const float* bias;       // [N] or nullptr
+  uint32_t* hdr;           // status word
+};
+
+template <int BN, int STAGES>
+struct TcLayout {
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;
+  static constexpr int B_BYTES = BN * TC_BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int B_OFF = STAGES * A_BYTES;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NBAR = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], done
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int GRP_OFF = MISC_OFF + 16;
+  static constexpr int TOTAL = GRP_OFF + 4 * 257 * 4;
+  static constexpr int ALLOC = TOTAL + 1024;
+  static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
+                                       : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+};
+
+// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           uint32_t* hdr) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      raise_error(hdr, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Wait used only while draining after an abort: ignores the abort flag, shorter limit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > DRAIN_LIMIT_NS) return;
+  }
+}
+
+struct TileInfo {
+  int g;
+  int row0;
+  int rowend;
+  int n0;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int t, int G, const int* s_lo, const int* s_hi,
+                                                const int* s_mt, const int* s_tpre, int BN) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_tpre[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int g = lo;
+  const int local = t - s_tpre[g];
+  const int mt = s_mt[g];
+  TileInfo ti;
+  ti.g = g;
+  ti.row0 = s_lo[g] + (local % mt) * TC_BM;
+  ti.rowend = s_hi[g];
+  ti.n0 = (local / mt) * BN;
+  return ti;
+}
+
+__device__ __forceinline__ float gelu_exact(float v) {
+  return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
+}
+
+template <int BN, int STAGES, int EPI, bool F16IN>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                       const __grid_constant__ CUtensorMap tmap_b, const TcArgs args) {
+  using Lay = TcLayout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + Lay::BAR_OFF);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* done = bars + 2 * STAGES + 4;
+  uint32_t* s_tmem = (uint32_t*)(smem + Lay::MISC_OFF);
+  volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
+  int* s_lo = (int*)(smem + Lay::GRP_OFF);
+  int* s_hi = s_lo + 257;
+  int* s_mt = s_hi + 257;
+  int* s_tpre = s_mt + 257;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = args.G;
+  const int n_tiles = (args.N + BN - 1) / BN;
+  const int nkb = (args.Kd + TC_BK - 1) / TC_BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(done, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 0) {
+    // per-group row ranges (clamped to the buffer), m-tiles and tile prefix
+    int carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int g = base + lane;
+      int lo = 0, hi = 0, mt = 0;
+      if (g < G) {
+        if (args.offsets == nullptr) {
+          lo = 0;
+          hi = args.M;
+        } else {
+          lo = args.offsets[g];
+          hi = args.offsets[g + 1];
+        }
+        if (hi > args.rows_cap) {
+          raise_error(args.hdr, DEV_ERR_OVERFLOW);
+          hi = (int)args.rows_cap;
+        }
+        if (lo < 0) lo = 0;
+        if (lo > hi) lo = hi;
+        mt = (hi - lo + TC_BM - 1) / TC_BM;
+        s_lo[g] = lo;
+        s_hi[g] = hi;
+        s_mt[g] = mt;
+      }
+      int v = mt * n_tiles;  // inclusive warp scan of tiles
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (g < G) s_tpre[g + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_tpre[0] = 0;
+  } else if (warp == 1) {
+    tmem_alloc(s_tmem, Lay::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total = s_tpre[G];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(t, G, s_lo, s_hi, s_mt, s_tpre, BN);
+        const int brow = ti.g * args.N + ti.n0;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * Lay::A_BYTES;
+          uint8_t* sb = smem + Lay::B_OFF + s * Lay::B_BYTES;
+          mbar_arrive_expect_tx(&full[s], Lay::STAGE_BYTES);
+          tma_load_2d(sa, &tmap_a, &full[s], kb * TC_BK, ti.row0);
+          tma_load_2d(sb, &tmap_b, &full[s], kb * TC_BK, brow);
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let the copies already in flight land before shared memory goes away
+        for (int i = 0; i < STAGES && i < issued; ++i) {
+          if (--s < 0) {
+            s = STAGES - 1;
+            ph ^= 1u;
+          }
+          drain_wait(&full[s], ph);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t IDESC = F16IN ? (idesc_bf16_f32(TC_BM, BN) & ~((7u << 7) | (7u << 10)))
+                                       : idesc_bf16_f32(TC_BM, BN);
+      int s = 0;
+      uint32_t ph = 0, acc = 0, aph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_phase(&full[s], ph, s_abort, args.hdr)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
+          const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < TC_BK / 16; ++k) {
+            mma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), IDESC,
+                     (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1u;
+        if (acc == 0) aph ^= 1u;
+      }
+      // every MMA issued by this thread has completed once `done` flips
+      mma_commit(done);
+      drain_wait(done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_in_tile = q * 32 + lane;
+    uint32_t acc = 0, aph = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile(t, G, s_lo, s_hi, s_mt, s_tpre, BN);
+      if (!wait_phase(&tfull[acc], aph, s_abort, args.hdr)) break;
+      tc_fence_after();
+      const int row = ti.row0 + r_in_tile;
+      const bool valid = row < ti.rowend;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = ti.n0 + c * 32;
+        if (col0 >= args.N) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
+        tmem_ld_wait();
+        if (!valid) continue;
+        if (EPI == TC_EPI_GELU_F16) {
+          __half* out = (__half*)args.out + (size_t)row * args.ldo + col0;
+          bool bad = false;
+#pragma unroll
+          for (int v8 = 0; v8 < 4; ++v8) {
+            if (col0 + v8 * 8 >= args.N) break;
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float a = gelu_exact(__uint_as_float(r[v8 * 8 + 2 * i]));
+              const float b = gelu_exact(__uint_as_float(r[v8 * 8 + 2 * i + 1]));
+              bad |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
+              __half2 h2 = __floats2half2_rn(a, b);
+              w[i] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            st_v4(out + v8 * 8, make_uint4(w[0], w[1], w[2], w[3]));
+          }
+          if (bad) raise_error(args.hdr, DEV_ERR_RANGE);
+        } else if (EPI == TC_EPI_F32) {
+          float* out = (float*)args.out + (size_t)row * args.ldo + col0;
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) {
+            if (col0 + v4 * 4 >= args.N) break;
+            st_v4(out + v4 * 4, make_uint4(r[v4 * 4], r[v4 * 4 + 1], r[v4 * 4 + 2], r[v4 * 4 + 3]));
+          }
+        } else {
+          float* out = (float*)args.out + (size_t)row * args.ldo;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = col0 + i;
+            if (col < args.N)
+              out[col] = __uint_as_float(r[i]) + (args.bias != nullptr ? args.bias[col] : 0.f);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Lay::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+// 2-D tensor map of a row-major [outer, inner] 16-bit matrix, box [box_outer, 64].
+static bool make_map(CUtensorMap* m, const void* base, bool f16, uint64_t inner, uint64_t outer,
+                     uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, int EPI, bool F16IN>
+static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int num_sms,
+                             cudaStream_t st) {
+  using Lay = TcLayout<BN, STAGES>;
+  static bool attr_set = false;
+  auto kern = tc_grouped_gemm_kernel<BN, STAGES, EPI, F16IN>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap ma, mb;
+  const int64_t a_rows = a.rows_cap > 0 ? a.rows_cap : 1;
+  if (!make_map(&ma, A, F16IN, (uint64_t)a.Kd, (uint64_t)a_rows, TC_BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, B, F16IN, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN)) return cudaErrorInvalidValue;
+  const int64_t n_tiles = (a.N + BN - 1) / BN;
+  const int64_t m_bound = (a.rows_cap + TC_BM - 1) / TC_BM + (a.offsets ? a.G : 0);
+  int64_t grid = m_bound * n_tiles;
+  if (grid > num_sms) grid = num_sms;
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, TC_THREADS, Lay::ALLOC, st>>>(ma, mb, a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// First expert Linear, bf16 in, GELU fused, fp16 out: h[r] = GELU(x_perm[r] . W1[g]^T).
+cudaError_t launch_tc_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets, int G,
+                         int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                         cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr};
+  return launch_tc<256, 4, TC_EPI_GELU_F16, false>(x_perm, w1, a, num_sms, st);
+}
+
+// Second expert Linear, fp16 in, fp32 out: y_perm[r] = h[r] . W2[g]^T.
+cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
+                           int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                           cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr};
+  return launch_tc<256, 4, TC_EPI_F32, true>(h, w2h, a, num_sms, st);
+}
+
+// Router Linear, bf16 in, fp32 logits + bias: logits[t] = x[t] . W_r^T + b_r.
+cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, float* logits, int T,
+                             int E, int d, uint32_t* hdr, int num_sms, cudaStream_t st) {
+  TcArgs a{nullptr, 1, T, E, d, (int64_t)T, logits, E, b_r, hdr};
+  // the epilogue reads TMEM 32 columns at a time, so the narrowest tile is 32 wide
+  if (E <= 32) return launch_tc<32, 8, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
+  if (E <= 64) return launch_tc<64, 8, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
+  if (E <= 128) return launch_tc<128, 6, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
+  return launch_tc<256, 4, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
+}
+
+}  // namespace moe

@@ -28,8 +28,8 @@ class MoELayer:
         self.T, self.d, self.E, self.K, self.F = T, d, E, K, F
         self.dtype = torch.float32 if dtype == "f32" else torch.bfloat16
         self.device = torch.device(device)
-        self.w_r, self.b_r, self.w1, self.w2 = w_r, b_r, w1, w2
-        self.w1s, self.w2s = w1s, w2s
+        self.w_r, self.b_r, self.w1 = w_r, b_r, w1
+        self.w1s = w1s
         self.rows_cap = N.rows_capacity(self.cfg)
         R = max(self.rows_cap, 1)
         dev, dt = self.device, self.dtype
@@ -43,17 +43,33 @@ class MoELayer:
         self.slot = torch.empty((T, K), dtype=i32, device=dev)
         self.src = torch.empty(R, dtype=i32, device=dev)
         self.x_perm = torch.empty((R, d), dtype=dt, device=dev)
-        self.h = torch.empty((R, F), dtype=dt, device=dev)
+        # the intermediate activation is fp16 for bf16 layers (see moe_expert_up)
+        self.h_dtype = torch.float16 if dtype == "bf16" else torch.float32
+        self.h = torch.empty((R, F), dtype=self.h_dtype, device=dev)
         self.y_perm = torch.empty((R, d), dtype=f32, device=dev)
         self.y = torch.empty((T, d), dtype=dt, device=dev)
         self.f = torch.empty(E, dtype=f32, device=dev)
         self.P = torch.empty(E, dtype=f32, device=dev)
         self.l_aux = torch.empty(1, dtype=f32, device=dev)
+        self.w2 = self._down_weights(w2)
         self.shared = w1s is not None
+        self.w2s = self._down_weights(w2s) if self.shared else None
         if self.shared:
             self.shared_offsets = torch.tensor([0, T], dtype=i32, device=dev)
-            self.h_s = torch.empty((max(T, 1), F), dtype=dt, device=dev)
+            self.h_s = torch.empty((max(T, 1), F), dtype=self.h_dtype, device=dev)
             self.y_s = torch.empty((max(T, 1), d), dtype=f32, device=dev)
+
+    def _down_weights(self, w2):
+        """Second-Linear weights in the operand type the kernels take: an fp16 copy of bf16
+        weights (converted once by the library), fp32 weights as they are."""
+        if w2.dtype != torch.bfloat16:
+            return w2
+        out = torch.empty(w2.shape, dtype=torch.float16, device=w2.device)
+        N.bf16_to_f16(w2, out, self.ws)
+        st = N.sync_status(self.ws)
+        if st != 0:
+            raise N.MoeError("moe_bf16_to_f16", st)
+        return out
 
     @classmethod
     def from_workload(cls, wl, inputs, device="cuda", renormalize=False):

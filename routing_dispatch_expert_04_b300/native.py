@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_E
 
 EXPORTS = ("moe_workspace_size", "moe_rows_capacity", "moe_route", "moe_dispatch",
            "moe_expert_up", "moe_expert_down", "moe_grouped_ffn", "moe_combine",
-           "moe_aux_stats", "moe_sync_status", "moe_status_string", "moe_launch_count",
+           "moe_aux_stats", "moe_bf16_to_f16", "moe_sync_status", "moe_status_string", "moe_launch_count",
            "moe_test_arm_scan_timeout")
 
 
@@ -53,6 +53,7 @@ _SIGS = {
                                        _P, _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_aux_stats": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
+    "moe_bf16_to_f16": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, _P]),
     "moe_sync_status": (ctypes.c_int, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_launch_count": (ctypes.c_uint64, []),
@@ -152,6 +153,11 @@ def combine(cfg, y_perm, slot, topk_w, y_shared, y, stream=None):
 def aux_stats(cfg, counts, ws, f, P, l_aux, stream=None):
     _check("moe_aux_stats", lib().moe_aux_stats(ctypes.byref(cfg), _ptr(counts), _ptr(ws), _ptr(f),
                                                  _ptr(P), _ptr(l_aux), _stream(stream)))
+
+
+def bf16_to_f16(src, dst, ws, stream=None):
+    _check("moe_bf16_to_f16", lib().moe_bf16_to_f16(_ptr(src), _ptr(dst), src.numel(), _ptr(ws),
+                                                     _stream(stream)))
 
 
 def sync_status(ws, stream=None) -> int:

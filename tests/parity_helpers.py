@@ -58,16 +58,45 @@ def comparable_tokens(L32, ids, K: int, C: int, thr: float = 1e-4) -> np.ndarray
 
 def assert_rounded_to(got, ref, dtype: str, acc_rel: float = 1e-4):
     """Elementwise: |got - ref| <= u * |ref| + acc_rel * RMS(ref), with u the unit
-    roundoff of the storage type (2^-8 for bf16, 2^-24 for fp32): a value stored once in
+    roundoff of the storage type (2^-8 bf16, 2^-11 fp16, 2^-24 fp32): a value stored once in
     that type after an fp32-accumulated computation."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     if ref.size == 0:
         return
-    u = 2.0 ** -8 if dtype == "bf16" else 2.0 ** -24
+    u = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11, "f32": 2.0 ** -24}[dtype]
     rms = np.sqrt(np.mean(ref ** 2))
     bound = u * np.abs(ref) + acc_rel * rms
     excess = np.abs(got - ref) - bound
     i = int(np.argmax(excess))
     assert excess.flat[i] <= 0, (f"element {i}: got {got.flat[i]!r} ref {ref.flat[i]!r} "
                                  f"bound {bound.flat[i]!r}")
+
+
+def half_ulp(ref, dtype: str):
+    """Half a unit in the last place of |ref| in the output type (0 where ref == 0)."""
+    ref = np.abs(np.asarray(ref, dtype=np.float64))
+    p = {"bf16": 8, "f16": 11, "f32": 24}[dtype]
+    e = np.floor(np.log2(np.where(ref > 0, ref, 1.0)))
+    return np.where(ref > 0, 2.0 ** (e - p), 0.0)
+
+
+def layer_output_error(got, ref, dtype: str):
+    """(metric, literal) for a layer output stored in ``dtype``.
+
+    literal = max|got - ref| / RMS(ref).  For bf16 outputs that bound is dominated by the
+    output's own rounding (an exactly computed result rounded to bf16 already reaches
+    0.02-0.04 on these workloads), so the metric compared with the tolerance is the error
+    in excess of half an output ulp: max(|got - ref| - ulp(ref)/2, 0) / RMS(ref).  For
+    fp32 outputs metric = literal."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0, 0.0
+    rms = np.sqrt(np.mean(ref ** 2))
+    rms = rms if rms > 0 else 1.0
+    err = np.abs(got - ref)
+    literal = float(err.max() / rms)
+    if dtype == "f32":
+        return literal, literal
+    return float(np.maximum(err - half_ulp(ref, dtype), 0).max() / rms), literal

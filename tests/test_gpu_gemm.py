@@ -1,0 +1,119 @@
+"""GPU: the tcgen05 grouped GEMM (moe_expert_up / moe_expert_down, bf16 layers) and the
+tensor-core router, called through the C ABI on hand-built group layouts, against the
+fp64 oracle.  Cases grow from one tile to ragged groups so a failure points at its cause.
+
+Bounds: h (fp16) elementwise within one fp16 rounding of the exact value plus 1e-4 RMS;
+y_perm (fp32) and logits within fp32-accumulation error (1e-4 of RMS / 1e-5 relative)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from routing_dispatch_expert_04_b300 import build as B
+from routing_dispatch_expert_04_b300 import native as N
+from parity_helpers import assert_rounded_to, rel_rms_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available()
+    B.build()
+    N.lib()
+
+
+def _gen(shape, std, seed, dtype):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return (torch.randn(*shape, generator=g, device="cuda") * std).to(dtype)
+
+
+CASES = [
+    # (name, offsets, Kd (=d for up), N (=F for up))
+    ("one_tile", [0, 128], 64, 256),
+    ("k_blocks", [0, 128], 512, 256),
+    ("multi_tile_ragged_m", [0, 300], 320, 768),
+    ("groups_empty_and_single_row", [0, 0, 130, 131, 400, 520], 136, 384),
+    ("many_groups", list(np.cumsum([0] + [37 * (i % 5) for i in range(40)])), 256, 512),
+]
+
+
+@pytest.mark.parametrize("name,offs,Kd,Nn", CASES, ids=[c[0] for c in CASES])
+def test_expert_up_gelu_f16(name, offs, Kd, Nn):
+    G = len(offs) - 1
+    rows = int(offs[-1])
+    rows_cap = rows + 64  # spare rows must stay untouched
+    cfg = N.make_config(max(rows, 1), Kd, G, 1, Nn, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    x = _gen((rows_cap, Kd), 1.0, 1, torch.bfloat16)
+    w1 = _gen((G, Nn, Kd), Kd ** -0.5, 2, torch.bfloat16)
+    h = torch.full((rows_cap, Nn), 7.0, dtype=torch.float16, device="cuda")
+    off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
+    N.expert_up(cfg, x, off_t, G, rows_cap, w1, h, ws)
+    assert N.sync_status(ws) == 0
+    xn, wn, hn = to_np(x), to_np(w1), h.float().cpu().numpy()
+    for g in range(G):
+        lo, hi = int(offs[g]), int(offs[g + 1])
+        if hi > lo:
+            ref = O.gelu(O.linear(xn[lo:hi], wn[g]))
+            assert_rounded_to(hn[lo:hi], ref, "f16")
+    assert (hn[rows:] == 7.0).all()
+
+
+@pytest.mark.parametrize("name,offs,Kd,Nn", CASES, ids=[c[0] for c in CASES])
+def test_expert_down_f32(name, offs, Kd, Nn):
+    G = len(offs) - 1
+    rows = int(offs[-1])
+    rows_cap = rows + 64
+    cfg = N.make_config(max(rows, 1), Nn, G, 1, Kd, "bf16", -1)  # down: N = d, Kd = F
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    h = _gen((rows_cap, Kd), 0.5, 3, torch.float16)
+    w2 = _gen((G, Nn, Kd), Kd ** -0.5, 4, torch.float16)
+    y = torch.full((rows_cap, Nn), 7.0, dtype=torch.float32, device="cuda")
+    off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
+    N.expert_down(cfg, h, off_t, G, rows_cap, w2, y, ws)
+    assert N.sync_status(ws) == 0
+    hn, wn, yn = h.float().cpu().numpy(), w2.float().cpu().numpy(), to_np(y)
+    for g in range(G):
+        lo, hi = int(offs[g]), int(offs[g + 1])
+        if hi > lo:
+            ref = O.linear(hn[lo:hi], wn[g])
+            assert rel_rms_err(yn[lo:hi], ref) <= 1e-4
+    assert (yn[rows:] == 7.0).all()
+
+
+@pytest.mark.parametrize("T,E,d,bias", [(300, 8, 256, False), (257, 128, 512, True),
+                                        (130, 256, 1024, True), (64, 5, 64, True)])
+def test_tensor_core_router(T, E, d, bias):
+    cfg = N.make_config(T, d, E, min(2, E), 64, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    x = _gen((T, d), 1.0, 5, torch.bfloat16)
+    wr = _gen((E, d), d ** -0.5, 6, torch.bfloat16)
+    b = _gen((E,), 0.5, 7, torch.float32) if bias else None
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, cfg.K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, cfg.K), dtype=torch.float32, device="cuda")
+    N.route(cfg, x, wr, b, logits, ids, w, ws)
+    assert N.sync_status(ws) == 0
+    L64, _ = O.router_logits(to_np(x), to_np(wr), None if b is None else to_np(b))
+    Lg = to_np(logits)
+    assert np.max(np.abs(Lg - L64) / (1.0 + np.abs(L64))) <= 1e-5
+
+
+def test_f16_conversion_exact_and_range_error():
+    src = _gen((4096,), 0.05, 8, torch.bfloat16)
+    src[7] = 1e-6   # below 2^-17: rounds at 2^-25
+    dst = torch.empty(4096, dtype=torch.float16, device="cuda")
+    cfg = N.make_config(1, 8, 1, 1, 8, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    N.bf16_to_f16(src, dst, ws)
+    assert N.sync_status(ws) == 0
+    a, b = src.float().cpu().numpy(), dst.float().cpu().numpy()
+    big = np.abs(a) >= 2.0 ** -17
+    assert np.array_equal(a[big], b[big])
+    assert np.max(np.abs(a - b)) <= 2.0 ** -25
+    src[100] = 70000.0
+    N.bf16_to_f16(src, dst, ws)
+    assert N.sync_status(ws) == 5
