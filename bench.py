@@ -49,6 +49,21 @@ def peaks():
             "source": "fallback"}
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (identity for one process)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank_step: int, steps: int, world: int,
+                           seconds_local: float, device=None) -> float:
+    """Tokens of all ranks divided by the slowest rank's time (replicas, weak scaling)."""
+    return world * tokens_per_rank_step * steps / max_over_ranks(seconds_local, world, device)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -268,12 +283,9 @@ def run_ours(args, wl):
         for i, n in enumerate(stage_names):
             stage_ms[n].append(e[i].elapsed_time(e[i + 1]))
         step_ms.append(e[0].elapsed_time(e[-1]))
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = world * wl.T * args.steps / total_s
+    local_s = sum(step_ms) / 1e3
+    value = whole_job_tokens_per_s(wl.T, args.steps, world, local_s, dev)
+    total_s = world * wl.T * args.steps / value
 
     # ---- algorithmic work of this batch (see the per-stage byte/flop model)
     R = int(layer.offsets[-1].item())
@@ -349,11 +361,7 @@ def run_ours(args, wl):
         z.record(stream)
         z.synchronize()
         e_ms.append(a.elapsed_time(z))
-    e2e_s = sum(e_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(sum(e_ms) / 1e3, world, dev)
     e2e = {"value": round(world * wl.T * args.steps / e2e_s, 1), "unit": "tokens/s",
            "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
            "d2h_bytes_per_step": y_host.numel() * y_host.element_size() + stats_host.numel() * 4,

@@ -21,7 +21,8 @@ cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const
                            const void* ys, void* y, int Tn, int d, int K, int num_sms,
                            cudaStream_t st);
 cudaError_t launch_aux(const int32_t* counts, const float* ppart, int nblk, int E, int Tn, int K,
-                       float alpha, float* f, float* P, float* l_aux, cudaStream_t st);
+                       float alpha, float* f, float* P, float* l_aux, double* auxfp, uint32_t* hdr,
+                       cudaStream_t st);
 cudaError_t launch_simt_grouped(int dtype, const void* A, const void* B, void* C,
                                 const int32_t* offsets, int G, int N, int Kd, int64_t rows_cap,
                                 bool gelu, uint32_t* hdr, cudaStream_t st);
@@ -236,8 +237,10 @@ moe_status_t moe_aux_stats(const moe_config* cfg, const int32_t* counts, const v
       ((uintptr_t)l_aux & 3))
     return MOE_ERR_INVALID;
   const WsLayout L = ws_layout(c);
-  return cuda_status(launch_aux(counts, (const float*)((const char*)ws + L.ppart), L.nblk_route,
-                                c.E, c.T, c.K, c.alpha, f, P, l_aux, (cudaStream_t)stream));
+  char* w = (char*)const_cast<void*>(ws);
+  return cuda_status(launch_aux(counts, (const float*)(w + L.ppart), L.nblk_route, c.E, c.T, c.K,
+                                c.alpha, f, P, l_aux, (double*)(w + L.auxfp), (uint32_t*)w,
+                                (cudaStream_t)stream));
 }
 
 moe_status_t moe_bf16_to_f16(const void* src, void* dst, int64_t n, void* ws, void* stream) {

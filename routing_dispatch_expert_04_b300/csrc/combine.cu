@@ -11,8 +11,9 @@
 //
 // Aux statistics -- "Load Balancing: The Auxiliary Loss": L_aux = alpha * sum_i f_i P_i
 // with f_i the fraction of the T*K assignments routed to expert i (counted before
-// dropping) and P_i the mean softmax probability of expert i.  P_i is the fixed-order
-// fp64 sum of the per-block partial sums the routing kernel left in the workspace.
+// dropping) and P_i the mean softmax probability of expert i.  P_i is a fixed-order
+// fp64 reduction of the per-block partial sums the routing kernel left in the workspace,
+// and the sum over experts is taken in expert order, so the result is deterministic.
 #include "common.cuh"
 
 namespace moe {
@@ -79,37 +80,53 @@ combine_kernel(const float* __restrict__ yp, const int32_t* __restrict__ slot,
   }
 }
 
-__global__ void __launch_bounds__(256)
+// One block per expert: P_i from the per-route-block partial sums (layout [E][nblk]),
+// f_i from the pre-drop counts; the last block to finish sums f_i * P_i over i in order.
+constexpr int AUX_THREADS = 128;
+
+__global__ void __launch_bounds__(AUX_THREADS)
 aux_kernel(const int32_t* __restrict__ counts, const float* __restrict__ ppart, int nblk, int E,
            int Tn, int K, float alpha, float* __restrict__ f, float* __restrict__ P,
-           float* __restrict__ l_aux) {
-  __shared__ double s_fp[256];
-  const int e = threadIdx.x;
-  if (e < E) {
-    double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
-    int b = 0;
-    for (; b + 3 < nblk; b += 4) {
-      a0 += (double)ppart[(size_t)(b + 0) * E + e];
-      a1 += (double)ppart[(size_t)(b + 1) * E + e];
-      a2 += (double)ppart[(size_t)(b + 2) * E + e];
-      a3 += (double)ppart[(size_t)(b + 3) * E + e];
-    }
-    for (; b < nblk; ++b) a0 += (double)ppart[(size_t)b * E + e];
-    const double psum = (a0 + a1) + (a2 + a3);
+           float* __restrict__ l_aux, double* auxfp, uint32_t* hdr) {
+  __shared__ double s_red[AUX_THREADS];
+  __shared__ bool s_last;
+  const int e = blockIdx.x, tid = threadIdx.x;
+  const float* row = ppart + (size_t)e * nblk;
+  double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+  int b = tid;
+  for (; b + 3 * AUX_THREADS < nblk; b += 4 * AUX_THREADS) {
+    a0 += (double)row[b];
+    a1 += (double)row[b + AUX_THREADS];
+    a2 += (double)row[b + 2 * AUX_THREADS];
+    a3 += (double)row[b + 3 * AUX_THREADS];
+  }
+  for (; b < nblk; b += AUX_THREADS) a0 += (double)row[b];
+  s_red[tid] = (a0 + a1) + (a2 + a3);
+  __syncthreads();
+  for (int w = AUX_THREADS / 2; w > 0; w >>= 1) {
+    if (tid < w) s_red[tid] += s_red[tid + w];
+    __syncthreads();
+  }
+  if (tid == 0) {
     double fe = 0.0, pe = 0.0;
     if (Tn > 0) {
       fe = (double)counts[e] / ((double)Tn * (double)K);
-      pe = psum / (double)Tn;
+      pe = s_red[0] / (double)Tn;
     }
     f[e] = (float)fe;
     P[e] = (float)pe;
-    s_fp[e] = fe * pe;
+    auxfp[e] = fe * pe;
+    __threadfence();
+    s_last = (atomicAdd(&hdr[2], 1u) == (uint32_t)(E - 1));
   }
   __syncthreads();
-  if (e == 0) {
+  if (s_last && tid == 0) {
+    __threadfence();
+    const volatile double* v = auxfp;
     double acc = 0.0;
-    for (int i = 0; i < E; ++i) acc += s_fp[i];
+    for (int i = 0; i < E; ++i) acc += v[i];
     l_aux[0] = (float)((double)alpha * acc);
+    hdr[2] = 0u;  // ready for the next call
   }
 }
 
@@ -129,8 +146,10 @@ cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const
 }
 
 cudaError_t launch_aux(const int32_t* counts, const float* ppart, int nblk, int E, int Tn, int K,
-                       float alpha, float* f, float* P, float* l_aux, cudaStream_t st) {
-  aux_kernel<<<1, 256, 0, st>>>(counts, ppart, nblk, E, Tn, K, alpha, f, P, l_aux);
+                       float alpha, float* f, float* P, float* l_aux, double* auxfp, uint32_t* hdr,
+                       cudaStream_t st) {
+  aux_kernel<<<E, AUX_THREADS, 0, st>>>(counts, ppart, nblk, E, Tn, K, alpha, f, P, l_aux, auxfp,
+                                        hdr);
   count_launch();
   return cudaGetLastError();
 }

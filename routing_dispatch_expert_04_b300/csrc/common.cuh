@@ -21,10 +21,11 @@ __device__ __forceinline__ void raise_error(uint32_t* status, uint32_t bit) {
 }
 
 // ------------------------------------------------------------------ workspace layout
-// [0, 256)        header: u32 status, u32 scan ticket
+// [0, 256)        header: u32 status, u32 scan ticket, u32 aux ticket
 // desc            scan descriptors, nblk_scan * E * u64 (flag << 32 | value)
 // pos             A * i32, position of each assignment inside its expert (pre-drop)
-// ppart           nblk_route * E * f32, per-block sums of softmax probabilities
+// ppart           E * nblk_route * f32, per-block sums of softmax probabilities
+// auxfp           E * f64, per-expert f_i * P_i for the final fixed-order sum
 constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_IPT = 16;
 constexpr int SCAN_ITEMS = SCAN_THREADS * SCAN_IPT;  // assignments per scan block
@@ -33,7 +34,7 @@ constexpr int ROUTE_TPW = 4;                          // tokens per warp
 constexpr int ROUTE_TOKENS = ROUTE_WARPS * ROUTE_TPW; // tokens per route block
 
 struct WsLayout {
-  size_t desc, pos, ppart, total;
+  size_t desc, pos, ppart, auxfp, total;
   int nblk_scan, nblk_route;
 };
 
@@ -51,6 +52,8 @@ inline WsLayout ws_layout(const moe_config& c) {
   off = align_up(off + (size_t)A * 4, 256);
   L.ppart = off;
   off = align_up(off + (size_t)L.nblk_route * c.E * 4, 256);
+  L.auxfp = off;
+  off = align_up(off + (size_t)c.E * 8, 256);
   L.total = off;
   return L;
 }

@@ -109,7 +109,7 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int r
     float acc = 0.f;
 #pragma unroll
     for (int w = 0; w < ROUTE_WARPS; ++w) acc += s_p[w][e];
-    ppart[(size_t)blockIdx.x * E + e] = acc;
+    ppart[(size_t)e * gridDim.x + blockIdx.x] = acc;
   }
 }
 
