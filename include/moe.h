@@ -108,6 +108,27 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
                           int32_t* counts, int32_t* offsets, int32_t* slot, int32_t* src,
                           void* x_perm, void* ws, void* stream);
 
+/* moe_dispatch without a workspace argument.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory when they run the
+ * layer (code inside a custom allocator or memory pool, plugins barred from cudaMalloc,
+ * runtimes that reserve all memory up front).  Same arguments, outputs and results as
+ * moe_dispatch minus `ws`: its scratch (scan descriptors, ticket, positions) lives in a
+ * static 4 MiB device array inside the library, which every GPU that loads the library
+ * holds until the process exits.  It allocates nothing and calls no allocating routine.
+ * - Limit: the scratch must hold 256 + ceil(T*K/4096)*E*8 + T*K*4 bytes (each part
+ *   rounded up to 256 bytes), i.e. T*K up to about 930,000 assignments at E = 256 and
+ *   1,040,000 at E = 8; larger configs return MOE_ERR_UNSUPPORTED with a message on
+ *   stderr before any CUDA call.
+ * - The first call on each device looks up the array's device address (with that device
+ *   current); make that first call before any stream capture.
+ * - All calls share the array: calls that can overlap on the GPU (other streams, other
+ *   host threads) race and must be serialised by the caller.
+ * - Device-side errors are not reported: an out-of-range expert id gets slot -1 and is
+ *   left out of counts, and a look-back wait that gives up leaves the results invalid. */
+moe_status_t moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                                  int32_t* counts, int32_t* offsets, int32_t* slot, int32_t* src,
+                                  void* x_perm, void* stream);
+
 /* Step 3a -- grouped first expert Linear with GELU fused in its epilogue
  * ("Each expert applies: Linear(d -> 4d) -> GELU -> Linear(4d -> d)").
  *   x_perm   [rows_cap, d] dtype in; group g owns rows [offsets[g], offsets[g+1])

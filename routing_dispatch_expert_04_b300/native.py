@@ -21,6 +21,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_E
           4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_DEVICE"}
 
 EXPORTS = ("moe_workspace_size", "moe_rows_capacity", "moe_route", "moe_dispatch",
+           "moe_dispatch_noalloc",
            "moe_expert_up", "moe_expert_down", "moe_grouped_ffn", "moe_combine",
            "moe_aux_stats", "moe_bf16_to_f16", "moe_sync_status", "moe_status_string", "moe_launch_count",
            "moe_test_arm_scan_timeout")
@@ -47,6 +48,7 @@ _SIGS = {
     "moe_rows_capacity": (ctypes.c_int64, [_CFG]),
     "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_up": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P]),
     "moe_expert_down": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P,
@@ -126,6 +128,13 @@ def dispatch(cfg, x, topk_ids, counts, offsets, slot, src, x_perm, ws, stream=No
     _check("moe_dispatch", lib().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_ids), _ptr(counts),
                                                _ptr(offsets), _ptr(slot), _ptr(src), _ptr(x_perm),
                                                _ptr(ws), _stream(stream)))
+
+
+def dispatch_noalloc(cfg, x, topk_ids, counts, offsets, slot, src, x_perm, stream=None):
+    """moe_dispatch with its scratch in the library's static device array (no workspace)."""
+    _check("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_ids), _ptr(counts), _ptr(offsets), _ptr(slot),
+        _ptr(src), _ptr(x_perm), _stream(stream)))
 
 
 def expert_up(cfg, x_perm, offsets, n_groups, rows_cap, w1, h, ws, stream=None):
