@@ -223,66 +223,40 @@ def run_ours(args, wl):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    stage_names = ["route", "dispatch", "expert_up", "expert_down"]
-    if layer.shared:
-        stage_names.append("shared_expert")
-    stage_names += ["combine", "aux"]
-
-    def step(evs=None):
-        def mark(i):
-            if evs is not None:
-                evs[i].record(stream)
-        mark(0)
-        layer.route(x)
-        mark(1)
-        layer.dispatch(x)
-        mark(2)
-        layer.experts_up()
-        mark(3)
-        layer.experts_down()
-        i = 4
-        if layer.shared:
-            mark(i)
-            layer.shared_expert(x)
-            i += 1
-        mark(i)
-        layer.combine()
-        mark(i + 1)
-        layer.aux()
-        mark(i + 2)
+    stage_names = layer.stage_names()
+    n_ev = len(stage_names) + 1
+    # one CUDA graph per step, with timing events recorded as graph nodes before every stage
+    marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
+    kernels_per_step = layer.capture(x, marks=marks)
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        layer.replay()
     torch.cuda.synchronize()
     layer.check_device_status()
 
-    n_ev = len(stage_names) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    stage_ms = {n: [] for n in stage_names}
+    step_ms = []
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    launches0 = N.launch_count()
     for k in range(args.steps):
         flush.zero_()
-        step(evs[k])
+        layer.replay()
+        torch.cuda.synchronize()   # the graph's events are re-recorded by the next replay
+        for i, n in enumerate(stage_names):
+            stage_ms[n].append(marks[i].elapsed_time(marks[i + 1]))
+        step_ms.append(marks[0].elapsed_time(marks[-1]))
     torch.cuda.synchronize()
-    launches = N.launch_count() - launches0
+    launches = kernels_per_step * args.steps
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
     layer.check_device_status()
 
-    stage_ms = {n: [] for n in stage_names}
-    step_ms = []
-    for k in range(args.steps):
-        e = evs[k]
-        for i, n in enumerate(stage_names):
-            stage_ms[n].append(e[i].elapsed_time(e[i + 1]))
-        step_ms.append(e[0].elapsed_time(e[-1]))
     local_s = sum(step_ms) / 1e3
     value = whole_job_tokens_per_s(wl.T, args.steps, world, local_s, dev)
     total_s = world * wl.T * args.steps / value
@@ -339,10 +313,9 @@ def run_ours(args, wl):
     x_host = x.cpu().pin_memory()
     y_host = torch.empty((wl.T, wl.d), dtype=layer.dtype).pin_memory()
     stats_host = torch.empty(2 * wl.E + 1, dtype=torch.float32).pin_memory()
-    x_dev = torch.empty_like(x)
 
     def e2e_step():
-        layer.forward_host(x_host, y_host, x_dev)
+        layer.forward_host(x_host, y_host)
         stats_host[:wl.E].copy_(layer.f, non_blocking=True)
         stats_host[wl.E:2 * wl.E].copy_(layer.P, non_blocking=True)
         stats_host[2 * wl.E:].copy_(layer.l_aux, non_blocking=True)
@@ -385,7 +358,9 @@ def run_ours(args, wl):
                    "capacity": layer.cfg.capacity, "parallelism": f"replicas x{world}",
                    "l2": "flushed before each step (512 MiB device write, outside the events)"},
         "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches, "gpu_launches_per_step": launches / args.steps, "clocks": clk,
+        "gpu_launches": launches, "gpu_launches_per_step": kernels_per_step,
+        "launch_mode": "one CUDA graph per step (library kernels + the scan's memset node)",
+        "clocks": clk,
         "device": torch.cuda.get_device_name(dev),
     }
     if rank == 0:

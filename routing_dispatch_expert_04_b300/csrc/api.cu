@@ -8,8 +8,9 @@
 
 namespace moe {
 
-cudaError_t launch_softmax_topk(const float* logits, int T, int E, int K, int renorm, int32_t* ids,
-                                float* w, float* ppart, int nblk, cudaStream_t st);
+cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, int32_t* ids,
+                                float* w, float* ppart, int nblk, const float* lpart, int nsplit,
+                                const float* bias, cudaStream_t st);
 cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsigned long long* desc,
                         int32_t* pos, int32_t* counts, int32_t* offsets, uint32_t* hdr,
                         int skip_block, int spin_limit, cudaStream_t st);
@@ -29,13 +30,13 @@ cudaError_t launch_simt_grouped(int dtype, const void* A, const void* B, void* C
 cudaError_t launch_simt_router(int dtype, const void* x, const void* w_r, const float* b_r,
                                float* logits, int T, int E, int d, uint32_t* hdr, cudaStream_t st);
 cudaError_t launch_tc_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets, int G,
-                         int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
-                         cudaStream_t st);
+                         int N, int Kd, int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr,
+                         int num_sms, cudaStream_t st);
 cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
-                           int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
-                           cudaStream_t st);
-cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, float* logits, int T,
-                             int E, int d, uint32_t* hdr, int num_sms, cudaStream_t st);
+                           int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
+                           uint32_t* hdr, int num_sms, cudaStream_t st);
+cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, float* out, int T,
+                             int E, int d, int nsplit, uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_bf16_to_f16(const void* src, void* dst, int64_t n, uint32_t* hdr, int num_sms,
                                cudaStream_t st);
 
@@ -78,6 +79,14 @@ static moe_status_t cuda_status(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
+// Most rows one group can hold (for tile planning only): C for the routed experts of a
+// layer with dropping, the whole buffer for a single group; <= 0 when unknown.
+static int64_t group_row_bound(const moe_config& c, int n_groups, int64_t rows_cap) {
+  if (n_groups == 1) return rows_cap;
+  if (n_groups == c.E && c.capacity >= 0) return c.capacity;
+  return 0;
+}
+
 static int64_t rows_capacity(const moe_config& c) {
   const int64_t A = (int64_t)c.T * c.K;
   if (c.capacity < 0) return A;
@@ -115,15 +124,24 @@ moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, co
   cudaStream_t st = (cudaStream_t)stream;
   const WsLayout L = ws_layout(c);
   uint32_t* hdr = (uint32_t*)ws;
+  const float* lpart = nullptr;
   if (x != nullptr) {
-    if (c.dtype == MOE_BF16)
-      s = cuda_status(launch_tc_router(x, w_r, b_r, logits, c.T, c.E, c.d, hdr, num_sms(), st));
-    else
+    if (c.dtype == MOE_BF16) {
+      float* out = logits;
+      if (L.router_splits > 1) {
+        out = (float*)((char*)ws + L.lpart);
+        lpart = out;
+      }
+      s = cuda_status(launch_tc_router(x, w_r, b_r, out, c.T, c.E, c.d, L.router_splits, hdr,
+                                       num_sms(), st));
+    } else {
       s = cuda_status(launch_simt_router(c.dtype, x, w_r, b_r, logits, c.T, c.E, c.d, hdr, st));
+    }
     if (s != MOE_OK) return s;
   }
   return cuda_status(launch_softmax_topk(logits, c.T, c.E, c.K, c.renormalize, topk_ids, topk_w,
-                                         (float*)((char*)ws + L.ppart), L.nblk_route, st));
+                                         (float*)((char*)ws + L.ppart), L.nblk_route, lpart,
+                                         L.router_splits, b_r, st));
 }
 
 moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_ids,
@@ -187,7 +205,8 @@ moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int3
   const moe_config& c = *cfg;
   if (c.dtype == MOE_BF16)
     return cuda_status(launch_tc_up(x_perm, w1, h, offsets, n_groups, c.F, c.d, rows_cap,
-                                    (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
+                                    group_row_bound(c, n_groups, rows_cap), (uint32_t*)ws,
+                                    num_sms(), (cudaStream_t)stream));
   return cuda_status(launch_simt_grouped(c.dtype, x_perm, w1, h, offsets, n_groups, c.F, c.d,
                                          rows_cap, true, (uint32_t*)ws, (cudaStream_t)stream));
 }
@@ -201,7 +220,8 @@ moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t
   const moe_config& c = *cfg;
   if (c.dtype == MOE_BF16)
     return cuda_status(launch_tc_down(h, w2, y_perm, offsets, n_groups, c.d, c.F, rows_cap,
-                                      (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
+                                      group_row_bound(c, n_groups, rows_cap), (uint32_t*)ws,
+                                      num_sms(), (cudaStream_t)stream));
   return cuda_status(launch_simt_grouped(c.dtype, h, w2, y_perm, offsets, n_groups, c.d, c.F,
                                          rows_cap, false, (uint32_t*)ws, (cudaStream_t)stream));
 }

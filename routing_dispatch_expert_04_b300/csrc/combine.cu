@@ -18,13 +18,28 @@
 
 namespace moe {
 
-// Expert outputs (yp, ys) are fp32; each thread handles 4 consecutive columns.
+// Expert outputs (yp, ys) are fp32.  Each lane handles two 4-column slots per pass (j and
+// j + 32) so that up to 2 x 4 row loads are in flight per lane; k is summed in order.
+template <typename T>
+__device__ __forceinline__ void store4(T* out, const float* acc);
+template <>
+__device__ __forceinline__ void store4<float>(float* out, const float* acc) {
+  st_v4(out, Elem<float>::pack(acc));
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* out, const float* acc) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
+  *reinterpret_cast<uint2*>(out) =
+      make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ yp, const int32_t* __restrict__ slot,
                const float* __restrict__ w, const float* __restrict__ ys, T* __restrict__ y,
                int Tn, int d, int K) {
-  constexpr int P = 4;
+  constexpr int P = 4, KC = 4;
   __shared__ int s_slot[8][32];
   __shared__ float s_w[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -35,46 +50,52 @@ combine_kernel(const float* __restrict__ yp, const int32_t* __restrict__ slot,
       s_w[warp][lane] = w[(size_t)t * K + lane];
     }
     __syncwarp();
-    for (int j = lane; j < nvec; j += 32) {
-      float acc[P];
+    for (int j0 = lane; j0 < nvec; j0 += 64) {
+      const int j1 = j0 + 32;
+      const bool two = j1 < nvec;
+      float acc0[P], acc1[P];
 #pragma unroll
-      for (int i = 0; i < P; ++i) acc[i] = 0.f;
-      for (int k0 = 0; k0 < K; k0 += 8) {
-        uint4 v[8];
+      for (int i = 0; i < P; ++i) acc0[i] = acc1[i] = 0.f;
+      for (int k0 = 0; k0 < K; k0 += KC) {
+        uint4 v0[KC], v1[KC];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < KC; ++u) {
           const int k = k0 + u;
           const int s = (k < K) ? s_slot[warp][k] : -1;
-          v[u] = (s >= 0) ? ld_nc_v4(reinterpret_cast<const uint4*>(yp + (size_t)s * d) + j)
-                          : make_uint4(0u, 0u, 0u, 0u);
+          const uint4* rowp = reinterpret_cast<const uint4*>(yp + (size_t)(s < 0 ? 0 : s) * d);
+          v0[u] = (s >= 0) ? ld_nc_v4(rowp + j0) : make_uint4(0u, 0u, 0u, 0u);
+          v1[u] = (s >= 0 && two) ? ld_nc_v4(rowp + j1) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < KC; ++u) {
           const int k = k0 + u;
           if (k < K && s_slot[warp][k] >= 0) {
-            float f[P];
-            Elem<float>::unpack(v[u], f);
+            float f0[P], f1[P];
+            Elem<float>::unpack(v0[u], f0);
+            Elem<float>::unpack(v1[u], f1);
             const float wk = s_w[warp][k];
 #pragma unroll
-            for (int i = 0; i < P; ++i) acc[i] = fmaf(wk, f[i], acc[i]);
+            for (int i = 0; i < P; ++i) {
+              acc0[i] = fmaf(wk, f0[i], acc0[i]);
+              acc1[i] = fmaf(wk, f1[i], acc1[i]);
+            }
           }
         }
       }
       if (ys != nullptr) {
-        float f[P];
-        Elem<float>::unpack(ld_nc_v4(reinterpret_cast<const uint4*>(ys + (size_t)t * d) + j), f);
+        const uint4* rs = reinterpret_cast<const uint4*>(ys + (size_t)t * d);
+        float f0[P], f1[P];
+        Elem<float>::unpack(ld_nc_v4(rs + j0), f0);
+        Elem<float>::unpack(two ? ld_nc_v4(rs + j1) : make_uint4(0u, 0u, 0u, 0u), f1);
 #pragma unroll
-        for (int i = 0; i < P; ++i) acc[i] += f[i];
+        for (int i = 0; i < P; ++i) {
+          acc0[i] += f0[i];
+          acc1[i] += f1[i];
+        }
       }
-      T* out = y + (size_t)t * d + (size_t)j * P;
-      if (sizeof(T) == 4) {
-        st_v4(out, Elem<float>::pack(acc));
-      } else {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
-        uint2 v2 = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-        *reinterpret_cast<uint2*>(out) = v2;
-      }
+      T* out = y + (size_t)t * d;
+      store4<T>(out + (size_t)j0 * P, acc0);
+      if (two) store4<T>(out + (size_t)j1 * P, acc1);
     }
     __syncwarp();
   }

@@ -26,17 +26,33 @@ __device__ __forceinline__ void raise_error(uint32_t* status, uint32_t bit) {
 // pos             A * i32, position of each assignment inside its expert (pre-drop)
 // ppart           E * nblk_route * f32, per-block sums of softmax probabilities
 // auxfp           E * f64, per-expert f_i * P_i for the final fixed-order sum
+// lpart           router_splits * T * E * f32, partial router logits (split-K router only)
 constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_IPT = 16;
 constexpr int SCAN_ITEMS = SCAN_THREADS * SCAN_IPT;  // assignments per scan block
 constexpr int ROUTE_WARPS = 8;
-constexpr int ROUTE_TPW = 4;                          // tokens per warp
+constexpr int ROUTE_TPW = 1;                          // tokens per warp
 constexpr int ROUTE_TOKENS = ROUTE_WARPS * ROUTE_TPW; // tokens per route block
 
 struct WsLayout {
-  size_t desc, pos, ppart, auxfp, total;
-  int nblk_scan, nblk_route;
+  size_t desc, pos, ppart, auxfp, lpart, total;
+  int nblk_scan, nblk_route, router_splits;
 };
+
+// K splits of the tensor-core router: enough CTAs to cover the SMs when T/128 row tiles
+// alone would not (planned for 148 SMs; a smaller GPU just runs more waves).  Every
+// slice keeps at least one 64-wide k-block.
+inline int router_splits(const moe_config& c) {
+  if (c.dtype != MOE_BF16 || c.T <= 0) return 1;
+  const int mt = (c.T + 127) / 128;
+  const int nkb = (c.d + 63) / 64;
+  int s = 148 / mt;
+  if (s > 4) s = 4;
+  if (s > nkb) s = nkb;
+  if (s < 2) return 1;
+  const int kpb = (nkb + s - 1) / s;
+  return (nkb + kpb - 1) / kpb;
+}
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -54,6 +70,9 @@ inline WsLayout ws_layout(const moe_config& c) {
   off = align_up(off + (size_t)L.nblk_route * c.E * 4, 256);
   L.auxfp = off;
   off = align_up(off + (size_t)c.E * 8, 256);
+  L.router_splits = router_splits(c);
+  L.lpart = off;
+  if (L.router_splits > 1) off = align_up(off + (size_t)L.router_splits * c.T * c.E * 4, 256);
   L.total = off;
   return L;
 }

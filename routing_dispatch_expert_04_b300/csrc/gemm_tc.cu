@@ -45,10 +45,13 @@ struct TcArgs {
   const int32_t* offsets;  // [G+1] device, or nullptr: one group of M rows
   int G, M, N, Kd;
   int64_t rows_cap;
-  void* out;               // [rows_cap, ldo]
+  void* out;               // [rows_cap, ldo] (times ksplit partial slices)
   int ldo;
-  const float* bias;       // [N] or nullptr
+  const float* bias;       // [N] or nullptr (added only when ksplit == 1)
   uint32_t* hdr;           // status word
+  int ksplit;              // K split across CTAs: slice s holds the partial sum of k-blocks
+  int kpb;                 //   [s*kpb, min(nkb, (s+1)*kpb)); ksplit*kpb covers nkb, no slice empty
+  int64_t split_stride;    // elements between the partial slices of `out`
 };
 
 template <int BN, int STAGES>
@@ -204,7 +207,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  const int total = s_tpre[G];
+  const int ksplit = args.ksplit;
+  const int total = s_tpre[G] * ksplit;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -214,9 +218,11 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       int issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(t, G, s_lo, s_hi, s_mt, s_tpre, BN);
+        const TileInfo ti = decode_tile(t / ksplit, G, s_lo, s_hi, s_mt, s_tpre, BN);
         const int brow = ti.g * args.N + ti.n0;
-        for (int kb = 0; kb < nkb; ++kb) {
+        const int kb0 = (t % ksplit) * args.kpb;
+        const int kb1 = min(nkb, kb0 + args.kpb);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr)) {
             ok = false;
             break;
@@ -256,7 +262,9 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (!wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < nkb; ++kb) {
+        const int kb0 = (t % ksplit) * args.kpb;
+        const int kb1 = min(nkb, kb0 + args.kpb);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_phase(&full[s], ph, s_abort, args.hdr)) {
             ok = false;
             break;
@@ -267,7 +275,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
           for (int k = 0; k < TC_BK / 16; ++k) {
             mma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), IDESC,
-                     (kb | k) != 0 ? 1u : 0u);
+                     (kb != kb0 || k != 0) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
           if (++s == STAGES) {
@@ -291,7 +299,9 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int r_in_tile = q * 32 + lane;
     uint32_t acc = 0, aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile(t, G, s_lo, s_hi, s_mt, s_tpre, BN);
+      const TileInfo ti = decode_tile(t / ksplit, G, s_lo, s_hi, s_mt, s_tpre, BN);
+      const int64_t slice = (int64_t)(t % ksplit) * args.split_stride;
+      const float* bias = ksplit == 1 ? args.bias : nullptr;
       if (!wait_phase(&tfull[acc], aph, s_abort, args.hdr)) break;
       tc_fence_after();
       const int row = ti.row0 + r_in_tile;
@@ -323,19 +333,19 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           }
           if (bad) raise_error(args.hdr, DEV_ERR_RANGE);
         } else if (EPI == TC_EPI_F32) {
-          float* out = (float*)args.out + (size_t)row * args.ldo + col0;
+          float* out = (float*)args.out + slice + (size_t)row * args.ldo + col0;
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
             if (col0 + v4 * 4 >= args.N) break;
             st_v4(out + v4 * 4, make_uint4(r[v4 * 4], r[v4 * 4 + 1], r[v4 * 4 + 2], r[v4 * 4 + 3]));
           }
         } else {
-          float* out = (float*)args.out + (size_t)row * args.ldo;
+          float* out = (float*)args.out + slice + (size_t)row * args.ldo;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int col = col0 + i;
             if (col < args.N)
-              out[col] = __uint_as_float(r[i]) + (args.bias != nullptr ? args.bias[col] : 0.f);
+              out[col] = __uint_as_float(r[i]) + (bias != nullptr ? bias[col] : 0.f);
           }
         }
       }
@@ -400,7 +410,7 @@ static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int 
   if (!make_map(&mb, B, F16IN, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN)) return cudaErrorInvalidValue;
   const int64_t n_tiles = (a.N + BN - 1) / BN;
   const int64_t m_bound = (a.rows_cap + TC_BM - 1) / TC_BM + (a.offsets ? a.G : 0);
-  int64_t grid = m_bound * n_tiles;
+  int64_t grid = m_bound * n_tiles * a.ksplit;
   if (grid > num_sms) grid = num_sms;
   if (grid < 1) grid = 1;
   kern<<<(unsigned)grid, TC_THREADS, Lay::ALLOC, st>>>(ma, mb, a);
@@ -408,26 +418,64 @@ static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int 
   return cudaGetLastError();
 }
 
+// N tile of an expert GEMM: 256, or 192 when 256-wide tiles would leave the last wave
+// of the persistent grid much emptier or waste columns.  The m-tile count is estimated
+// on the host from the row capacity (each group holds at most `cap_per_group` rows
+// when that is known).
+static int pick_bn(int64_t rows_cap, int G, int64_t cap_per_group, int N, int num_sms) {
+  int64_t m_tiles;
+  if (cap_per_group > 0) {
+    const int64_t per = cap_per_group < rows_cap ? cap_per_group : rows_cap;
+    m_tiles = (int64_t)G * ((per + TC_BM - 1) / TC_BM);
+    const int64_t bound = (rows_cap + TC_BM - 1) / TC_BM + G;
+    if (m_tiles > bound) m_tiles = bound;
+  } else {
+    m_tiles = (rows_cap + TC_BM - 1) / TC_BM + G / 2;
+  }
+  double best = -1.0;
+  int best_bn = 256;
+  for (int bn : {256, 192}) {
+    const int64_t nt = (N + bn - 1) / bn;
+    const double waves = (double)(m_tiles * nt) / num_sms;
+    const double full_waves = (double)(int64_t)(waves + 0.999999);
+    const double eff = waves / full_waves * ((double)N / (double)(nt * bn));
+    if (eff > best + 0.02) {
+      best = eff;
+      best_bn = bn;
+    }
+  }
+  return best_bn;
+}
+
 // First expert Linear, bf16 in, GELU fused, fp16 out: h[r] = GELU(x_perm[r] . W1[g]^T).
 cudaError_t launch_tc_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets, int G,
-                         int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
-                         cudaStream_t st) {
-  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr};
+                         int N, int Kd, int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr,
+                         int num_sms, cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0};
+  if (pick_bn(rows_cap, G, cap_per_group, N, num_sms) == 192)
+    return launch_tc<192, 5, TC_EPI_GELU_F16, false>(x_perm, w1, a, num_sms, st);
   return launch_tc<256, 4, TC_EPI_GELU_F16, false>(x_perm, w1, a, num_sms, st);
 }
 
 // Second expert Linear, fp16 in, fp32 out: y_perm[r] = h[r] . W2[g]^T.
 cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
-                           int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
-                           cudaStream_t st) {
-  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr};
+                           int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
+                           uint32_t* hdr, int num_sms, cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0};
+  if (pick_bn(rows_cap, G, cap_per_group, N, num_sms) == 192)
+    return launch_tc<192, 5, TC_EPI_F32, true>(h, w2h, a, num_sms, st);
   return launch_tc<256, 4, TC_EPI_F32, true>(h, w2h, a, num_sms, st);
 }
 
-// Router Linear, bf16 in, fp32 logits + bias: logits[t] = x[t] . W_r^T + b_r.
-cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, float* logits, int T,
-                             int E, int d, uint32_t* hdr, int num_sms, cudaStream_t st) {
-  TcArgs a{nullptr, 1, T, E, d, (int64_t)T, logits, E, b_r, hdr};
+// Router Linear, bf16 in, fp32 logits: logits[t] = x[t] . W_r^T + b_r.  With nsplit > 1
+// the K dimension is split over CTAs and `out` receives nsplit partial slices of
+// T*E floats (no bias); the softmax kernel sums them in slice order and adds the bias.
+cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, float* out, int T,
+                             int E, int d, int nsplit, uint32_t* hdr, int num_sms, cudaStream_t st) {
+  const int nkb = (d + TC_BK - 1) / TC_BK;
+  const int kpb = (nkb + nsplit - 1) / nsplit;
+  const int ks = (nkb + kpb - 1) / kpb;
+  TcArgs a{nullptr, 1, T, E, d, (int64_t)T, out, E, b_r, hdr, ks, kpb, (int64_t)T * E};
   // the epilogue reads TMEM 32 columns at a time, so the narrowest tile is 32 wide
   if (E <= 32) return launch_tc<32, 8, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
   if (E <= 64) return launch_tc<64, 8, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);

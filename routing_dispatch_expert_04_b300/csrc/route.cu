@@ -18,9 +18,10 @@ namespace moe {
 
 template <int VPT>
 __global__ void __launch_bounds__(ROUTE_WARPS * 32)
-softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renorm,
+softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
                     int32_t* __restrict__ ids, float* __restrict__ wout,
-                    float* __restrict__ ppart) {
+                    float* __restrict__ ppart, const float* __restrict__ lpart, int nsplit,
+                    const float* __restrict__ bias) {
   __shared__ float s_p[ROUTE_WARPS][VPT * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float pacc[VPT];
@@ -28,16 +29,39 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int r
   for (int j = 0; j < VPT; ++j) pacc[j] = 0.f;
 
   const int t0 = blockIdx.x * ROUTE_TOKENS + warp * ROUTE_TPW;
+  // the warp's token rows are loaded up front: one memory latency for all of them.  With
+  // a split-K router the logits are the partial slices summed in slice order, plus the
+  // bias; they are written back to `logits`.
+  float vv[ROUTE_TPW][VPT];
+  const size_t stride = (size_t)T * E;
+#pragma unroll
   for (int i = 0; i < ROUTE_TPW; ++i) {
     const int t = t0 + i;
-    if (t >= T) break;  // warp-uniform
-    const float* row = logits + (size_t)t * E;
-    float v[VPT];
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       const int e = lane + 32 * j;
-      v[j] = (e < E) ? row[e] : -INFINITY;
+      float v = -INFINITY;
+      if (t < T && e < E) {
+        const size_t o = (size_t)t * E + e;
+        if (lpart == nullptr) {
+          v = logits[o];
+        } else {
+          v = lpart[o];
+          for (int sp = 1; sp < nsplit; ++sp) v += lpart[sp * stride + o];
+          if (bias != nullptr) v += bias[e];
+          logits[o] = v;
+        }
+      }
+      vv[i][j] = v;
     }
+  }
+#pragma unroll
+  for (int i = 0; i < ROUTE_TPW; ++i) {
+    const int t = t0 + i;
+    if (t >= T) break;  // warp-uniform
+    float v[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) v[j] = vv[i][j];
     // softmax: max, sum of exp, normalise
     float m = v[0];
 #pragma unroll
@@ -113,13 +137,20 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int r
   }
 }
 
-cudaError_t launch_softmax_topk(const float* logits, int T, int E, int K, int renorm, int32_t* ids,
-                                float* w, float* ppart, int nblk, cudaStream_t st) {
+// lpart == nullptr: `logits` is the input.  Otherwise the logits are the sum of nsplit
+// partial slices of lpart (+ bias), and are also written to `logits`.
+cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, int32_t* ids,
+                                float* w, float* ppart, int nblk, const float* lpart, int nsplit,
+                                const float* bias, cudaStream_t st) {
   const dim3 grid(nblk), block(ROUTE_WARPS * 32);
-  if (E <= 32) softmax_topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart);
-  else if (E <= 64) softmax_topk_kernel<2><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart);
-  else if (E <= 128) softmax_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart);
-  else softmax_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart);
+  if (E <= 32)
+    softmax_topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias);
+  else if (E <= 64)
+    softmax_topk_kernel<2><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias);
+  else if (E <= 128)
+    softmax_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias);
+  else
+    softmax_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias);
   count_launch();
   return cudaGetLastError();
 }

@@ -13,9 +13,10 @@
 //
 // scan_kernel -- one pass over the flat id stream.  Each block takes a chunk of
 // SCAN_ITEMS assignments (chunk index drawn from an atomic ticket, so every block it
-// waits for has already started), ranks its assignments per expert with warp
-// match/popc and a per-expert running count in shared memory, publishes its per-expert
-// totals, and obtains the totals of all earlier chunks by a decoupled look-back with
+// waits for has already started).  Each warp ranks a contiguous segment of the chunk
+// per expert with warp match/popc and a warp-private running count in shared memory;
+// one prefix over the warps turns those into chunk ranks.  The block publishes its
+// per-expert totals, and obtains the totals of all earlier chunks by a decoupled look-back with
 // one descriptor per (chunk, expert).  Every wait is bounded: past `spin_limit` polls
 // the block records a timeout in the status word and carries on, so the kernel always
 // terminates.  The last chunk knows the grand totals and writes counts and offsets.
@@ -44,58 +45,64 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
             unsigned long long* desc, int32_t* __restrict__ pos, int32_t* __restrict__ counts,
             int32_t* __restrict__ offsets, uint32_t* hdr, int skip_block, int spin_limit) {
   constexpr int NW = SCAN_THREADS / 32;
-  __shared__ uint32_t s_wcnt[NW][256];  // (round stamp << 8) | count of e in warp
-  __shared__ int s_run[256];            // running count of e inside this chunk
-  __shared__ int s_excl[256];           // count of e in all earlier chunks
+  constexpr int WITEMS = SCAN_IPT * 32;  // each warp ranks one contiguous segment
+  __shared__ int s_wrun[NW][256];        // per-warp running count of e, then warp base
+  __shared__ int s_run[256];             // count of e in this chunk
+  __shared__ int s_excl[256];            // count of e in all earlier chunks
   __shared__ int s_b;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) s_b = (int)atomicAdd(&hdr[1], 1u);
-  for (int i = tid; i < NW * 256; i += SCAN_THREADS) (&s_wcnt[0][0])[i] = 0u;
-  for (int e = tid; e < 256; e += SCAN_THREADS) s_run[e] = 0;
+  for (int i = tid; i < NW * 256; i += SCAN_THREADS) (&s_wrun[0][0])[i] = 0;
   __syncthreads();
   const int b = s_b;
   const int64_t base = (int64_t)b * SCAN_ITEMS;
+  const int64_t wbase = base + (int64_t)warp * WITEMS;
   uint32_t lt;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
 
+  // this lane's ids, loaded up front: one memory latency for the whole segment
   int my_e[SCAN_IPT], my_r[SCAN_IPT];
 #pragma unroll
   for (int r = 0; r < SCAN_IPT; ++r) {
-    const int64_t a = base + (int64_t)r * SCAN_THREADS + tid;
-    int e = -1;
-    if (a < A) {
-      e = ids[a];
-      if (e < 0 || e >= E) {
-        raise_error(hdr, DEV_ERR_BAD_ID);
-        e = -1;
-      }
+    const int64_t a = wbase + r * 32 + lane;
+    my_e[r] = (a < A) ? ids[a] : -1;
+  }
+#pragma unroll
+  for (int r = 0; r < SCAN_IPT; ++r) {
+    const int64_t a = wbase + r * 32 + lane;
+    if (a < A && (my_e[r] < 0 || my_e[r] >= E)) {
+      raise_error(hdr, DEV_ERR_BAD_ID);
+      my_e[r] = -1;
     }
+  }
+  // rank inside the warp's segment, 32 assignments at a time, in flat order
+#pragma unroll
+  for (int r = 0; r < SCAN_IPT; ++r) {
+    const int e = my_e[r];
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    const int wrank = __popc(peers & lt);
-    const bool leader = (31 - __clz(peers)) == lane;
-    const uint32_t stamp = (uint32_t)(r + 1) << 8;
-    if (e >= 0 && leader) s_wcnt[warp][e] = stamp | (uint32_t)__popc(peers);
-    __syncthreads();
-    bool last = false;
-    int rank = 0;
-    if (e >= 0) {
-      int pre = 0;
-      for (int w = 0; w < warp; ++w) {
-        const uint32_t v = s_wcnt[w][e];
-        if ((v & ~0xffu) == stamp) pre += (int)(v & 0xffu);
-      }
-      last = leader;
-      for (int w = warp + 1; w < NW; ++w)
-        if ((s_wcnt[w][e] & ~0xffu) == stamp) last = false;
-      rank = s_run[e] + pre + wrank;
-    }
-    my_e[r] = e;
-    my_r[r] = rank;
-    __syncthreads();
-    if (last) s_run[e] = rank + 1;
+    const int run = (e >= 0) ? s_wrun[warp][e] : 0;
+    my_r[r] = run + __popc(peers & lt);
+    __syncwarp();
+    if (e >= 0 && (31 - __clz(peers)) == lane) s_wrun[warp][e] = run + __popc(peers);
+    __syncwarp();
   }
   __syncthreads();
+  // exclusive prefix of the per-warp counts (earlier warps hold earlier assignments)
+  for (int e = tid; e < E; e += SCAN_THREADS) {
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const int c = s_wrun[w][e];
+      s_wrun[w][e] = acc;
+      acc += c;
+    }
+    s_run[e] = acc;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < SCAN_IPT; ++r)
+    if (my_e[r] >= 0) my_r[r] += s_wrun[warp][my_e[r]];
 
   // decoupled look-back, one thread per expert
   const bool publish = (b != skip_block);
@@ -131,7 +138,7 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
 
 #pragma unroll
   for (int r = 0; r < SCAN_IPT; ++r) {
-    if (my_e[r] >= 0) pos[base + (int64_t)r * SCAN_THREADS + tid] = s_excl[my_e[r]] + my_r[r];
+    if (my_e[r] >= 0) pos[wbase + r * 32 + lane] = s_excl[my_e[r]] + my_r[r];
   }
 
   if (b == nblk - 1) {  // block-uniform

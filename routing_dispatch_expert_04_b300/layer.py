@@ -22,7 +22,7 @@ from . import native as N
 
 class MoELayer:
     def __init__(self, T, d, E, K, F, dtype, capacity_factor, alpha, w_r, b_r, w1, w2,
-                 w1s=None, w2s=None, renormalize=False, device="cuda"):
+                 w1s=None, w2s=None, renormalize=False, device="cuda", overlap=True):
         self.cfg = N.make_config(T, d, E, K, F, dtype, N.capacity(T, E, capacity_factor),
                                  renormalize, alpha)
         self.T, self.d, self.E, self.K, self.F = T, d, E, K, F
@@ -51,6 +51,12 @@ class MoELayer:
         self.f = torch.empty(E, dtype=f32, device=dev)
         self.P = torch.empty(E, dtype=f32, device=dev)
         self.l_aux = torch.empty(1, dtype=f32, device=dev)
+        # independent work goes on a second stream: the shared expert (needs only x) runs
+        # beside routing and the routed experts, the aux statistics (need only the routing
+        # results) beside the expert GEMMs
+        self.overlap = overlap
+        self.side = torch.cuda.Stream(device=dev) if overlap else None
+        self.graph = None
         self.w2 = self._down_weights(w2)
         self.shared = w1s is not None
         self.w2s = self._down_weights(w2s) if self.shared else None
@@ -72,10 +78,11 @@ class MoELayer:
         return out
 
     @classmethod
-    def from_workload(cls, wl, inputs, device="cuda", renormalize=False):
+    def from_workload(cls, wl, inputs, device="cuda", renormalize=False, overlap=True):
         return cls(wl.T, wl.d, wl.E, wl.K, wl.F, wl.dtype, wl.capacity_factor, wl.alpha,
                    inputs["w_r"], inputs["b_r"], inputs["w1"], inputs["w2"],
-                   inputs.get("w1s"), inputs.get("w2s"), renormalize=renormalize, device=device)
+                   inputs.get("w1s"), inputs.get("w2s"), renormalize=renormalize, device=device,
+                   overlap=overlap)
 
     # ---------------------------------------------------------------- stages
     def route(self, x, stream=None, logits_in=None):
@@ -112,23 +119,106 @@ class MoELayer:
         N.aux_stats(self.cfg, self.counts, self.ws, self.f, self.P, self.l_aux, stream)
 
     # ---------------------------------------------------------------- whole layer
-    def forward(self, x, stream=None, logits_in=None):
-        """Enqueue the whole layer on ``stream``; returns the output buffer ``self.y``."""
-        self.route(x, stream, logits_in)
-        self.dispatch(x, stream)
-        self.experts_up(stream)
-        self.experts_down(stream)
+    def stage_names(self):
+        """Stages timed on the main stream, in order (with overlap the shared expert and
+        the aux statistics run on the side stream and are not separate stages)."""
+        names = ["route", "dispatch", "expert_up", "expert_down"]
+        if self.overlap:
+            return names + ["combine"]
         if self.shared:
-            self.shared_expert(x, stream)
-        self.combine(stream)
-        self.aux(stream)
+            names.append("shared_expert")
+        return names + ["combine", "aux"]
+
+    def forward(self, x, stream=None, logits_in=None, marks=None):
+        """Enqueue the whole layer; returns the output buffer ``self.y``.
+
+        With ``overlap`` the work goes on the current stream plus the layer's side stream,
+        forked and joined with events (so it can be captured in a CUDA graph); otherwise
+        everything goes on ``stream``.  ``marks``: optional len(stage_names()) + 1 CUDA
+        events recorded on the main stream before each stage and after the last one."""
+        def mark(i):
+            if marks is not None:
+                marks[i].record()
+        if not self.overlap:
+            mark(0)
+            self.route(x, stream, logits_in)
+            mark(1)
+            self.dispatch(x, stream)
+            mark(2)
+            self.experts_up(stream)
+            mark(3)
+            self.experts_down(stream)
+            i = 4
+            if self.shared:
+                mark(i)
+                self.shared_expert(x, stream)
+                i += 1
+            mark(i)
+            self.combine(stream)
+            mark(i + 1)
+            self.aux(stream)
+            mark(i + 2)
+            return self.y
+        main = torch.cuda.current_stream()
+        side = self.side
+        if self.shared:
+            fork = torch.cuda.Event()
+            fork.record(main)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                self.shared_expert(x)
+        mark(0)
+        self.route(x, None, logits_in)
+        mark(1)
+        self.dispatch(x)
+        routed = torch.cuda.Event()
+        routed.record(main)
+        side.wait_event(routed)
+        with torch.cuda.stream(side):
+            self.aux()
+        joined = torch.cuda.Event()
+        joined.record(side)
+        mark(2)
+        self.experts_up()
+        mark(3)
+        self.experts_down()
+        mark(4)
+        main.wait_event(joined)
+        self.combine()
+        mark(5)
         return self.y
 
-    def forward_host(self, x_host, y_host, x_dev, stream=None):
-        """End-to-end call with host buffers: copy x (pinned host) in, run the layer, copy
-        y back into pinned host memory, all on one stream."""
-        x_dev.copy_(x_host, non_blocking=True)
-        self.forward(x_dev, stream)
+    def capture(self, x, marks=None):
+        """Record the whole forward on the input buffer ``x`` as one CUDA graph, so a step
+        costs one launch instead of one per kernel.  ``marks`` (events created with
+        ``external=True``) become timing nodes inside the graph.  Returns the number of
+        library kernels one replay launches."""
+        self.forward(x)            # first use of every kernel happens outside capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        before = N.launch_count()
+        with torch.cuda.graph(graph):
+            self.forward(x, marks=marks)
+        self.graph = graph
+        self.graph_x = x
+        self.graph_kernels = N.launch_count() - before
+        return self.graph_kernels
+
+    def replay(self):
+        """Run the captured forward on the current stream."""
+        self.graph.replay()
+        return self.y
+
+    def forward_host(self, x_host, y_host, x_dev=None, stream=None):
+        """End-to-end call with host buffers: copy x (pinned host) in, run the layer (the
+        captured graph when there is one, into its input buffer), copy y back into pinned
+        host memory, all on the current stream."""
+        if self.graph is not None:
+            self.graph_x.copy_(x_host, non_blocking=True)
+            self.replay()
+        else:
+            x_dev.copy_(x_host, non_blocking=True)
+            self.forward(x_dev, stream)
         y_host.copy_(self.y, non_blocking=True)
         return y_host
 

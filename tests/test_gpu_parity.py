@@ -329,3 +329,30 @@ def _sampled_full_check(name, n_tokens=48, seed=0):
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3"])
 def test_full_size_sampled(name):
     _sampled_full_check(name)
+
+
+@pytest.mark.parametrize("idx,overlap", [(2, True), (4, True), (4, False)])
+def test_graph_replay_matches_eager(idx, overlap):
+    """The whole forward captured as one CUDA graph (timing events as graph nodes, with or
+    without the side-stream overlap) reproduces the serial eager forward bit for bit,
+    replay after replay."""
+    wl = SMALL[idx]
+    inp = make_inputs(wl, "cuda")
+    serial = MoELayer.from_workload(wl, inp, overlap=False)
+    serial.forward(inp["x"])
+    torch.cuda.synchronize()
+    y_ref = serial.y.clone()
+    l_ref = serial.l_aux.clone()
+    layer = MoELayer.from_workload(wl, inp, overlap=overlap)
+    marks = [torch.cuda.Event(enable_timing=True, external=True)
+             for _ in range(len(layer.stage_names()) + 1)]
+    n = layer.capture(inp["x"], marks=marks)
+    assert n >= 7
+    for _ in range(2):
+        layer.y.zero_()
+        layer.l_aux.zero_()
+        layer.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(layer.y, y_ref) and torch.equal(layer.l_aux, l_ref)
+        assert marks[0].elapsed_time(marks[-1]) > 0
+    layer.check_device_status()
