@@ -217,6 +217,8 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local)
     pk = peaks()
 
+    N.set_gemm_pairing({"auto": N.GEMM_AUTO, "single": N.GEMM_SINGLE, "pair": N.GEMM_PAIR,
+                        "split": N.GEMM_SPLIT}[args.gemm])
     inp = make_inputs(wl, dev, seed=0)
     layer = MoELayer.from_workload(wl, inp, device=dev)
     x = inp["x"]
@@ -356,6 +358,7 @@ def run_ours(args, wl):
         "config": {"workload": f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} K={wl.K} F={wl.F} "
                                f"{wl.dtype} capacity_factor={wl.capacity_factor}",
                    "capacity": layer.cfg.capacity, "parallelism": f"replicas x{world}",
+                   "expert_gemm": args.gemm,
                    "l2": "flushed before each step (512 MiB device write, outside the events)"},
         "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches, "gpu_launches_per_step": kernels_per_step,
@@ -409,6 +412,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral", choices=sorted(WORKLOADS))
+    ap.add_argument("--gemm", choices=["auto", "single", "pair", "split"], default="auto",
+                    help="expert GEMM kernels: one CTA per 128-row tile, CTA pairs per "
+                         "256-row tile, pairs for whole 256-row tiles + one CTA for the "
+                         "rest, or the library's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--cpu-rows", type=int, default=512)

@@ -34,8 +34,9 @@
  *   first, equal values -> lower expert id.  Routing weights are the softmax
  *   probabilities (cfg.renormalize = 1 divides them by their sum over the K picks).
  * - Drop order: an assignment is dropped iff its expert already holds C assignments
- *   earlier in flat order.  Rows inside an expert's packed block are in ascending
- *   flat order.  Routing, counts, offsets, slot and src are deterministic.
+ *   that arrived before it, in flat order unless cfg.drop_order says otherwise.  Rows
+ *   inside an expert's packed block are in arrival order.  Routing, counts, offsets,
+ *   slot and src are deterministic.
  * - Limits: 1 <= K <= min(E, 32), E <= 256, T >= 0 with T*K < 2^31; d and F multiples
  *   of 8 (bf16) or 4 (fp32).  Violations return MOE_ERR_INVALID / MOE_ERR_UNSUPPORTED.
  */
@@ -70,7 +71,14 @@ typedef struct {
   int32_t capacity;     /* C per expert; < 0 means no dropping */
   int32_t renormalize;  /* 0: w = softmax prob (default); 1: w / sum_k w */
   float alpha;          /* aux-loss weight */
+  int32_t drop_order;   /* moe_drop_order_t: the order assignments arrive at experts */
 } moe_config;
+
+/* Arrival order that decides which assignments a full expert drops and the row order
+ * inside an expert's packed block.  TOKEN_MAJOR (default): flat order a = t*K + k.
+ * SLOT_MAJOR: every token's k-th choice arrives before any token's (k+1)-th choice
+ * (order k*T + t), so first choices are dropped last. */
+typedef enum { MOE_DROP_TOKEN_MAJOR = 0, MOE_DROP_SLOT_MAJOR = 1 } moe_drop_order_t;
 
 /* Bytes of device workspace `ws` the calls below need for this config.  The caller
  * allocates it and ZERO-FILLS it once before first use; the library keeps it
@@ -93,6 +101,26 @@ int64_t moe_rows_capacity(const moe_config* cfg);
  *            that moe_aux_stats reduces. */
 moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
                        float* logits, int32_t* topk_ids, float* topk_w, void* ws, void* stream);
+
+/* Step 1 with a selection-only expert bias: the auxiliary-loss-free balancing that
+ * "Expert Parallelism (EP)", "Load balancing" names for DeepSeek-V3 (a per-expert bias
+ * adjusted to balance the load instead of an auxiliary loss).  Same as moe_route, except
+ * that the top-K choice compares fl32(logit + sel_bias[e]) (ties -> lower id) while the
+ * routing weights and the probability sums for P_i stay those of the unbiased softmax.
+ *   sel_bias [E] fp32 device pointer, required (4-byte aligned). */
+moe_status_t moe_route_select_bias(const moe_config* cfg, const void* x, const void* w_r,
+                                   const float* b_r, const float* sel_bias, float* logits,
+                                   int32_t* topk_ids, float* topk_w, void* ws, void* stream);
+
+/* Nudge the selection bias toward balance after a step (the bias-adjustment scheme of
+ * the same section; the pages name it without a formula, and this rule is the reading
+ * taken here): sel_bias[i] += gamma * sign(T*K/E - counts[i]) -- lowered for experts
+ * above the mean load, raised below it, unchanged at it (the comparison is exact, in
+ * integers), each sum rounded once to fp32.
+ *   counts [E] int32 (pre-drop counts from moe_dispatch), sel_bias [E] fp32 in/out,
+ *   gamma >= 0 and finite, else MOE_ERR_INVALID. */
+moe_status_t moe_adjust_select_bias(const moe_config* cfg, const int32_t* counts, float* sel_bias,
+                                    float gamma, void* stream);
 
 /* Step 2 -- histogram, capacity, drop mask and dispatch permutation
  * ("The All-to-All Communication", "Top-K Routing and Capacity Factor").
@@ -189,6 +217,27 @@ moe_status_t moe_bf16_to_f16(const void* src, void* dst, int64_t n, void* ws, vo
 /* Synchronise `stream`, then return and clear the device status word in `ws`
  * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE), or MOE_ERR_CUDA if a kernel failed. */
 moe_status_t moe_sync_status(void* ws, void* stream);
+
+/* Which tensor-core kernels run the expert GEMMs of MOE_BF16 layers (moe_expert_up /
+ * moe_expert_down).  Not a step of the layer: a process-wide performance setting.
+ *   MOE_GEMM_SINGLE one CTA per 128-row tile (tcgen05 cta_group::1);
+ *   MOE_GEMM_PAIR   two CTAs per 256-row tile (tcgen05 cta_group::2: one MMA over two
+ *                   SMs, each SM loading half of the operands), which pads each group
+ *                   to a multiple of 256 rows;
+ *   MOE_GEMM_SPLIT  pairs for each group's whole 256-row tiles, then one CTA per 128-row
+ *                   tile for the remaining rows (two launches on the stream);
+ *   MOE_GEMM_AUTO   (default) pairs when the 256-row padding is at most 5% of the rows
+ *                   (judged from the capacity; the output width must be a multiple of
+ *                   256), one CTA otherwise.
+ * Every choice sums the same products in the same order, so results are identical.
+ * Returns MOE_ERR_INVALID for any other value.  Calls already enqueued are unaffected. */
+typedef enum {
+  MOE_GEMM_AUTO = 0,
+  MOE_GEMM_SINGLE = 1,
+  MOE_GEMM_PAIR = 2,
+  MOE_GEMM_SPLIT = 3
+} moe_gemm_pairing_t;
+moe_status_t moe_set_gemm_pairing(int32_t mode);
 
 /* Human-readable name of a status code (static storage). */
 const char* moe_status_string(moe_status_t status);

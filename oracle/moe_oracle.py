@@ -43,12 +43,27 @@ Readings taken where the pages are silent, garbled or inconsistent:
   never added to Y.
 * The shared expert (DeepSeek-V3 style) has weight 1 and is added to Y for every token.
 
+Routing variants (readings; the pages name these schemes without fixing them):
+
+* Selection-only expert bias ([EPH] "Load balancing": DeepSeek-V3's auxiliary-loss-free
+  bias-adjustment scheme).  A per-expert bias b_i is added to the fp32 logits (one fp32
+  addition, round to nearest even) for choosing the top-K experts only; routing weights
+  and P_i stay those of the unbiased softmax.  After a step the bias is nudged toward
+  balance: b_i <- b_i + gamma * sign(T*K/E - count_i) (raise under-loaded experts, lower
+  over-loaded ones; an expert at exactly the mean keeps its bias), one fp32 addition.
+* Slot-major drop priority: assignments arrive in the order a' = k*T + t (every token's
+  first choice before any second choice), instead of flat token-major order; rows of
+  an expert's packed block follow the same arrival order.
+* Capacity counted in assignments: C_K = floor((T*K / E) * capacity_factor), the reading
+  under which "capacity is rarely hit" when the load is balanced.
+
 Parity is pinned for every function here by the CPU tests (worked dispatch example,
 closed forms of the aux loss, the E=1 reduction to the dense FFN, brute-force dense
 evaluation, brute-force top-K and capacity, tabulated values of the normal CDF).  The
-two optional variants (``renormalize=True`` and any drop order other than flat order)
-are readings, not fixed by the pages: for them parity is unpinned beyond the
-definition.
+variants above and ``renormalize=True`` are readings, not fixed by the pages: the tests
+pin the oracle to those readings (reductions to the default path, brute force, hand
+cases), but parity with the pages is unpinned for them beyond the reading; for the
+bias adjustment rule in particular it is "parity unpinned".
 """
 
 from __future__ import annotations
@@ -93,14 +108,25 @@ def softmax(L32) -> np.ndarray:
     return e / e.sum(axis=1, keepdims=True)
 
 
-def top_k(L32, K: int) -> np.ndarray:
+def selection_scores(L32, sel_bias=None) -> np.ndarray:
+    """Scores the top-K choice compares: the fp32 logits, or with a selection-only bias
+    (DeepSeek-V3's bias-adjustment scheme, [EPH] "Load balancing") the fp32 sum
+    L32 + b, rounded once to fp32."""
+    L32 = np.asarray(L32, dtype=np.float32)
+    if sel_bias is None:
+        return L32
+    return (L32 + np.asarray(sel_bias, dtype=np.float32)[None, :]).astype(np.float32)
+
+
+def top_k(L32, K: int, sel_bias=None) -> np.ndarray:
     """Top-K experts per token ([EPM] "MoE Layer Structure": "the top-K experts are
-    activated"; [EPH] step 1).  Order: fp32 logit descending, ties -> lower expert id.
+    activated"; [EPH] step 1).  Order: fp32 score descending, ties -> lower expert id;
+    the score is the logit, plus the selection-only bias when one is given.
 
     A stable sort of the negated fp32 values keeps equal values in index order.
     """
-    L32 = np.asarray(L32, dtype=np.float32)
-    order = np.argsort(-L32, axis=1, kind="stable")
+    S = selection_scores(L32, sel_bias)
+    order = np.argsort(-S, axis=1, kind="stable")
     return order[:, :K].astype(np.int32)
 
 
@@ -125,24 +151,51 @@ def capacity(T: int, E: int, capacity_factor) -> int:
     return math.floor(Fraction(T) / E * Fraction(capacity_factor))
 
 
-def dispatch_plan(ids, E: int, C: int):
+def capacity_assignments(T: int, E: int, K: int, capacity_factor) -> int:
+    """C_K = floor((T * K / E) * capacity_factor) exactly: the capacity read as counting
+    top-K assignments rather than tokens (variant).  ``None`` -> -1 (no dropping)."""
+    if capacity_factor is None:
+        return -1
+    return math.floor(Fraction(T * K) / E * Fraction(capacity_factor))
+
+
+def arrival_order(T: int, K: int, order: str = "token") -> np.ndarray:
+    """Flat assignment indices a = t*K + k in the order assignments arrive at the
+    experts: token-major (t, then k) by default; "slot" is slot-major (k, then t)."""
+    a = np.arange(T * K, dtype=np.int64)
+    if order == "token":
+        return a
+    if order == "slot":
+        return a.reshape(T, K).T.reshape(-1)
+    raise ValueError(order)
+
+
+def dispatch_plan(ids, E: int, C: int, order: str = "token"):
     """Histogram, capacity, drop mask and the packing permutation.
 
-    Walk the assignments in flat order a = t*K + k.  An assignment's position in its
-    expert is the number of earlier assignments to the same expert; it is kept iff that
-    position is below C (C < 0: keep all).  Kept rows of expert e are packed
-    contiguously at rows [offsets[e], offsets[e+1]) in ascending flat order -- on one
+    Walk the assignments in arrival order (flat order a = t*K + k; ``order="slot"``:
+    every token's k-th choice before any (k+1)-th).  An assignment's position in its
+    expert is the number of assignments to the same expert that arrived before it; it
+    is kept iff that position is below C (C < 0: keep all).  Kept rows of expert e are
+    packed contiguously at rows [offsets[e], offsets[e+1]) in arrival order -- on one
     GPU this packing is what the all-to-all dispatch of [EPM] "The All-to-All
     Communication" and [EPH] step 2 amounts to.
 
     Returns dict with counts [E] (before dropping), kept [E], offsets [E+1], pos [A],
     slot [A] (packed row or -1 if dropped) and src [R] (packed row -> flat assignment).
     """
-    flat = np.asarray(ids, dtype=np.int64).reshape(-1)
+    ids_arr = np.asarray(ids, dtype=np.int64)
+    flat = ids_arr.reshape(-1)
     A = flat.size
+    if order == "token":
+        arrivals = np.arange(A, dtype=np.int64)
+    else:
+        if ids_arr.ndim != 2:
+            raise ValueError("slot-major arrival needs ids shaped [T, K]")
+        arrivals = arrival_order(ids_arr.shape[0], ids_arr.shape[1], order)
     counts = np.zeros(E, dtype=np.int64)
     pos = np.zeros(A, dtype=np.int64)
-    for a in range(A):
+    for a in arrivals:
         e = flat[a]
         pos[a] = counts[e]
         counts[e] += 1
@@ -238,15 +291,34 @@ def aux_stats(ids, p, E: int, alpha: float):
 
 
 # --------------------------------------------------------------------------------------
+# Selection-bias adjustment: [EPH] "Load balancing" (DeepSeek-V3's auxiliary-loss-free
+# bias-adjustment scheme; the update rule is a reading, see the module docstring).
+# --------------------------------------------------------------------------------------
+def adjust_selection_bias(sel_bias, counts, T: int, K: int, gamma: float) -> np.ndarray:
+    """b_i + gamma * sign(T*K/E - count_i), each sum rounded once to fp32.
+
+    The comparison with the mean load T*K/E is exact (count_i * E against T*K in
+    integers): an expert above the mean is lowered by gamma, one below is raised, one at
+    the mean keeps its bias."""
+    b = np.asarray(sel_bias, dtype=np.float32)
+    counts = np.asarray(counts, dtype=np.int64)
+    E = b.size
+    sign = np.sign(T * K - counts * E).astype(np.float32)
+    return (b + np.float32(gamma) * sign).astype(np.float32)
+
+
+# --------------------------------------------------------------------------------------
 # The whole layer.
 # --------------------------------------------------------------------------------------
 def moe_forward(x, w_r, b_r, w1, w2, K: int, C: int, alpha: float,
-                renormalize: bool = False, shared=None, logits32=None):
+                renormalize: bool = False, shared=None, logits32=None, sel_bias=None,
+                order: str = "token"):
     """Forward pass of one MoE FFN layer, every intermediate returned.
 
     x [T,d]; w_r [E,d]; b_r [E] or None; w1 [E,F,d]; w2 [E,d,F];
     shared = (w1s [F,d], w2s [d,F]) or None; logits32 [T,E] float32 replaces the router
-    when given (the routing stages are then driven by those exact fp32 values).
+    when given (the routing stages are then driven by those exact fp32 values);
+    sel_bias [E] fp32: selection-only bias; order: arrival order for dropping.
     """
     x = np.asarray(x)
     T = x.shape[0]
@@ -256,9 +328,9 @@ def moe_forward(x, w_r, b_r, w1, w2, K: int, C: int, alpha: float,
     else:
         L32 = np.asarray(logits32, dtype=np.float32)
     p = softmax(L32)
-    ids = top_k(L32, K)
+    ids = top_k(L32, K, sel_bias)
     w = routing_weights(p, ids, renormalize)
-    plan = dispatch_plan(ids, E, C)
+    plan = dispatch_plan(ids, E, C, order)
     R = plan["R"]
     src = plan["src"].astype(np.int64)
     d = x.shape[1]

@@ -10,10 +10,13 @@ namespace moe {
 
 cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, int32_t* ids,
                                 float* w, float* ppart, int nblk, const float* lpart, int nsplit,
-                                const float* bias, cudaStream_t st);
+                                const float* bias, const float* sel_bias, cudaStream_t st);
+cudaError_t launch_adjust_select_bias(const int32_t* counts, float* sel_bias, int E, int64_t A,
+                                      float gamma, cudaStream_t st);
 cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsigned long long* desc,
                         int32_t* pos, int32_t* counts, int32_t* offsets, uint32_t* hdr,
-                        int skip_block, int spin_limit, cudaStream_t st);
+                        int skip_block, int spin_limit, int slot_major, int Tn, int K,
+                        cudaStream_t st);
 cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const int32_t* pos,
                             const int32_t* offsets, int Tn, int d, int E, int K, int C,
                             int32_t* slot, int32_t* src, void* xp, int64_t rows_cap, uint32_t* hdr,
@@ -30,11 +33,11 @@ cudaError_t launch_simt_grouped(int dtype, const void* A, const void* B, void* C
 cudaError_t launch_simt_router(int dtype, const void* x, const void* w_r, const float* b_r,
                                float* logits, int T, int E, int d, uint32_t* hdr, cudaStream_t st);
 cudaError_t launch_tc_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets, int G,
-                         int N, int Kd, int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr,
-                         int num_sms, cudaStream_t st);
+                         int N, int Kd, int64_t rows_cap, int64_t cap_per_group, int pair_mode,
+                         uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
                            int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
-                           uint32_t* hdr, int num_sms, cudaStream_t st);
+                           int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, float* out, int T,
                              int E, int d, int nsplit, uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_bf16_to_f16(const void* src, void* dst, int64_t n, uint32_t* hdr, int num_sms,
@@ -45,6 +48,7 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 static std::atomic<int> g_skip_block{-1};
 static std::atomic<int> g_spin_limit{1 << 21};
+static std::atomic<int> g_gemm_pairing{MOE_GEMM_AUTO};
 
 static int num_sms() {
   static int cached[64] = {0};
@@ -65,6 +69,8 @@ static moe_status_t check_cfg(const moe_config* c) {
   if (c->T < 0 || c->d <= 0 || c->E <= 0 || c->K <= 0 || c->F <= 0) return MOE_ERR_INVALID;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID;
   if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID;
+  if (c->drop_order != MOE_DROP_TOKEN_MAJOR && c->drop_order != MOE_DROP_SLOT_MAJOR)
+    return MOE_ERR_INVALID;
   if (c->K > c->E) return MOE_ERR_INVALID;
   if (c->E > 256 || c->K > 32) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->K >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
@@ -110,8 +116,9 @@ int64_t moe_rows_capacity(const moe_config* cfg) {
   return rows_capacity(*cfg);
 }
 
-moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
-                       float* logits, int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
+static moe_status_t route_impl(const moe_config* cfg, const void* x, const void* w_r,
+                               const float* b_r, const float* sel_bias, float* logits,
+                               int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
@@ -121,6 +128,7 @@ moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, co
     return MOE_ERR_INVALID;
   if (x != nullptr && (w_r == nullptr || !aligned16(x) || !aligned16(w_r))) return MOE_ERR_INVALID;
   if (b_r != nullptr && !aligned16(b_r)) return MOE_ERR_INVALID;
+  if (sel_bias != nullptr && ((uintptr_t)sel_bias & 3u)) return MOE_ERR_INVALID;
   cudaStream_t st = (cudaStream_t)stream;
   const WsLayout L = ws_layout(c);
   uint32_t* hdr = (uint32_t*)ws;
@@ -141,7 +149,31 @@ moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, co
   }
   return cuda_status(launch_softmax_topk(logits, c.T, c.E, c.K, c.renormalize, topk_ids, topk_w,
                                          (float*)((char*)ws + L.ppart), L.nblk_route, lpart,
-                                         L.router_splits, b_r, st));
+                                         L.router_splits, b_r, sel_bias, st));
+}
+
+moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
+                       float* logits, int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
+  return route_impl(cfg, x, w_r, b_r, nullptr, logits, topk_ids, topk_w, ws, stream);
+}
+
+moe_status_t moe_route_select_bias(const moe_config* cfg, const void* x, const void* w_r,
+                                   const float* b_r, const float* sel_bias, float* logits,
+                                   int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
+  if (sel_bias == nullptr) return MOE_ERR_INVALID;
+  return route_impl(cfg, x, w_r, b_r, sel_bias, logits, topk_ids, topk_w, ws, stream);
+}
+
+moe_status_t moe_adjust_select_bias(const moe_config* cfg, const int32_t* counts, float* sel_bias,
+                                    float gamma, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!counts || !sel_bias || ((uintptr_t)counts & 3u) || ((uintptr_t)sel_bias & 3u))
+    return MOE_ERR_INVALID;
+  if (!(gamma >= 0.0f) || isinf(gamma)) return MOE_ERR_INVALID;
+  return cuda_status(launch_adjust_select_bias(counts, sel_bias, cfg->E,
+                                               (int64_t)cfg->T * cfg->K, gamma,
+                                               (cudaStream_t)stream));
 }
 
 moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_ids,
@@ -175,7 +207,7 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
   int32_t* pos = (int32_t*)((char*)ws + L.pos);
   s = cuda_status(launch_scan(topk_ids, A, c.E, c.capacity, L.nblk_scan,
                               (unsigned long long*)((char*)ws + L.desc), pos, counts, offsets, hdr,
-                              skip, spin, st));
+                              skip, spin, c.drop_order, c.T, c.K, st));
   if (s != MOE_OK) return s;
   return cuda_status(launch_dispatch(c.dtype, x, topk_ids, pos, offsets, c.T, c.d, c.E, c.K,
                                      c.capacity, slot, src, x_perm, rows_capacity(c), hdr,
@@ -205,8 +237,8 @@ moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int3
   const moe_config& c = *cfg;
   if (c.dtype == MOE_BF16)
     return cuda_status(launch_tc_up(x_perm, w1, h, offsets, n_groups, c.F, c.d, rows_cap,
-                                    group_row_bound(c, n_groups, rows_cap), (uint32_t*)ws,
-                                    num_sms(), (cudaStream_t)stream));
+                                    group_row_bound(c, n_groups, rows_cap), g_gemm_pairing.load(),
+                                    (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
   return cuda_status(launch_simt_grouped(c.dtype, x_perm, w1, h, offsets, n_groups, c.F, c.d,
                                          rows_cap, true, (uint32_t*)ws, (cudaStream_t)stream));
 }
@@ -220,8 +252,8 @@ moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t
   const moe_config& c = *cfg;
   if (c.dtype == MOE_BF16)
     return cuda_status(launch_tc_down(h, w2, y_perm, offsets, n_groups, c.d, c.F, rows_cap,
-                                      group_row_bound(c, n_groups, rows_cap), (uint32_t*)ws,
-                                      num_sms(), (cudaStream_t)stream));
+                                      group_row_bound(c, n_groups, rows_cap), g_gemm_pairing.load(),
+                                      (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
   return cuda_status(launch_simt_grouped(c.dtype, h, w2, y_perm, offsets, n_groups, c.d, c.F,
                                          rows_cap, false, (uint32_t*)ws, (cudaStream_t)stream));
 }
@@ -300,6 +332,14 @@ const char* moe_status_string(moe_status_t st) {
 }
 
 uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+moe_status_t moe_set_gemm_pairing(int32_t mode) {
+  if (mode != MOE_GEMM_AUTO && mode != MOE_GEMM_SINGLE && mode != MOE_GEMM_PAIR &&
+      mode != MOE_GEMM_SPLIT)
+    return MOE_ERR_INVALID;
+  g_gemm_pairing.store(mode);
+  return MOE_OK;
+}
 
 void moe_test_arm_scan_timeout(int32_t skip_block, int32_t spin_limit) {
   g_spin_limit.store(spin_limit > 0 ? spin_limit : 1);

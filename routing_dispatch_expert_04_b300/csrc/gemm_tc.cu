@@ -22,37 +22,12 @@
 // zeros).  Every mbarrier wait is bounded: after WAIT_LIMIT_NS the CTA records a timeout
 // in the status word, every role leaves its loop, in-flight copies and MMAs are awaited
 // (bounded), TMEM is freed and the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_fp16.h>
-#include <math.h>
-
-#include "common.cuh"
-#include "tc_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 using namespace tc;
 
 constexpr int TC_BM = 128;
-constexpr int TC_BK = 64;            // 64 bf16/fp16 = one 128-byte swizzle row
-constexpr int TC_THREADS = 192;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
-constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
-
-enum { TC_EPI_GELU_F16 = 0, TC_EPI_F32 = 1, TC_EPI_BIAS_F32 = 2 };
-
-struct TcArgs {
-  const int32_t* offsets;  // [G+1] device, or nullptr: one group of M rows
-  int G, M, N, Kd;
-  int64_t rows_cap;
-  void* out;               // [rows_cap, ldo] (times ksplit partial slices)
-  int ldo;
-  const float* bias;       // [N] or nullptr (added only when ksplit == 1)
-  uint32_t* hdr;           // status word
-  int ksplit;              // K split across CTAs: slice s holds the partial sum of k-blocks
-  int kpb;                 //   [s*kpb, min(nkb, (s+1)*kpb)); ksplit*kpb covers nkb, no slice empty
-  int64_t split_stride;    // elements between the partial slices of `out`
-};
 
 template <int BN, int STAGES>
 struct TcLayout {
@@ -64,65 +39,11 @@ struct TcLayout {
   static constexpr int NBAR = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], done
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int GRP_OFF = MISC_OFF + 16;
-  static constexpr int TOTAL = GRP_OFF + 4 * 257 * 4;
+  static constexpr int TOTAL = GRP_OFF + (int)sizeof(GroupTable);
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
                                        : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
 };
-
-// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           uint32_t* hdr) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-      *abort_flag = 1;
-      raise_error(hdr, DEV_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// Wait used only while draining after an abort: ignores the abort flag, shorter limit.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > DRAIN_LIMIT_NS) return;
-  }
-}
-
-struct TileInfo {
-  int g;
-  int row0;
-  int rowend;
-  int n0;
-};
-
-__device__ __forceinline__ TileInfo decode_tile(int t, int G, const int* s_lo, const int* s_hi,
-                                                const int* s_mt, const int* s_tpre, int BN) {
-  int lo = 0, hi = G;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s_tpre[mid] <= t) lo = mid;
-    else hi = mid;
-  }
-  const int g = lo;
-  const int local = t - s_tpre[g];
-  const int mt = s_mt[g];
-  TileInfo ti;
-  ti.g = g;
-  ti.row0 = s_lo[g] + (local % mt) * TC_BM;
-  ti.rowend = s_hi[g];
-  ti.n0 = (local / mt) * BN;
-  return ti;
-}
-
-__device__ __forceinline__ float gelu_exact(float v) {
-  return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
-}
 
 template <int BN, int STAGES, int EPI, bool F16IN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -139,10 +60,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint64_t* done = bars + 2 * STAGES + 4;
   uint32_t* s_tmem = (uint32_t*)(smem + Lay::MISC_OFF);
   volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
-  int* s_lo = (int*)(smem + Lay::GRP_OFF);
-  int* s_hi = s_lo + 257;
-  int* s_mt = s_hi + 257;
-  int* s_tpre = s_mt + 257;
+  GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
@@ -165,40 +83,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     tma_prefetch_desc(&tmap_b);
   }
   if (warp == 0) {
-    // per-group row ranges (clamped to the buffer), m-tiles and tile prefix
-    int carry = 0;
-    for (int base = 0; base < G; base += 32) {
-      const int g = base + lane;
-      int lo = 0, hi = 0, mt = 0;
-      if (g < G) {
-        if (args.offsets == nullptr) {
-          lo = 0;
-          hi = args.M;
-        } else {
-          lo = args.offsets[g];
-          hi = args.offsets[g + 1];
-        }
-        if (hi > args.rows_cap) {
-          raise_error(args.hdr, DEV_ERR_OVERFLOW);
-          hi = (int)args.rows_cap;
-        }
-        if (lo < 0) lo = 0;
-        if (lo > hi) lo = hi;
-        mt = (hi - lo + TC_BM - 1) / TC_BM;
-        s_lo[g] = lo;
-        s_hi[g] = hi;
-        s_mt[g] = mt;
-      }
-      int v = mt * n_tiles;  // inclusive warp scan of tiles
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      if (g < G) s_tpre[g + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    if (lane == 0) s_tpre[0] = 0;
+    build_group_table<TC_BM>(tab, args, n_tiles, lane);
   } else if (warp == 1) {
     tmem_alloc(s_tmem, Lay::TMEM_COLS);
     tmem_relinquish();
@@ -208,7 +93,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int ksplit = args.ksplit;
-  const int total = s_tpre[G] * ksplit;
+  const int total = tab->tpre[G] * ksplit;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -218,7 +103,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       int issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(t / ksplit, G, s_lo, s_hi, s_mt, s_tpre, BN);
+        const TileInfo ti = decode_tile<TC_BM>(t / ksplit, G, tab, BN);
         const int brow = ti.g * args.N + ti.n0;
         const int kb0 = (t % ksplit) * args.kpb;
         const int kb1 = min(nkb, kb0 + args.kpb);
@@ -299,7 +184,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int r_in_tile = q * 32 + lane;
     uint32_t acc = 0, aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile(t / ksplit, G, s_lo, s_hi, s_mt, s_tpre, BN);
+      const TileInfo ti = decode_tile<TC_BM>(t / ksplit, G, tab, BN);
       const int64_t slice = (int64_t)(t % ksplit) * args.split_stride;
       const float* bias = ksplit == 1 ? args.bias : nullptr;
       if (!wait_phase(&tfull[acc], aph, s_abort, args.hdr)) break;
@@ -314,40 +199,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
         tmem_ld_wait();
         if (!valid) continue;
-        if (EPI == TC_EPI_GELU_F16) {
-          __half* out = (__half*)args.out + (size_t)row * args.ldo + col0;
-          bool bad = false;
-#pragma unroll
-          for (int v8 = 0; v8 < 4; ++v8) {
-            if (col0 + v8 * 8 >= args.N) break;
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float a = gelu_exact(__uint_as_float(r[v8 * 8 + 2 * i]));
-              const float b = gelu_exact(__uint_as_float(r[v8 * 8 + 2 * i + 1]));
-              bad |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
-              __half2 h2 = __floats2half2_rn(a, b);
-              w[i] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            st_v4(out + v8 * 8, make_uint4(w[0], w[1], w[2], w[3]));
-          }
-          if (bad) raise_error(args.hdr, DEV_ERR_RANGE);
-        } else if (EPI == TC_EPI_F32) {
-          float* out = (float*)args.out + slice + (size_t)row * args.ldo + col0;
-#pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4) {
-            if (col0 + v4 * 4 >= args.N) break;
-            st_v4(out + v4 * 4, make_uint4(r[v4 * 4], r[v4 * 4 + 1], r[v4 * 4 + 2], r[v4 * 4 + 3]));
-          }
-        } else {
-          float* out = (float*)args.out + slice + (size_t)row * args.ldo;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = col0 + i;
-            if (col < args.N)
-              out[col] = __uint_as_float(r[i]) + (bias != nullptr ? bias[col] : 0.f);
-          }
-        }
+        if (epilogue_chunk<EPI>(r, row, col0, args, slice, bias)) raise_error(args.hdr, DEV_ERR_RANGE);
       }
       tc_fence_before();
       __syncwarp();
@@ -364,7 +216,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 }
 
 // ------------------------------------------------------------------ host side
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
     void* p = nullptr;
@@ -377,10 +229,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D tensor map of a row-major [outer, inner] 16-bit matrix, box [box_outer, 64].
-static bool make_map(CUtensorMap* m, const void* base, bool f16, uint64_t inner, uint64_t outer,
-                     uint32_t box_outer) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+bool tc_make_map(CUtensorMap* m, const void* base, bool f16, uint64_t inner, uint64_t outer,
+                 uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tc_encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
@@ -406,8 +257,8 @@ static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int 
   }
   CUtensorMap ma, mb;
   const int64_t a_rows = a.rows_cap > 0 ? a.rows_cap : 1;
-  if (!make_map(&ma, A, F16IN, (uint64_t)a.Kd, (uint64_t)a_rows, TC_BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, B, F16IN, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN)) return cudaErrorInvalidValue;
+  if (!tc_make_map(&ma, A, F16IN, (uint64_t)a.Kd, (uint64_t)a_rows, TC_BM)) return cudaErrorInvalidValue;
+  if (!tc_make_map(&mb, B, F16IN, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN)) return cudaErrorInvalidValue;
   const int64_t n_tiles = (a.N + BN - 1) / BN;
   const int64_t m_bound = (a.rows_cap + TC_BM - 1) / TC_BM + (a.offsets ? a.G : 0);
   int64_t grid = m_bound * n_tiles * a.ksplit;
@@ -447,24 +298,75 @@ static int pick_bn(int64_t rows_cap, int G, int64_t cap_per_group, int N, int nu
   return best_bn;
 }
 
+cudaError_t launch_tc2_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
+                          int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
+                          int num_sms, cudaStream_t st);
+cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
+                            int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
+                            int num_sms, cudaStream_t st);
+
+// How the expert GEMM's rows are split between the kernels: one CTA per 128-row tile
+// for all rows, CTA pairs per 256-row tile for all rows, or pairs for each group's whole
+// 256-row tiles and one CTA per 128-row tile for the rest.  A one-CTA 128x256 MMA reads
+// 96 B/clk of operands from shared memory and its TMA stages write as much again, more
+// than the SM's shared memory delivers, which caps the tensor pipe near two thirds; a
+// pair MMA reads and stages half of B per SM.  But pairs pad a group to a multiple of
+// 256 rows, and the split's second launch waits for the first one's tail.  Measured on
+// the layer shapes (B300), pairs win only where that padding is small, so MOE_GEMM_AUTO
+// takes pairs when the padding is at most 5% (judged from the per-group row bound, when
+// known, and with N filling 256-wide tiles) and one CTA otherwise.
+enum { PLAN_SINGLE = 0, PLAN_PAIR = 1, PLAN_SPLIT = 2 };
+
+static int gemm_plan(int mode, int64_t rows_cap, int G, int64_t cap_per_group, int N) {
+  if (mode == MOE_GEMM_SINGLE) return PLAN_SINGLE;
+  if (mode == MOE_GEMM_PAIR) return PLAN_PAIR;
+  if (mode == MOE_GEMM_SPLIT) return PLAN_SPLIT;
+  if (N % 256 != 0 || cap_per_group <= 0) return PLAN_SINGLE;
+  const int64_t per = cap_per_group < rows_cap ? cap_per_group : rows_cap;
+  const int64_t rows128 = (int64_t)G * ((per + 127) / 128) * 128;
+  const int64_t rows256 = (int64_t)G * ((per + 255) / 256) * 256;
+  return rows256 * 100 <= rows128 * 105 ? PLAN_PAIR : PLAN_SINGLE;
+}
+
+template <int EPI, bool F16IN>
+static cudaError_t launch_tc_single(const void* A, const void* B, void* out, const int32_t* offsets,
+                                    int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
+                                    int row_part, uint32_t* hdr, int num_sms, cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, out, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
+           row_part};
+  if (pick_bn(rows_cap, G, cap_per_group, N, num_sms) == 192)
+    return launch_tc<192, 5, EPI, F16IN>(A, B, a, num_sms, st);
+  return launch_tc<256, 4, EPI, F16IN>(A, B, a, num_sms, st);
+}
+
 // First expert Linear, bf16 in, GELU fused, fp16 out: h[r] = GELU(x_perm[r] . W1[g]^T).
 cudaError_t launch_tc_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets, int G,
-                         int N, int Kd, int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr,
-                         int num_sms, cudaStream_t st) {
-  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0};
-  if (pick_bn(rows_cap, G, cap_per_group, N, num_sms) == 192)
-    return launch_tc<192, 5, TC_EPI_GELU_F16, false>(x_perm, w1, a, num_sms, st);
-  return launch_tc<256, 4, TC_EPI_GELU_F16, false>(x_perm, w1, a, num_sms, st);
+                         int N, int Kd, int64_t rows_cap, int64_t cap_per_group, int pair_mode,
+                         uint32_t* hdr, int num_sms, cudaStream_t st) {
+  const int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_SINGLE)
+    return launch_tc_single<TC_EPI_GELU_F16, false>(x_perm, w1, h, offsets, G, N, Kd, rows_cap,
+                                                    cap_per_group, TC_ROWS_ALL, hdr, num_sms, st);
+  cudaError_t e = launch_tc2_up(x_perm, w1, h, offsets, G, N, Kd, rows_cap,
+                                plan == PLAN_PAIR ? TC_ROWS_ALL : TC_ROWS_FULL256, hdr, num_sms, st);
+  if (e != cudaSuccess || plan == PLAN_PAIR) return e;
+  return launch_tc_single<TC_EPI_GELU_F16, false>(x_perm, w1, h, offsets, G, N, Kd, rows_cap,
+                                                  G > 0 ? 255 : 0, TC_ROWS_REST256, hdr, num_sms, st);
 }
 
 // Second expert Linear, fp16 in, fp32 out: y_perm[r] = h[r] . W2[g]^T.
 cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
                            int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
-                           uint32_t* hdr, int num_sms, cudaStream_t st) {
-  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0};
-  if (pick_bn(rows_cap, G, cap_per_group, N, num_sms) == 192)
-    return launch_tc<192, 5, TC_EPI_F32, true>(h, w2h, a, num_sms, st);
-  return launch_tc<256, 4, TC_EPI_F32, true>(h, w2h, a, num_sms, st);
+                           int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st) {
+  const int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_SINGLE)
+    return launch_tc_single<TC_EPI_F32, true>(h, w2h, y_perm, offsets, G, N, Kd, rows_cap,
+                                              cap_per_group, TC_ROWS_ALL, hdr, num_sms, st);
+  cudaError_t e = launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap,
+                                  plan == PLAN_PAIR ? TC_ROWS_ALL : TC_ROWS_FULL256, hdr, num_sms, st);
+  if (e != cudaSuccess || plan == PLAN_PAIR) return e;
+  return launch_tc_single<TC_EPI_F32, true>(h, w2h, y_perm, offsets, G, N, Kd, rows_cap,
+                                            G > 0 ? 255 : 0, TC_ROWS_REST256, hdr, num_sms, st);
 }
 
 // Router Linear, bf16 in, fp32 logits: logits[t] = x[t] . W_r^T + b_r.  With nsplit > 1
@@ -475,7 +377,8 @@ cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, f
   const int nkb = (d + TC_BK - 1) / TC_BK;
   const int kpb = (nkb + nsplit - 1) / nsplit;
   const int ks = (nkb + kpb - 1) / kpb;
-  TcArgs a{nullptr, 1, T, E, d, (int64_t)T, out, E, b_r, hdr, ks, kpb, (int64_t)T * E};
+  TcArgs a{nullptr, 1, T, E, d, (int64_t)T, out, E, b_r, hdr, ks, kpb, (int64_t)T * E,
+           TC_ROWS_ALL};
   // the epilogue reads TMEM 32 columns at a time, so the narrowest tile is 32 wide
   if (E <= 32) return launch_tc<32, 8, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
   if (E <= 64) return launch_tc<64, 8, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);

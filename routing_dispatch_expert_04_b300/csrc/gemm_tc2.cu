@@ -1,0 +1,269 @@
+// Grouped GEMM on CTA pairs: tcgen05.mma.cta_group::2 over two SMs, sm_103a.
+//
+// Same computation and tile list as the one-CTA kernel (gemm_tc.cu) -- the expert FFN
+// of "Expert Parallelism (MoE)", "MoE Layer Structure", for all experts in one launch --
+// with 256-row tiles computed by a cluster of two CTAs:
+//   - each CTA TMA-loads its own 128 rows of the A tile and its own half (BN/2 rows) of
+//     the B tile into its shared memory, so a CTA streams 32 KB per 64-deep k-block
+//     instead of 48 KB, and six stages fit where the one-CTA kernel holds four;
+//   - the even CTA issues one M=256 x N=BN MMA that reads both CTAs' stages; each CTA's
+//     TMEM receives its 128 rows of the accumulator (two accumulators of BN columns);
+//   - both CTAs' copies signal the even CTA's "full" barrier (it expects both CTAs'
+//     bytes); its MMA commits arrive on the "empty" and "accumulator full" barriers of
+//     both CTAs; both CTAs' epilogue warps arrive on the even CTA's "accumulator empty"
+//     barrier, which therefore counts 8 warps.
+// Roles per CTA: warp 0 TMA producer, warp 1 TMEM owner (+ MMA issuer in the even CTA),
+// warps 2..5 epilogue (same fused GELU / fp32 epilogues as the one-CTA kernel).
+// Every mbarrier wait is bounded (the CTA records a timeout and leaves its loops); the
+// pair meets at a cluster barrier before TMEM is freed, so neither CTA exits while the
+// other's MMAs or copies may still touch its shared memory or TMEM.
+#include "tc_common.cuh"
+
+namespace moe {
+using namespace tc;
+
+constexpr int TC2_BM = 256;      // rows per pair tile
+constexpr int TC2_CTA_ROWS = 128;
+
+template <int BN, int STAGES>
+struct Tc2Layout {
+  static constexpr int A_BYTES = TC2_CTA_ROWS * TC_BK * 2;
+  static constexpr int B_BYTES = (BN / 2) * TC_BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int B_OFF = STAGES * A_BYTES;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NBAR = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], done
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int GRP_OFF = MISC_OFF + 16;
+  static constexpr int TOTAL = GRP_OFF + (int)sizeof(GroupTable);
+  static constexpr int ALLOC = TOTAL + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // BN in {128, 256}
+  static_assert(BN == 128 || BN == 256, "pair tiles are 128 or 256 wide");
+};
+
+// Time an aborting CTA gives copies it cannot observe (they signal the other CTA's
+// barrier) to land before its shared memory is released.
+constexpr uint64_t PAIR_ABORT_SETTLE_NS = 200000ull;
+
+template <int BN, int STAGES, int EPI, bool F16IN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b, const TcArgs args) {
+  using Lay = Tc2Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + Lay::BAR_OFF);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* done = bars + 2 * STAGES + 4;
+  uint32_t* s_tmem = (uint32_t*)(smem + Lay::MISC_OFF);
+  volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
+  GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int G = args.G;
+  const int n_tiles = (args.N + BN - 1) / BN;
+  const int nkb = (args.Kd + TC_BK - 1) / TC_BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 8);
+    }
+    mbar_init(done, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 0) {
+    build_group_table<TC2_BM>(tab, args, n_tiles, lane);
+  } else if (warp == 1) {
+    tmem_alloc_pair(s_tmem, Lay::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  // barriers of both CTAs initialised and TMEM allocated before anyone uses them
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total = tab->tpre[G];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = cluster; t < total && ok; t += n_clusters) {
+        const TileInfo ti = decode_tile<TC2_BM>(t, G, tab, BN);
+        const int arow = ti.row0 + (int)rank * TC2_CTA_ROWS;
+        const int brow = ti.g * args.N + ti.n0 + (int)rank * (BN / 2);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * Lay::A_BYTES;
+          uint8_t* sb = smem + Lay::B_OFF + s * Lay::B_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Lay::STAGE_BYTES);
+          const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's full[s]
+          tma_load_2d_pair(sa, &tmap_a, fb, kb * TC_BK, arow);
+          tma_load_2d_pair(sb, &tmap_b, fb, kb * TC_BK, brow);
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        if (rank == 0) {  // the even CTA can see its stages complete
+          for (int i = 0; i < STAGES && i < issued; ++i) {
+            if (--s < 0) {
+              s = STAGES - 1;
+              ph ^= 1u;
+            }
+            drain_wait(&full[s], ph);
+          }
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < PAIR_ABORT_SETTLE_NS) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t IDESC = F16IN ? (idesc_bf16_f32(TC2_BM, BN) & ~((7u << 7) | (7u << 10)))
+                                       : idesc_bf16_f32(TC2_BM, BN);
+      int s = 0;
+      uint32_t ph = 0, acc = 0, aph = 0;
+      bool ok = true;
+      for (int t = cluster; t < total && ok; t += n_clusters) {
+        if (!wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_phase(&full[s], ph, s_abort, args.hdr)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
+          const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < TC_BK / 16; ++k) {
+            mma_f16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), IDESC,
+                         (kb != 0 || k != 0) ? 1u : 0u);
+          }
+          mma_commit_pair_mc(&empty[s], (uint16_t)3);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(&tfull[acc], (uint16_t)3);
+        acc ^= 1u;
+        if (acc == 0) aph ^= 1u;
+      }
+      // every MMA issued by this thread has completed once `done` flips
+      mma_commit_pair_local(done);
+      drain_wait(done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_in_tile = (int)rank * TC2_CTA_ROWS + q * 32 + lane;
+    uint32_t acc = 0, aph = 0;
+    for (int t = cluster; t < total; t += n_clusters) {
+      const TileInfo ti = decode_tile<TC2_BM>(t, G, tab, BN);
+      if (!wait_phase(&tfull[acc], aph, s_abort, args.hdr)) break;
+      tc_fence_after();
+      const int row = ti.row0 + r_in_tile;
+      const bool valid = row < ti.rowend;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = ti.n0 + c * 32;
+        if (col0 >= args.N) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
+        tmem_ld_wait();
+        if (!valid) continue;
+        if (epilogue_chunk<EPI>(r, row, col0, args, 0, nullptr)) raise_error(args.hdr, DEV_ERR_RANGE);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      acc ^= 1u;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, Lay::TMEM_COLS);
+}
+
+template <int BN, int STAGES, int EPI, bool F16IN>
+static cudaError_t launch_tc2(const void* A, const void* B, const TcArgs& a, int num_sms,
+                              cudaStream_t st) {
+  using Lay = Tc2Layout<BN, STAGES>;
+  static bool attr_set = false;
+  auto kern = tc2_grouped_gemm_kernel<BN, STAGES, EPI, F16IN>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap ma, mb;
+  const int64_t a_rows = a.rows_cap > 0 ? a.rows_cap : 1;
+  if (!tc_make_map(&ma, A, F16IN, (uint64_t)a.Kd, (uint64_t)a_rows, TC2_CTA_ROWS))
+    return cudaErrorInvalidValue;
+  if (!tc_make_map(&mb, B, F16IN, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN / 2))
+    return cudaErrorInvalidValue;
+  const int64_t n_tiles = (a.N + BN - 1) / BN;
+  const int64_t m_bound = (a.rows_cap + TC2_BM - 1) / TC2_BM + (a.offsets ? a.G : 0);
+  int64_t clusters = m_bound * n_tiles;
+  if (clusters > num_sms / 2) clusters = num_sms / 2;
+  if (clusters < 1) clusters = 1;
+  kern<<<(unsigned)(2 * clusters), TC_THREADS, Lay::ALLOC, st>>>(ma, mb, a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// First expert Linear on CTA pairs, bf16 in, GELU fused, fp16 out, over the rows that
+// `row_part` selects.
+cudaError_t launch_tc2_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
+                          int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
+                          int num_sms, cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
+           row_part};
+  return launch_tc2<256, 6, TC_EPI_GELU_F16, false>(x_perm, w1, a, num_sms, st);
+}
+
+// Second expert Linear on CTA pairs, fp16 in, fp32 out.
+cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
+                            int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
+                            int num_sms, cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
+           row_part};
+  return launch_tc2<256, 6, TC_EPI_F32, true>(h, w2h, a, num_sms, st);
+}
+
+}  // namespace moe

@@ -21,7 +21,8 @@ namespace moe {
 
 cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsigned long long* desc,
                         int32_t* pos, int32_t* counts, int32_t* offsets, uint32_t* hdr,
-                        int skip_block, int spin_limit, cudaStream_t st);
+                        int skip_block, int spin_limit, int slot_major, int Tn, int K,
+                        cudaStream_t st);
 cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const int32_t* pos,
                             const int32_t* offsets, int Tn, int d, int E, int K, int C,
                             int32_t* slot, int32_t* src, void* xp, int64_t rows_cap, uint32_t* hdr,
@@ -114,7 +115,7 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config* cfg, const void* 
   uint32_t* hdr = (uint32_t*)base;
   int32_t* pos = (int32_t*)(base + L.pos);
   e = launch_scan(topk_ids, A, c.E, c.capacity, L.nblk_scan, (unsigned long long*)(base + L.desc),
-                  pos, counts, offsets, hdr, -1, 1 << 21, st);
+                  pos, counts, offsets, hdr, -1, 1 << 21, c.drop_order, c.T, c.K, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   int64_t rows_cap = A;
   if (c.capacity >= 0 && (int64_t)c.E * c.capacity < rows_cap) rows_cap = (int64_t)c.E * c.capacity;

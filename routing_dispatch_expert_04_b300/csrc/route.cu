@@ -6,6 +6,10 @@
 // softmax).  Selection compares the fp32 logits: higher first, equal values go to the
 // lower expert id, so the picks are a deterministic function of the fp32 logits.
 //
+// With a selection-only bias (DeepSeek-V3's auxiliary-loss-free balancing, "Expert
+// Parallelism (EP)", "Load balancing") the choice compares logit + bias, while the
+// weights and the probability sums stay those of the unbiased softmax.
+//
 // The kernel also leaves, per block, the sum over its tokens of every expert's
 // probability; the aux-statistics kernel reduces those partial sums in a fixed order
 // to P_i, so the result is deterministic without floating-point atomics.
@@ -21,12 +25,17 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32)
 softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
                     int32_t* __restrict__ ids, float* __restrict__ wout,
                     float* __restrict__ ppart, const float* __restrict__ lpart, int nsplit,
-                    const float* __restrict__ bias) {
+                    const float* __restrict__ bias, const float* __restrict__ sel_bias) {
   __shared__ float s_p[ROUTE_WARPS][VPT * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float pacc[VPT];
+  float sb[VPT];  // selection-only bias of this lane's experts (0 without one)
 #pragma unroll
-  for (int j = 0; j < VPT; ++j) pacc[j] = 0.f;
+  for (int j = 0; j < VPT; ++j) {
+    const int e = lane + 32 * j;
+    pacc[j] = 0.f;
+    sb[j] = (sel_bias != nullptr && e < E) ? sel_bias[e] : 0.f;
+  }
 
   const int t0 = blockIdx.x * ROUTE_TOKENS + warp * ROUTE_TPW;
   // the warp's token rows are loaded up front: one memory latency for all of them.  With
@@ -83,7 +92,11 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
       p[j] = p[j] / s;
       pacc[j] += p[j];
     }
-    // top-K: K rounds of a warp arg-max under (value desc, id asc)
+    // top-K: K rounds of a warp arg-max under (score desc, id asc); the score is the
+    // logit, plus the selection-only bias when there is one (one fp32 addition)
+    float sc[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) sc[j] = (sel_bias != nullptr) ? __fadd_rn(v[j], sb[j]) : v[j];
     uint32_t taken = 0;
     int my_id = 0;
     float my_w = 0.f, wsum = 0.f;
@@ -93,8 +106,8 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
 #pragma unroll
       for (int j = 0; j < VPT; ++j) {
         const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < bi))) {
-          bv = v[j];
+        if (e < E && !((taken >> j) & 1u) && (sc[j] > bv || (sc[j] == bv && e < bi))) {
+          bv = sc[j];
           bi = e;
         }
       }
@@ -141,16 +154,35 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
 // partial slices of lpart (+ bias), and are also written to `logits`.
 cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, int32_t* ids,
                                 float* w, float* ppart, int nblk, const float* lpart, int nsplit,
-                                const float* bias, cudaStream_t st) {
+                                const float* bias, const float* sel_bias, cudaStream_t st) {
   const dim3 grid(nblk), block(ROUTE_WARPS * 32);
   if (E <= 32)
-    softmax_topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias);
+    softmax_topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias, sel_bias);
   else if (E <= 64)
-    softmax_topk_kernel<2><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias);
+    softmax_topk_kernel<2><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias, sel_bias);
   else if (E <= 128)
-    softmax_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias);
+    softmax_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias, sel_bias);
   else
-    softmax_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias);
+    softmax_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias, sel_bias);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// Selection-bias adjustment after a step: b_i += gamma * sign(T*K/E - count_i), the
+// comparison with the mean load done exactly in integers, the sum rounded once to fp32.
+__global__ void adjust_select_bias_kernel(const int32_t* __restrict__ counts,
+                                          float* __restrict__ sel_bias, int E, int64_t A,
+                                          float gamma) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const int64_t diff = A - (int64_t)counts[e] * E;
+  const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.f);
+  sel_bias[e] = __fadd_rn(sel_bias[e], step);
+}
+
+cudaError_t launch_adjust_select_bias(const int32_t* counts, float* sel_bias, int E, int64_t A,
+                                      float gamma, cudaStream_t st) {
+  adjust_select_bias_kernel<<<(E + 255) / 256, 256, 0, st>>>(counts, sel_bias, E, A, gamma);
   count_launch();
   return cudaGetLastError();
 }

@@ -6,10 +6,12 @@
 // routing, every token is sent to the holder of each chosen expert; on one GPU the
 // all-to-all becomes a permutation that packs each expert's rows contiguously.
 //
-// Order fixed here: assignments are taken in flat order a = t*K + k.  An assignment's
-// position in its expert is the number of earlier assignments to the same expert; it
-// is kept iff that position is below C, and kept rows of expert e are packed at
-// offsets[e] + position.  The result is unique, so it can be compared bit for bit.
+// Order fixed here: assignments arrive in flat order a = t*K + k (or, with the
+// slot-major drop priority, every token's k-th choice before any (k+1)-th).  An
+// assignment's position in its expert is the number of assignments to the same expert
+// that arrived before it; it is kept iff that position is below C, and kept rows of
+// expert e are packed at offsets[e] + position.  The result is unique, so it can be
+// compared bit for bit.
 //
 // scan_kernel -- one pass over the flat id stream.  Each block takes a chunk of
 // SCAN_ITEMS assignments (chunk index drawn from an atomic ticket, so every block it
@@ -40,10 +42,17 @@ __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned l
 constexpr unsigned long long FLAG_AGG = 1ull << 32;   // this chunk's own totals
 constexpr unsigned long long FLAG_INCL = 2ull << 32;  // totals of chunks 0..this one
 
+// Flat assignment index (t*K + k) of the i-th assignment in arrival order: token-major
+// (the identity) or slot-major (every token's k-th choice before any (k+1)-th).
+__device__ __forceinline__ int64_t arrival_to_flat(int64_t i, int slot_major, int Tn, int K) {
+  return slot_major ? (i % Tn) * K + i / Tn : i;
+}
+
 __global__ void __launch_bounds__(SCAN_THREADS)
 scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
             unsigned long long* desc, int32_t* __restrict__ pos, int32_t* __restrict__ counts,
-            int32_t* __restrict__ offsets, uint32_t* hdr, int skip_block, int spin_limit) {
+            int32_t* __restrict__ offsets, uint32_t* hdr, int skip_block, int spin_limit,
+            int slot_major, int Tn, int K) {
   constexpr int NW = SCAN_THREADS / 32;
   constexpr int WITEMS = SCAN_IPT * 32;  // each warp ranks one contiguous segment
   __shared__ int s_wrun[NW][256];        // per-warp running count of e, then warp base
@@ -66,7 +75,7 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
 #pragma unroll
   for (int r = 0; r < SCAN_IPT; ++r) {
     const int64_t a = wbase + r * 32 + lane;
-    my_e[r] = (a < A) ? ids[a] : -1;
+    my_e[r] = (a < A) ? ids[arrival_to_flat(a, slot_major, Tn, K)] : -1;
   }
 #pragma unroll
   for (int r = 0; r < SCAN_IPT; ++r) {
@@ -138,7 +147,8 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
 
 #pragma unroll
   for (int r = 0; r < SCAN_IPT; ++r) {
-    if (my_e[r] >= 0) pos[wbase + r * 32 + lane] = s_excl[my_e[r]] + my_r[r];
+    if (my_e[r] >= 0)
+      pos[arrival_to_flat(wbase + r * 32 + lane, slot_major, Tn, K)] = s_excl[my_e[r]] + my_r[r];
   }
 
   if (b == nblk - 1) {  // block-uniform
@@ -215,9 +225,10 @@ dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids,
 
 cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsigned long long* desc,
                         int32_t* pos, int32_t* counts, int32_t* offsets, uint32_t* hdr,
-                        int skip_block, int spin_limit, cudaStream_t st) {
+                        int skip_block, int spin_limit, int slot_major, int Tn, int K,
+                        cudaStream_t st) {
   scan_kernel<<<nblk, SCAN_THREADS, 0, st>>>(ids, A, E, C, nblk, desc, pos, counts, offsets, hdr,
-                                              skip_block, spin_limit);
+                                              skip_block, spin_limit, slot_major, Tn, K);
   count_launch();
   return cudaGetLastError();
 }

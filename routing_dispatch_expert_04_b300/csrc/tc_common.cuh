@@ -1,0 +1,204 @@
+// Pieces shared by the one-CTA and the CTA-pair tcgen05 grouped GEMMs: the argument
+// block, bounded mbarrier waits, the ragged (group, n-tile, m-tile) tile list built on
+// the device from `offsets`, the fused epilogues and the TMA descriptor encoding.
+//
+// The GEMM is the expert FFN of "Expert Parallelism (MoE)", "MoE Layer Structure" (each
+// expert applies Linear(d -> 4d) -> GELU -> Linear(4d -> d)) run for all experts in one
+// launch ("Expert Parallelism (EP)", step 3: expert GEMMs compute locally):
+//   C[r, n] = epi( sum_k A[r, k] * B[g*N + n, k] ),  r in [offsets[g], offsets[g+1]).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+constexpr int TC_BK = 64;  // 64 bf16/fp16 = one 128-byte swizzle row
+constexpr int TC_THREADS = 192;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
+constexpr int TC_MAX_GROUPS = 256;
+
+enum { TC_EPI_GELU_F16 = 0, TC_EPI_F32 = 1, TC_EPI_BIAS_F32 = 2 };
+
+struct TcArgs {
+  const int32_t* offsets;  // [G+1] device, or nullptr: one group of M rows
+  int G, M, N, Kd;
+  int64_t rows_cap;
+  void* out;               // [rows_cap, ldo] (times ksplit partial slices)
+  int ldo;
+  const float* bias;       // [N] or nullptr (added only when ksplit == 1)
+  uint32_t* hdr;           // status word
+  int ksplit;              // K split across CTAs: slice s holds the partial sum of k-blocks
+  int kpb;                 //   [s*kpb, min(nkb, (s+1)*kpb)); ksplit*kpb covers nkb, no slice empty
+  int64_t split_stride;    // elements between the partial slices of `out`
+  int row_part;            // rows of each group this launch covers: 0 all; 1 the leading
+                           //   whole 256-row tiles; 2 the rest (fewer than 256 rows)
+};
+
+constexpr int TC_ROWS_ALL = 0, TC_ROWS_FULL256 = 1, TC_ROWS_REST256 = 2;
+
+// Group table in shared memory: row range, m-tile count and tile prefix per group.
+struct GroupTable {
+  int lo[TC_MAX_GROUPS + 1];
+  int hi[TC_MAX_GROUPS + 1];
+  int mt[TC_MAX_GROUPS + 1];
+  int tpre[TC_MAX_GROUPS + 1];
+};
+
+// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           uint32_t* hdr) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::globaltimer_ns();
+  while (true) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (tc::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      raise_error(hdr, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Wait used only while draining after an abort: ignores the abort flag, shorter limit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = tc::globaltimer_ns();
+  while (!tc::mbar_try_wait(bar, parity)) {
+    if (tc::globaltimer_ns() - t0 > DRAIN_LIMIT_NS) return;
+  }
+}
+
+// One warp fills the group table: rows clamped to the buffer, m-tiles of BM rows, and
+// the exclusive prefix of tiles (mt * n_tiles) over the groups.
+template <int BM>
+__device__ __forceinline__ void build_group_table(GroupTable* tab, const TcArgs& args, int n_tiles,
+                                                  int lane) {
+  int carry = 0;
+  for (int base = 0; base < args.G; base += 32) {
+    const int g = base + lane;
+    int lo = 0, hi = 0, mt = 0;
+    if (g < args.G) {
+      if (args.offsets == nullptr) {
+        lo = 0;
+        hi = args.M;
+      } else {
+        lo = args.offsets[g];
+        hi = args.offsets[g + 1];
+      }
+      if (hi > args.rows_cap) {
+        raise_error(args.hdr, DEV_ERR_OVERFLOW);
+        hi = (int)args.rows_cap;
+      }
+      if (lo < 0) lo = 0;
+      if (lo > hi) lo = hi;
+      if (args.row_part != TC_ROWS_ALL) {
+        const int whole = ((hi - lo) / 256) * 256;
+        if (args.row_part == TC_ROWS_FULL256) hi = lo + whole;
+        else lo += whole;
+      }
+      mt = (hi - lo + BM - 1) / BM;
+      tab->lo[g] = lo;
+      tab->hi[g] = hi;
+      tab->mt[g] = mt;
+    }
+    int v = mt * n_tiles;  // inclusive warp scan of tiles
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (g < args.G) tab->tpre[g + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+  if (lane == 0) tab->tpre[0] = 0;
+}
+
+struct TileInfo {
+  int g;
+  int row0;
+  int rowend;
+  int n0;
+};
+
+// Tile t of the list: groups in order, inside a group n-tiles in order, inside an
+// n-tile m-tiles in order (m fastest, so CTAs that run together share the weight box).
+template <int BM>
+__device__ __forceinline__ TileInfo decode_tile(int t, int G, const GroupTable* tab, int BN) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tab->tpre[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int g = lo;
+  const int local = t - tab->tpre[g];
+  const int mt = tab->mt[g];
+  TileInfo ti;
+  ti.g = g;
+  ti.row0 = tab->lo[g] + (local % mt) * BM;
+  ti.rowend = tab->hi[g];
+  ti.n0 = (local / mt) * BN;
+  return ti;
+}
+
+__device__ __forceinline__ float gelu_exact(float v) {
+  return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
+}
+
+// Epilogue for 32 accumulator columns [col0, col0+32) of one output row, held by this
+// thread in r[] (fp32 bit patterns).  Returns true if a GELU output left the fp16 range.
+template <int EPI>
+__device__ __forceinline__ bool epilogue_chunk(const uint32_t (&r)[32], int row, int col0,
+                                               const TcArgs& args, int64_t slice,
+                                               const float* bias) {
+  bool bad = false;
+  if (EPI == TC_EPI_GELU_F16) {
+    __half* out = (__half*)args.out + (size_t)row * args.ldo + col0;
+#pragma unroll
+    for (int v8 = 0; v8 < 4; ++v8) {
+      if (col0 + v8 * 8 >= args.N) break;
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = gelu_exact(__uint_as_float(r[v8 * 8 + 2 * i]));
+        const float b = gelu_exact(__uint_as_float(r[v8 * 8 + 2 * i + 1]));
+        bad |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
+        __half2 h2 = __floats2half2_rn(a, b);
+        w[i] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      st_v4(out + v8 * 8, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+  } else if (EPI == TC_EPI_F32) {
+    float* out = (float*)args.out + slice + (size_t)row * args.ldo + col0;
+#pragma unroll
+    for (int v4 = 0; v4 < 8; ++v4) {
+      if (col0 + v4 * 4 >= args.N) break;
+      st_v4(out + v4 * 4, make_uint4(r[v4 * 4], r[v4 * 4 + 1], r[v4 * 4 + 2], r[v4 * 4 + 3]));
+    }
+  } else {
+    float* out = (float*)args.out + slice + (size_t)row * args.ldo;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int col = col0 + i;
+      if (col < args.N) out[col] = __uint_as_float(r[i]) + (bias != nullptr ? bias[col] : 0.f);
+    }
+  }
+  return bad;
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn();
+
+// 2-D tensor map of a row-major [outer, inner] 16-bit matrix, box [box_outer, 64],
+// 128-byte swizzle.
+bool tc_make_map(CUtensorMap* m, const void* base, bool f16, uint64_t inner, uint64_t outer,
+                 uint32_t box_outer);
+
+}  // namespace moe

@@ -22,9 +22,21 @@ from . import native as N
 
 class MoELayer:
     def __init__(self, T, d, E, K, F, dtype, capacity_factor, alpha, w_r, b_r, w1, w2,
-                 w1s=None, w2s=None, renormalize=False, device="cuda", overlap=True):
-        self.cfg = N.make_config(T, d, E, K, F, dtype, N.capacity(T, E, capacity_factor),
-                                 renormalize, alpha)
+                 w1s=None, w2s=None, renormalize=False, device="cuda", overlap=True,
+                 drop_order="token", capacity_mode="tokens", sel_bias=None):
+        """``drop_order``: "token" (flat order) or "slot" (first choices first) decides which
+        assignments a full expert drops.  ``capacity_mode``: "tokens" gives the capacity as
+        printed, C = floor(T/E * cf); "assignments" counts top-K assignments,
+        C = floor(T*K/E * cf).  ``sel_bias``: optional [E] fp32 device tensor, a
+        selection-only expert bias (see :meth:`adjust_selection_bias`)."""
+        if capacity_mode == "tokens":
+            C = N.capacity(T, E, capacity_factor)
+        elif capacity_mode == "assignments":
+            C = N.capacity_assignments(T, E, K, capacity_factor)
+        else:
+            raise ValueError(capacity_mode)
+        self.cfg = N.make_config(T, d, E, K, F, dtype, C, renormalize, alpha, drop_order)
+        self.sel_bias = sel_bias
         self.T, self.d, self.E, self.K, self.F = T, d, E, K, F
         self.dtype = torch.float32 if dtype == "f32" else torch.bfloat16
         self.device = torch.device(device)
@@ -78,11 +90,13 @@ class MoELayer:
         return out
 
     @classmethod
-    def from_workload(cls, wl, inputs, device="cuda", renormalize=False, overlap=True):
+    def from_workload(cls, wl, inputs, device="cuda", renormalize=False, overlap=True,
+                      drop_order="token", capacity_mode="tokens", sel_bias=None):
         return cls(wl.T, wl.d, wl.E, wl.K, wl.F, wl.dtype, wl.capacity_factor, wl.alpha,
                    inputs["w_r"], inputs["b_r"], inputs["w1"], inputs["w2"],
                    inputs.get("w1s"), inputs.get("w2s"), renormalize=renormalize, device=device,
-                   overlap=overlap)
+                   overlap=overlap, drop_order=drop_order, capacity_mode=capacity_mode,
+                   sel_bias=sel_bias)
 
     # ---------------------------------------------------------------- stages
     def route(self, x, stream=None, logits_in=None):
@@ -90,9 +104,21 @@ class MoELayer:
         skipped and those logits drive the routing."""
         if logits_in is not None:
             self.logits.copy_(logits_in)
-            N.route(self.cfg, None, None, None, self.logits, self.ids, self.w, self.ws, stream)
+            x, w_r, b_r = None, None, None
         else:
-            N.route(self.cfg, x, self.w_r, self.b_r, self.logits, self.ids, self.w, self.ws, stream)
+            w_r, b_r = self.w_r, self.b_r
+        if self.sel_bias is None:
+            N.route(self.cfg, x, w_r, b_r, self.logits, self.ids, self.w, self.ws, stream)
+        else:
+            N.route_select_bias(self.cfg, x, w_r, b_r, self.sel_bias, self.logits, self.ids,
+                                self.w, self.ws, stream)
+
+    def adjust_selection_bias(self, gamma: float, stream=None):
+        """After a forward: nudge the selection-only bias toward balance from this step's
+        pre-drop counts (lower over-loaded experts, raise under-loaded ones by gamma)."""
+        if self.sel_bias is None:
+            raise ValueError("the layer has no selection bias")
+        N.adjust_select_bias(self.cfg, self.counts, self.sel_bias, gamma, stream)
 
     def dispatch(self, x, stream=None):
         N.dispatch(self.cfg, x, self.ids, self.counts, self.offsets, self.slot, self.src,

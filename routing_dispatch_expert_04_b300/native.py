@@ -20,11 +20,12 @@ MOE_F32, MOE_BF16 = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
           4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_DEVICE"}
 
-EXPORTS = ("moe_workspace_size", "moe_rows_capacity", "moe_route", "moe_dispatch",
+EXPORTS = ("moe_workspace_size", "moe_rows_capacity", "moe_route", "moe_route_select_bias",
+           "moe_adjust_select_bias", "moe_dispatch",
            "moe_dispatch_noalloc",
            "moe_expert_up", "moe_expert_down", "moe_grouped_ffn", "moe_combine",
            "moe_aux_stats", "moe_bf16_to_f16", "moe_sync_status", "moe_status_string", "moe_launch_count",
-           "moe_test_arm_scan_timeout")
+           "moe_test_arm_scan_timeout", "moe_set_gemm_pairing")
 
 
 class MoeError(RuntimeError):
@@ -37,7 +38,7 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("F", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("capacity", ctypes.c_int32), ("renormalize", ctypes.c_int32),
-                ("alpha", ctypes.c_float)]
+                ("alpha", ctypes.c_float), ("drop_order", ctypes.c_int32)]
 
 
 _lib = None
@@ -47,6 +48,8 @@ _SIGS = {
     "moe_workspace_size": (ctypes.c_size_t, [_CFG]),
     "moe_rows_capacity": (ctypes.c_int64, [_CFG]),
     "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route_select_bias": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_adjust_select_bias": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, _P]),
     "moe_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_up": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P]),
@@ -60,6 +63,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_launch_count": (ctypes.c_uint64, []),
     "moe_test_arm_scan_timeout": (None, [ctypes.c_int32, ctypes.c_int32]),
+    "moe_set_gemm_pairing": (ctypes.c_int, [ctypes.c_int32]),
 }
 
 
@@ -86,9 +90,23 @@ def capacity(T: int, E: int, capacity_factor) -> int:
     return math.floor(Fraction(T) / E * Fraction(capacity_factor))
 
 
-def make_config(T, d, E, K, F, dtype, capacity=-1, renormalize=False, alpha=0.01) -> MoeConfig:
+DROP_TOKEN_MAJOR, DROP_SLOT_MAJOR = 0, 1
+
+
+def capacity_assignments(T: int, E: int, K: int, capacity_factor) -> int:
+    """C_K = floor((T * K / E) * capacity_factor) exactly (capacity counting top-K
+    assignments instead of tokens); -1 for None."""
+    if capacity_factor is None:
+        return -1
+    return math.floor(Fraction(T * K) / E * Fraction(capacity_factor))
+
+
+def make_config(T, d, E, K, F, dtype, capacity=-1, renormalize=False, alpha=0.01,
+                drop_order=DROP_TOKEN_MAJOR) -> MoeConfig:
     dt = {"f32": MOE_F32, "bf16": MOE_BF16}[dtype] if isinstance(dtype, str) else int(dtype)
-    return MoeConfig(T, d, E, K, F, dt, capacity, int(bool(renormalize)), alpha)
+    if isinstance(drop_order, str):
+        drop_order = {"token": DROP_TOKEN_MAJOR, "slot": DROP_SLOT_MAJOR}[drop_order]
+    return MoeConfig(T, d, E, K, F, dt, capacity, int(bool(renormalize)), alpha, int(drop_order))
 
 
 def _ptr(t) -> int | None:
@@ -122,6 +140,17 @@ def rows_capacity(cfg: MoeConfig) -> int:
 def route(cfg, x, w_r, b_r, logits, topk_ids, topk_w, ws, stream=None):
     _check("moe_route", lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(b_r), _ptr(logits),
                                          _ptr(topk_ids), _ptr(topk_w), _ptr(ws), _stream(stream)))
+
+
+def route_select_bias(cfg, x, w_r, b_r, sel_bias, logits, topk_ids, topk_w, ws, stream=None):
+    _check("moe_route_select_bias", lib().moe_route_select_bias(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(b_r), _ptr(sel_bias), _ptr(logits),
+        _ptr(topk_ids), _ptr(topk_w), _ptr(ws), _stream(stream)))
+
+
+def adjust_select_bias(cfg, counts, sel_bias, gamma: float, stream=None):
+    _check("moe_adjust_select_bias", lib().moe_adjust_select_bias(
+        ctypes.byref(cfg), _ptr(counts), _ptr(sel_bias), float(gamma), _stream(stream)))
 
 
 def dispatch(cfg, x, topk_ids, counts, offsets, slot, src, x_perm, ws, stream=None):
@@ -176,6 +205,15 @@ def sync_status(ws, stream=None) -> int:
 
 def launch_count() -> int:
     return lib().moe_launch_count()
+
+
+GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR, GEMM_SPLIT = 0, 1, 2, 3
+
+
+def set_gemm_pairing(mode: int):
+    """Kernel choice for the bf16 expert GEMMs: GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR or
+    GEMM_SPLIT (pairs for whole 256-row tiles, one CTA for the rest)."""
+    _check("moe_set_gemm_pairing", lib().moe_set_gemm_pairing(mode))
 
 
 def arm_scan_timeout(skip_block: int, spin_limit: int):

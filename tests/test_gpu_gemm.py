@@ -30,6 +30,14 @@ def _gen(shape, std, seed, dtype):
     return (torch.randn(*shape, generator=g, device="cuda") * std).to(dtype)
 
 
+@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT], ids=["single", "pair", "split"])
+def pairing(request):
+    """Run the case on the one-CTA kernel, the CTA-pair kernel and the split of the two."""
+    N.set_gemm_pairing(request.param)
+    yield request.param
+    N.set_gemm_pairing(N.GEMM_AUTO)
+
+
 CASES = [
     # (name, offsets, Kd (=d for up), N (=F for up))
     ("one_tile", [0, 128], 64, 256),
@@ -37,11 +45,12 @@ CASES = [
     ("multi_tile_ragged_m", [0, 300], 320, 768),
     ("groups_empty_and_single_row", [0, 0, 130, 131, 400, 520], 136, 384),
     ("many_groups", list(np.cumsum([0] + [37 * (i % 5) for i in range(40)])), 256, 512),
+    ("pair_tiles_ragged", [0, 600, 600, 856, 1111, 1367], 1024, 512),
 ]
 
 
 @pytest.mark.parametrize("name,offs,Kd,Nn", CASES, ids=[c[0] for c in CASES])
-def test_expert_up_gelu_f16(name, offs, Kd, Nn):
+def test_expert_up_gelu_f16(name, offs, Kd, Nn, pairing):
     G = len(offs) - 1
     rows = int(offs[-1])
     rows_cap = rows + 64  # spare rows must stay untouched
@@ -63,7 +72,7 @@ def test_expert_up_gelu_f16(name, offs, Kd, Nn):
 
 
 @pytest.mark.parametrize("name,offs,Kd,Nn", CASES, ids=[c[0] for c in CASES])
-def test_expert_down_f32(name, offs, Kd, Nn):
+def test_expert_down_f32(name, offs, Kd, Nn, pairing):
     G = len(offs) - 1
     rows = int(offs[-1])
     rows_cap = rows + 64
@@ -117,3 +126,35 @@ def test_f16_conversion_exact_and_range_error():
     src[100] = 70000.0
     N.bf16_to_f16(src, dst, ws)
     assert N.sync_status(ws) == 5
+
+
+@pytest.mark.parametrize("fn", ["up", "down"])
+def test_single_and_pair_kernels_agree_bitwise(fn):
+    """Both kernels multiply the same operands and accumulate the 64-deep k-blocks in the
+    same order; their outputs are compared bit for bit."""
+    offs = [0, 300, 812, 813, 1400]
+    G, rows, Kd, Nn = 4, 1400, 512, 768
+    rows_cap = rows + 16
+    cfg = N.make_config(rows, Kd if fn == "up" else Nn, G, 1, Nn if fn == "up" else Kd, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
+    outs = []
+    for mode in (N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT):
+        N.set_gemm_pairing(mode)
+        try:
+            if fn == "up":
+                a = _gen((rows_cap, Kd), 1.0, 11, torch.bfloat16)
+                w = _gen((G, Nn, Kd), Kd ** -0.5, 12, torch.bfloat16)
+                out = torch.zeros((rows_cap, Nn), dtype=torch.float16, device="cuda")
+                N.expert_up(cfg, a, off_t, G, rows_cap, w, out, ws)
+            else:
+                a = _gen((rows_cap, Kd), 0.5, 13, torch.float16)
+                w = _gen((G, Nn, Kd), Kd ** -0.5, 14, torch.float16)
+                out = torch.zeros((rows_cap, Nn), dtype=torch.float32, device="cuda")
+                N.expert_down(cfg, a, off_t, G, rows_cap, w, out, ws)
+        finally:
+            N.set_gemm_pairing(N.GEMM_AUTO)
+        assert N.sync_status(ws) == 0
+        outs.append(out.cpu())
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(outs[0], outs[2])

@@ -36,9 +36,9 @@ def _lib():
     N.lib()
 
 
-def _routing_only(T, E, K, C, L32, renorm=False):
+def _routing_only(T, E, K, C, L32, renorm=False, sel_bias=None, order="token"):
     """Drive moe_route (logits given) + moe_dispatch (no row copy) + moe_aux_stats."""
-    cfg = N.make_config(T, 8, E, K, 8, "bf16", C, renorm, 0.01)
+    cfg = N.make_config(T, 8, E, K, 8, "bf16", C, renorm, 0.01, order)
     dev = "cuda"
     R = max(N.rows_capacity(cfg), 1)
     ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device=dev)
@@ -52,7 +52,11 @@ def _routing_only(T, E, K, C, L32, renorm=False):
     f = torch.empty(E, dtype=torch.float32, device=dev)
     P = torch.empty(E, dtype=torch.float32, device=dev)
     l = torch.empty(1, dtype=torch.float32, device=dev)
-    N.route(cfg, None, None, None, logits, ids, w, ws)
+    if sel_bias is None:
+        N.route(cfg, None, None, None, logits, ids, w, ws)
+    else:
+        N.route_select_bias(cfg, None, None, None, torch.from_numpy(sel_bias).to(dev), logits,
+                            ids, w, ws)
     N.dispatch(cfg, None, ids, counts, offsets, slot, src, None, ws)
     N.aux_stats(cfg, counts, ws, f, P, l)
     assert N.sync_status(ws) == 0
@@ -60,11 +64,11 @@ def _routing_only(T, E, K, C, L32, renorm=False):
                 slot=to_np(slot), src=to_np(src), f=to_np(f), P=to_np(P), l_aux=float(l.item()))
 
 
-def _check_routing(g, L32, K, C, E, renorm=False, alpha=0.01):
-    ids = O.top_k(L32, K)
+def _check_routing(g, L32, K, C, E, renorm=False, alpha=0.01, sel_bias=None, order="token"):
+    ids = O.top_k(L32, K, sel_bias)
     p = O.softmax(L32)
     w = O.routing_weights(p, ids, renorm)
-    plan = O.dispatch_plan(ids, E, C)
+    plan = O.dispatch_plan(ids, E, C, order)
     assert np.array_equal(g["ids"], ids)
     assert np.max(np.abs(g["w"] - w) / np.abs(w)) <= 1e-6
     assert np.array_equal(g["counts"], plan["counts"])
@@ -114,6 +118,43 @@ def test_routing_bit_exact_workload_logits(name):
     if name == "long":
         share = float(plan["counts"].max()) / (wl.T * wl.K)
         assert 0.37 <= share <= 0.43, share
+
+
+@pytest.mark.parametrize("T,E,K,cf,ties,bias,order,cap", [
+    (4096, 8, 2, 1.25, True, True, "token", "tokens"),
+    (4096, 8, 2, 1.25, False, False, "slot", "tokens"),
+    (16384, 128, 8, 1.5, True, True, "slot", "assignments"),
+    (8192, 256, 8, None, False, True, "token", "tokens"),
+    (5000, 64, 4, 0.9, True, True, "slot", "tokens"),
+    (65536, 8, 2, 1.0, False, False, "slot", "assignments"),
+    (37, 5, 5, 0.5, True, True, "slot", "tokens"),
+])
+def test_routing_variants_bit_exact(T, E, K, cf, ties, bias, order, cap):
+    """Selection-only bias, slot-major drop priority and capacity counting assignments:
+    ids, counts, offsets, slot, src bit for bit; weights and P from the unbiased
+    softmax."""
+    L32 = make_logits(T, E, seed=T + 7 * E, ties=ties).numpy()
+    rng = np.random.default_rng(T + E)
+    b = (np.round(rng.standard_normal(E) * 4) / 8).astype(np.float32) if bias else None
+    C = O.capacity(T, E, cf) if cap == "tokens" else O.capacity_assignments(T, E, K, cf)
+    g = _routing_only(T, E, K, C, L32, sel_bias=b, order=order)
+    _check_routing(g, L32, K, C, E, sel_bias=b, order=order)
+
+
+def test_adjust_selection_bias_matches_oracle():
+    T, E, K = 3000, 64, 4
+    L32 = make_logits(T, E, seed=21).numpy()
+    g = _routing_only(T, E, K, -1, L32)
+    b = np.random.default_rng(3).standard_normal(E).astype(np.float32)
+    cfg = N.make_config(T, 8, E, K, 8, "bf16", -1)
+    counts = torch.from_numpy(g["counts"]).cuda()
+    bias = torch.from_numpy(b).cuda()
+    N.adjust_select_bias(cfg, counts, bias, 1e-3)
+    torch.cuda.synchronize()
+    want = O.adjust_selection_bias(b, g["counts"], T, K, 1e-3)
+    assert np.array_equal(bias.cpu().numpy(), want)
+    with pytest.raises(N.MoeError):
+        N.adjust_select_bias(cfg, counts, bias, -1.0)
 
 
 def test_scan_spans_many_blocks_all_one_expert():
@@ -235,6 +276,40 @@ def test_layer_stages_with_oracle_logits(wl):
     assert abs(layer.l_aux.item() - ref["l_aux"]) <= 1e-5 * ref["l_aux"]
 
 
+@pytest.mark.parametrize("idx,order,cap", [(2, "slot", "assignments"), (3, "slot", "tokens"),
+                                         (4, "token", "assignments")])
+def test_layer_routing_variants_end_to_end(idx, order, cap):
+    """Whole layer with a selection-only bias, slot-major drop priority and/or capacity
+    counting assignments, fed the oracle's logits: routing bit for bit, output within
+    tolerance; then one bias adjustment step matches the oracle's."""
+    wl = SMALL[idx]
+    inp = make_inputs(wl, "cuda")
+    rng = np.random.default_rng(idx)
+    b = (rng.standard_normal(wl.E) * 0.3).astype(np.float32)
+    sel = torch.from_numpy(b).cuda()
+    layer = MoELayer.from_workload(wl, inp, drop_order=order, capacity_mode=cap, sel_bias=sel)
+    x_np = to_np(inp["x"])
+    b_np = None if inp["b_r"] is None else to_np(inp["b_r"])
+    _, L32 = O.router_logits(x_np, to_np(inp["w_r"]), b_np)
+    layer.forward(inp["x"], logits_in=torch.from_numpy(L32).cuda())
+    layer.check_device_status()
+    C = (O.capacity(wl.T, wl.E, wl.capacity_factor) if cap == "tokens"
+         else O.capacity_assignments(wl.T, wl.E, wl.K, wl.capacity_factor))
+    assert layer.cfg.capacity == C
+    shared = (to_np(inp["w1s"])[0], to_np(inp["w2s"])[0]) if wl.shared else None
+    ref = O.moe_forward(x_np, to_np(inp["w_r"]), b_np, to_np(inp["w1"]), to_np(inp["w2"]),
+                        wl.K, C, wl.alpha, shared=shared, logits32=L32, sel_bias=b, order=order)
+    assert np.array_equal(to_np(layer.ids), ref["ids"])
+    assert np.array_equal(to_np(layer.slot), ref["slot"].reshape(wl.T, wl.K))
+    assert np.array_equal(to_np(layer.src)[:ref["R"]], ref["src"])
+    err, literal = layer_output_error(to_np(layer.y), ref["y"], wl.dtype)
+    assert err <= TOL[wl.dtype], (err, literal)
+    layer.adjust_selection_bias(0.01)
+    torch.cuda.synchronize()
+    assert np.array_equal(sel.cpu().numpy(),
+                          O.adjust_selection_bias(b, ref["counts"], wl.T, wl.K, 0.01))
+
+
 def test_capacity_zero_drops_everything():
     wl = Workload("cap0", 64, 64, 8, 2, 64, "bf16", 0.1)  # C = floor(64*0.1/8) = 0
     layer, ref, L32, C = _layer_case(wl)
@@ -266,10 +341,10 @@ def test_determinism_two_runs():
 
 
 # ------------------------------------------------------------------ full-size workloads
-def _sampled_full_check(name, n_tokens=48, seed=0):
+def _sampled_full_check(name, n_tokens=48, seed=0, max_rows=512):
     """Full-size workload in the bench's launch configuration: routing in full against
-    the oracle's own logits (near ties excluded), the expert FFN on every row of two
-    experts and the layer output on a token sample."""
+    the oracle's own logits (near ties excluded), the expert FFN on the first
+    ``max_rows`` packed rows of two experts and the layer output on a token sample."""
     wl = WORKLOADS[name]
     inp = make_inputs(wl, "cuda")
     layer = MoELayer.from_workload(wl, inp)
@@ -297,9 +372,10 @@ def _sampled_full_check(name, n_tokens=48, seed=0):
         lo, hi = int(offs[e]), int(offs[e + 1])
         if hi == lo or not np.array_equal(g_offs[e:e + 2], offs[e:e + 2]):
             continue
+        hi = min(hi, lo + max_rows)
         rows = plan["src"][lo:hi] // wl.K
         y_ref, h_ref = O.expert_ffn(x_np[rows], to_np(inp["w1"][e]), to_np(inp["w2"][e]))
-        glo, ghi = int(g_offs[e]), int(g_offs[e + 1])
+        glo, ghi = int(g_offs[e]), int(g_offs[e]) + (hi - lo)
         assert np.array_equal(to_np(layer.src)[glo:ghi] // wl.K, rows)
         assert_rounded_to(to_np(layer.h[glo:ghi]), h_ref, "f16" if wl.dtype == "bf16" else "f32")
         assert rel_rms_err(to_np(layer.y_perm[glo:ghi]), y_ref) <= tol
@@ -326,7 +402,7 @@ def _sampled_full_check(name, n_tokens=48, seed=0):
     assert err <= tol, (err, literal)
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3"])
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3", "long"])
 def test_full_size_sampled(name):
     _sampled_full_check(name)
 

@@ -334,3 +334,131 @@ def test_all_subsets_topk_small():
 def test_aux_empty_batch_is_zero():
     f, P, L = O.aux_stats(np.zeros((0, 2), np.int32), np.zeros((0, 4)), 4, 0.01)
     assert f.tolist() == [0.0] * 4 and P.tolist() == [0.0] * 4 and L == 0.0
+
+
+# ---------------------------------------------------------------- routing variants
+# "Expert Parallelism (EP)", "Load balancing" names DeepSeek-V3's auxiliary-loss-free
+# bias-adjustment scheme and capacity-factor dropping without fixing their details; the
+# variants below are readings.  These tests pin the oracle to those readings by routes
+# other than its own code: reductions to the default path, brute force, hand cases.
+def test_selection_bias_zero_is_plain_topk():
+    rng = np.random.default_rng(11)
+    L = rng.standard_normal((50, 9)).astype(np.float32)
+    assert np.array_equal(O.top_k(L, 3, np.zeros(9, np.float32)), O.top_k(L, 3))
+
+
+def test_selection_bias_moves_choice_not_weights():
+    """A large bias on expert 4 makes it every token's first choice, while the routing
+    weights and P_i remain those of the unbiased softmax."""
+    rng = np.random.default_rng(12)
+    T, E, K = 40, 6, 2
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    b = np.zeros(E, np.float32)
+    b[4] = 100.0
+    ids = O.top_k(L, K, b)
+    assert (ids[:, 0] == 4).all()
+    p = O.softmax(L)
+    w = O.routing_weights(p, ids)
+    # weight of the forced expert = its unbiased probability, computed here directly
+    z = L.astype(np.float64)
+    direct = np.exp(z[:, 4] - z.max(axis=1)) / np.exp(z - z.max(axis=1, keepdims=True)).sum(axis=1)
+    assert np.allclose(w[:, 0], direct, rtol=1e-13, atol=0)
+    # second choice: the best of the others by the unbiased logits
+    others = np.where(np.arange(E) == 4, -np.inf, z)
+    assert np.array_equal(ids[:, 1], np.argmax(others, axis=1))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_selection_bias_bruteforce(seed):
+    """Top-K by the fp32 score s = fl(L + b) with (s desc, id asc), checked by Python's
+    sort of explicit (key, id) pairs on a coarse grid that makes ties frequent."""
+    rng = np.random.default_rng(seed)
+    T, E, K = 30, 7, 3
+    L = (np.round(rng.standard_normal((T, E)) * 2) / 2).astype(np.float32)
+    b = (np.round(rng.standard_normal(E) * 2) / 4).astype(np.float32)
+    ids = O.top_k(L, K, b)
+    for t in range(T):
+        keys = [(-(float(np.float32(L[t, e]) + np.float32(b[e]))), e) for e in range(E)]
+        want = [e for _, e in sorted(keys)[:K]]
+        assert ids[t].tolist() == want
+
+
+def test_adjust_selection_bias_hand_case():
+    """counts [5, 3, 0, 8] with T*K = 16 over E = 4 (mean 4): expert 0 and 3 are over the
+    mean (lowered), 1 and 2 under it (raised)."""
+    b = np.array([0.5, -0.25, 0.0, 1.0], np.float32)
+    nb = O.adjust_selection_bias(b, [5, 3, 0, 8], T=8, K=2, gamma=0.125)
+    assert nb.tolist() == [0.375, -0.125, 0.125, 0.875]
+    assert nb.dtype == np.float32
+
+
+def test_adjust_selection_bias_at_mean_and_rounding():
+    """An expert exactly at the mean keeps its bias; the update is one fp32 addition, so
+    a step below half an ulp of the bias leaves it unchanged."""
+    b = np.array([1.0, 1.0, 1.0], np.float32)
+    assert O.adjust_selection_bias(b, [2, 2, 2], T=3, K=2, gamma=0.5).tolist() == [1.0, 1.0, 1.0]
+    tiny = O.adjust_selection_bias(b, [3, 2, 1], T=3, K=2, gamma=2.0 ** -30)
+    assert tiny.tolist() == [1.0, 1.0, 1.0]
+
+
+def test_slot_major_hand_case():
+    """T=3, K=2, E=2, C=2, choices [[0,1],[1,0],[0,1]].  Token-major arrival drops token
+    2's first choice (expert 0 already holds tokens 0 and 1); slot-major arrival takes
+    every first choice before any second choice, so token 2's first choice is kept and
+    token 1's second choice is dropped instead."""
+    ids = np.array([[0, 1], [1, 0], [0, 1]], np.int32)
+    tok = O.dispatch_plan(ids, 2, 2, "token")
+    slt = O.dispatch_plan(ids, 2, 2, "slot")
+    assert tok["slot"].reshape(3, 2).tolist() == [[0, 2], [3, 1], [-1, -1]]
+    # slot-major: expert 0 packs (t0,k0), (t2,k0); expert 1 packs (t1,k0), (t0,k1)
+    assert slt["slot"].reshape(3, 2).tolist() == [[0, 3], [2, -1], [1, -1]]
+    assert slt["src"].tolist() == [0, 4, 2, 1]
+    assert slt["counts"].tolist() == tok["counts"].tolist() == [3, 3]
+
+
+def test_slot_major_with_one_choice_is_token_major():
+    rng = np.random.default_rng(5)
+    ids = rng.integers(0, 6, size=(70, 1)).astype(np.int32)
+    a, b = O.dispatch_plan(ids, 6, 9, "token"), O.dispatch_plan(ids, 6, 9, "slot")
+    for key in ("counts", "offsets", "slot", "src"):
+        assert np.array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("seed,T,E,K,C", [(0, 64, 8, 2, 10), (1, 33, 16, 4, 5), (2, 40, 5, 3, 0),
+                                          (3, 25, 4, 4, 100)])
+def test_slot_major_bruteforce(seed, T, E, K, C):
+    """Arrival numbers by one-hot cumulative sums over the transposed stream."""
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    plan = O.dispatch_plan(ids, E, C, "slot")
+    stream = ids.T.reshape(-1)                      # k-major: (k=0, all t), (k=1, all t)...
+    keep_s, pos_s = _bruteforce_keep(stream, E, C)
+    keep = keep_s.reshape(K, T).T.reshape(-1)
+    pos = pos_s.reshape(K, T).T.reshape(-1)
+    assert np.array_equal(plan["keep"], keep)
+    assert np.array_equal(plan["pos"], pos)
+    # inside each expert's block, rows follow the transposed stream
+    for e in range(E):
+        lo, hi = plan["offsets"][e], plan["offsets"][e + 1]
+        a = plan["src"][lo:hi].astype(np.int64)
+        order_key = (a % K) * T + a // K
+        assert (np.diff(order_key) > 0).all()
+
+
+@pytest.mark.parametrize("T,E,K,cf,C", [(256, 8, 2, 1.25, 80), (4096, 8, 2, 1.25, 1280),
+                                        (16384, 128, 8, 1.5, 1536), (65536, 8, 2, 1.0, 16384),
+                                        (8192, 256, 8, None, -1), (10, 3, 2, 1.0, 6)])
+def test_capacity_counting_assignments(T, E, K, cf, C):
+    assert O.capacity_assignments(T, E, K, cf) == C
+
+
+def test_capacity_counting_assignments_balanced_load_never_drops():
+    """"Capacity is rarely hit" when the load is even: with the capacity counting
+    assignments and capacity_factor 1, an exactly balanced routing drops nothing."""
+    T, E, K = 48, 6, 2
+    ids = (np.arange(T * K) % E).reshape(T, K).astype(np.int32)  # each expert 16 times
+    C = O.capacity_assignments(T, E, K, 1.0)
+    plan = O.dispatch_plan(ids, E, C)
+    assert C == 16 and plan["R"] == T * K and (plan["slot"] >= 0).all()
+    # the capacity as printed (tokens) drops K-1 of every K assignments here
+    assert O.dispatch_plan(ids, E, O.capacity(T, E, 1.0))["R"] == E * (T // E)
