@@ -220,7 +220,8 @@ def run_ours(args, wl):
     N.set_gemm_pairing({"auto": N.GEMM_AUTO, "single": N.GEMM_SINGLE, "pair": N.GEMM_PAIR,
                         "split": N.GEMM_SPLIT}[args.gemm])
     inp = make_inputs(wl, dev, seed=0)
-    layer = MoELayer.from_workload(wl, inp, device=dev)
+    layer = MoELayer.from_workload(wl, inp, device=dev, fused_dispatch=args.dispatch == "fused",
+                                   experts=args.experts)
     x = inp["x"]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -271,7 +272,12 @@ def run_ours(args, wl):
     A = wl.T * wl.K
     flops_up = 2.0 * R * wl.d * wl.F
     flops_down = 2.0 * R * wl.F * wl.d
-    bytes_dispatch = t_active * wl.d * b + R * wl.d * b + A * 12 + R * 4
+    # dispatch: the routing plan (ids read, positions, slot and src written) and, when
+    # not fused into the first expert GEMM, each token row read once and written to its
+    # kept packed rows
+    bytes_dispatch = A * 12 + R * 4
+    if args.dispatch == "copy":
+        bytes_dispatch += t_active * wl.d * b + R * wl.d * b
     bytes_combine = R * wl.d * 4 + wl.T * wl.d * b + A * 8 + (wl.T * wl.d * 4 if layer.shared else 0)
     bytes_route = wl.T * wl.d * b + wl.E * wl.d * b + wl.T * wl.E * 4 * 2 + A * 8
     med = {n: statistics.median(v) for n, v in stage_ms.items()}
@@ -284,10 +290,15 @@ def run_ours(args, wl):
     if not os.path.exists(os.path.join(ROOT, kernel_src)):
         kernel_src = "routing_dispatch_expert_04_b300/csrc/gemm_simt.cu"
     traffic = recorded_traffic(f"{dom}:{wl.name}", source_digest(kernel_src))
+    if args.experts == "e4m3":
+        # FP8 contraction: the measured bf16 peak times the nominal fp8/bf16 ratio (2)
+        peak_tf, peak_src = 2.0 * pk["bf16_tflops"], f"{pk['source']} bf16 dense (burst) x 2 (nominal e4m3/bf16)"
+    else:
+        peak_tf, peak_src = pk["bf16_tflops"], f"{pk['source']} bf16 dense (burst)"
     roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved_tf, 2),
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved_tf / pk["bf16_tflops"], 4), "traffic": traffic,
-                "peak_source": f"{pk['source']} bf16 dense (burst)",
+                "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(achieved_tf / peak_tf, 4), "traffic": traffic,
+                "peak_source": peak_src,
                 "algorithmic_flops_per_launch": dom_flops}
     hbm = pk["hbm_gbs"]
 
@@ -300,7 +311,7 @@ def run_ours(args, wl):
         "expert_down_tflops": round(flops_down / (avg["expert_down"] * 1e-3) / 1e12, 2),
         "grouped_gemm_frac_of_bf16_peak": round(
             (flops_up + flops_down) / ((avg["expert_up"] + avg["expert_down"]) * 1e-3) / 1e12
-            / pk["bf16_tflops"], 4),
+            / peak_tf, 4),
         "dispatch_gbs": round(gbs(bytes_dispatch, avg["dispatch"]), 1),
         "dispatch_frac_of_hbm": round(gbs(bytes_dispatch, avg["dispatch"]) / hbm, 4),
         "combine_gbs": round(gbs(bytes_combine, avg["combine"]), 1),
@@ -354,11 +365,13 @@ def run_ours(args, wl):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_s * 1e3 / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype if args.experts == "bf16" else f"{wl.dtype} layer, e4m3 expert GEMMs",
+        "data": "synthetic",
         "config": {"workload": f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} K={wl.K} F={wl.F} "
                                f"{wl.dtype} capacity_factor={wl.capacity_factor}",
                    "capacity": layer.cfg.capacity, "parallelism": f"replicas x{world}",
-                   "expert_gemm": args.gemm,
+                   "expert_gemm": args.gemm, "dispatch": args.dispatch, "experts": args.experts,
                    "l2": "flushed before each step (512 MiB device write, outside the events)"},
         "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches, "gpu_launches_per_step": kernels_per_step,
@@ -416,6 +429,13 @@ def main():
                     help="expert GEMM kernels: one CTA per 128-row tile, CTA pairs per "
                          "256-row tile, pairs for whole 256-row tiles + one CTA for the "
                          "rest, or the library's choice")
+    ap.add_argument("--dispatch", choices=["fused", "copy"], default="copy",
+                    help="fused: the first expert GEMM gathers its rows from x while loading "
+                         "them; copy: the dispatch step copies them into a packed buffer")
+    ap.add_argument("--experts", choices=["bf16", "e4m3"], default="bf16",
+                    help="expert Linears in bf16 (the layer's precision) or the FP8 variant "
+                         "(per-row E4M3 operands); an e4m3 line is a different precision "
+                         "and says so in its dtype")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--cpu-rows", type=int, default=512)

@@ -59,7 +59,7 @@ typedef enum {
   MOE_ERR_DEVICE = 5        /* (device) bad expert id, packed-row or fp16 overflow */
 } moe_status_t;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_F16 = 2 /* moe_quantize_e4m3 input only */ } moe_dtype_t;
 
 typedef struct {
   int32_t T;            /* tokens */
@@ -175,6 +175,20 @@ moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int3
                            int32_t n_groups, int64_t rows_cap, const void* w1, void* h,
                            void* ws, void* stream);
 
+/* Step 3a with the dispatch fused into the expert GEMM's operand load: the packed rows
+ * are gathered from the token matrix while each tile is loaded (TMA row gathers), so
+ * no x_perm is written or read.  Same result as moe_dispatch's row copy followed by
+ * moe_expert_up:
+ *   h[r] = GELU(x[src[r] / K] . W1[g]^T)   for r in [offsets[g], offsets[g+1])
+ *   x    [T, d] dtype (the layer's input rows; cfg.T rows)
+ *   src  [rows_cap] int32 device pointer (4-byte aligned): packed row -> flat assignment
+ *        t*K + k, as written by moe_dispatch (which can then run with x = x_perm = NULL)
+ *   the other arguments as moe_expert_up.  A src entry naming a token outside [0, T) is
+ *   reported as MOE_ERR_DEVICE and gathers row 0 instead. */
+moe_status_t moe_expert_up_gather(const moe_config* cfg, const void* x, const int32_t* src,
+                                  const int32_t* offsets, int32_t n_groups, int64_t rows_cap,
+                                  const void* w1, void* h, void* ws, void* stream);
+
 /* Step 3b -- grouped second expert Linear: y_perm = h . W2[g]^T.
  *   h [rows_cap, F] as written by moe_expert_up (fp32, or fp16 for MOE_BF16 layers);
  *   w2 [n_groups, d, F]: fp32 for MOE_F32 layers; FP16 for MOE_BF16 layers (convert the
@@ -184,6 +198,43 @@ moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int3
 moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t* offsets,
                              int32_t n_groups, int64_t rows_cap, const void* w2, void* y_perm,
                              void* ws, void* stream);
+
+/* FP8 variant of step 3 for MOE_BF16 layers.  The pages fix no FP8 recipe (they only
+ * note that MoE is the most FP8-sensitive architecture); this is the plainest one:
+ * E4M3 operands (round to nearest even, saturating at +-448) with one fp32 scale per
+ * row of each operand -- per token row of x, per row of h, per output channel of each
+ * weight -- and fp32 accumulation on the tensor cores (tcgen05 kind::f8f6f4).  Results
+ * differ from the bf16 path by the E4M3 rounding of every operand (about 2^-4 relative
+ * per element); the outputs keep the bf16 path's types.
+ *
+ * moe_quantize_e4m3: codes[r, c] = E4M3(src[r, c] * (448 / amax_r)) and
+ *   scales[r] = amax_r / 448 (amax_r = max_c |src[r, c]|; a zero row gives zero codes and
+ *   scale 0), each step one correctly rounded fp32 operation.
+ *   src [rows, cols] of dtype MOE_F32, MOE_BF16 or MOE_F16 (16-byte aligned), cols a
+ *   multiple of 16; codes [rows, cols] bytes (16-byte aligned); scales [rows] fp32.
+ *   rows_dev: nullable device int32; when given, only the first min(rows, *rows_dev)
+ *   rows are converted (e.g. offsets + E: the packed rows actually kept).
+ *   Use it once for the stacked weights (W1 as [E*F, d] rows, W2 as [E*d, F]), and per
+ *   step for x ([T, d]) and for h ([rows_cap, F], fp16).
+ *
+ * moe_expert_up_e4m3: h[r] = GELU(x_scale[a] * w1_scale[g*F + n] * sum_k xq[a,k] w1q[g*F+n,k])
+ *   with a = src[r] / K (rows gathered from the quantised token matrix xq [T, d], as in
+ *   moe_expert_up_gather) or a = r when src is NULL (xq then holds the packed rows);
+ *   h [rows_cap, F] fp16 out.
+ * moe_expert_down_e4m3: y_perm[r] = h_scale[r] * w2_scale[g*d + n] * sum_k hq[r,k] w2q[g*d+n,k];
+ *   y_perm [rows_cap, d] fp32 out.
+ * Other arguments as moe_expert_up / moe_expert_down.  d and F must be multiples of 16
+ * (else MOE_ERR_UNSUPPORTED); MOE_F32 layers return MOE_ERR_UNSUPPORTED. */
+moe_status_t moe_quantize_e4m3(const void* src, int32_t dtype, int64_t rows, int32_t cols,
+                               const int32_t* rows_dev, void* codes, float* scales, void* stream);
+moe_status_t moe_expert_up_e4m3(const moe_config* cfg, const void* xq, const float* x_scale,
+                                const int32_t* src, const int32_t* offsets, int32_t n_groups,
+                                int64_t rows_cap, const void* w1q, const float* w1_scale, void* h,
+                                void* ws, void* stream);
+moe_status_t moe_expert_down_e4m3(const moe_config* cfg, const void* hq, const float* h_scale,
+                                  const int32_t* offsets, int32_t n_groups, int64_t rows_cap,
+                                  const void* w2q, const float* w2_scale, void* y_perm, void* ws,
+                                  void* stream);
 
 /* Step 3 -- both expert Linears (moe_expert_up then moe_expert_down). */
 moe_status_t moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
@@ -207,6 +258,17 @@ moe_status_t moe_combine(const moe_config* cfg, const void* y_perm, const int32_
  * call that used the same ws. */
 moe_status_t moe_aux_stats(const moe_config* cfg, const int32_t* counts, const void* ws,
                            float* f, float* P, float* l_aux, void* stream);
+
+/* Backward of the auxiliary loss (the pages: it "is added to the main task loss and
+ * backpropagated"; it does not affect inference).  Writes the gradient of
+ * L_aux = alpha * sum_i f_i P_i with respect to the router logits:
+ *   grad_logits[t,j] = (alpha / T) * p[t,j] * (f_j - sum_i f_i p[t,i]),
+ * p = softmax(logits[t]) recomputed in fp32.  f_i is a count of top-K choices, a step
+ * function of the logits whose derivative is zero away from ties, so only P_i carries
+ * gradient.  logits [T, E] fp32 (as moe_route wrote them), f [E] fp32 (from
+ * moe_aux_stats), grad_logits [T, E] fp32 out; all 4-byte aligned device pointers. */
+moe_status_t moe_aux_loss_grad(const moe_config* cfg, const float* logits, const float* f,
+                               float* grad_logits, void* stream);
 
 /* Convert n bf16 values to fp16 (n a multiple of 8), e.g. the second expert Linear's
  * weights of a MOE_BF16 layer.  Magnitudes in [2^-17, 65504] convert exactly, smaller

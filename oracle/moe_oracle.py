@@ -290,6 +290,77 @@ def aux_stats(ids, p, E: int, alpha: float):
     return f, P, float(alpha) * float(np.sum(f * P))
 
 
+def aux_loss_grad_logits(L32, ids, alpha: float) -> np.ndarray:
+    """Gradient of L_aux = alpha * sum_i f_i P_i with respect to the router logits, in fp64
+    ([EPM] "Load Balancing": the auxiliary loss "is added to the main task loss and
+    backpropagated").
+
+    f_i counts top-K choices, a step function of the logits: its derivative is zero
+    wherever no tie is crossed, so only P_i = (1/T) sum_t softmax(L)[t,i] carries
+    gradient.  With p = softmax(L[t]) and the softmax Jacobian p_i (delta_ij - p_j):
+        dL_aux/dL[t,j] = (alpha / T) * p[t,j] * (f_j - sum_i f_i p[t,i]).
+    """
+    p = softmax(L32)
+    T, E = p.shape
+    if T == 0:
+        return np.zeros((0, E))
+    f, _, _ = aux_stats(ids, p, E, alpha)
+    mean_f = p @ f
+    return (float(alpha) / T) * p * (f[None, :] - mean_f[:, None])
+
+
+# --------------------------------------------------------------------------------------
+# FP8 expert GEMMs (variant; "Expert Parallelism (EP)", "See also": MoE is the most
+# FP8-sensitive architecture).  The pages fix no FP8 recipe; the reading taken here is the
+# plainest one: E4M3 values (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+# infinities, largest finite 448, smallest subnormal 2^-9), round to nearest even,
+# saturating; one fp32 scale per row of each operand (per token row of the activations,
+# per output channel of the weights), amax / 448.
+# --------------------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def round_e4m3(v) -> np.ndarray:
+    """Nearest E4M3 value (ties to even), saturating at +-448; returned as float64."""
+    v = np.clip(np.asarray(v, dtype=np.float64), -E4M3_MAX, E4M3_MAX)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)                   # below 2^-6 the spacing is that of subnormals
+    quantum = np.exp2(e - 3)                # 3 mantissa bits
+    q = np.round(v / quantum) * quantum     # np.round rounds halves to even
+    return np.clip(q, -E4M3_MAX, E4M3_MAX)
+
+
+def quantize_rows_e4m3(m):
+    """Per-row E4M3 quantisation of an fp32 matrix, in fp32 arithmetic as stated:
+    amax = max |row|, inv = 448 / amax, code = e4m3(row * inv), scale = amax / 448
+    (a zero row gets inv = scale = 0 and codes 0).  Returns (codes as float64, scale fp32)."""
+    m = np.asarray(m, dtype=np.float32)
+    amax = np.max(np.abs(m), axis=1) if m.shape[1] else np.zeros(m.shape[0], np.float32)
+    nz = amax > 0
+    inv = np.zeros_like(amax)
+    inv[nz] = (np.float32(E4M3_MAX) / amax[nz]).astype(np.float32)
+    scaled = (m * inv[:, None]).astype(np.float32)
+    scale = np.zeros_like(amax)
+    scale[nz] = (amax[nz] / np.float32(E4M3_MAX)).astype(np.float32)
+    return round_e4m3(scaled), scale
+
+
+def expert_ffn_e4m3(x_rows, w1, w2):
+    """One expert on E4M3 operands (variant): x rows and the weight rows quantised per
+    row (quantize_rows_e4m3), h = GELU(dequantised product) in fp64 and stored in fp16
+    (as the intermediate activation of bf16 layers is), h quantised per row in turn,
+    y = dequantised product with W2.  Returns (y [n,d], h [n,F] before the fp16 store)."""
+    xq, sx = quantize_rows_e4m3(x_rows)
+    w1q, s1 = quantize_rows_e4m3(w1)
+    h = gelu((xq @ w1q.T) * widen(sx)[:, None] * widen(s1)[None, :])
+    hq, sh = quantize_rows_e4m3(h.astype(np.float16).astype(np.float32))
+    w2q, s2 = quantize_rows_e4m3(w2)
+    y = (hq @ w2q.T) * widen(sh)[:, None] * widen(s2)[None, :]
+    return y, h
+
+
 # --------------------------------------------------------------------------------------
 # Selection-bias adjustment: [EPH] "Load balancing" (DeepSeek-V3's auxiliary-loss-free
 # bias-adjustment scheme; the update rule is a reading, see the module docstring).
@@ -312,14 +383,17 @@ def adjust_selection_bias(sel_bias, counts, T: int, K: int, gamma: float) -> np.
 # --------------------------------------------------------------------------------------
 def moe_forward(x, w_r, b_r, w1, w2, K: int, C: int, alpha: float,
                 renormalize: bool = False, shared=None, logits32=None, sel_bias=None,
-                order: str = "token"):
+                order: str = "token", experts: str = "exact"):
     """Forward pass of one MoE FFN layer, every intermediate returned.
 
     x [T,d]; w_r [E,d]; b_r [E] or None; w1 [E,F,d]; w2 [E,d,F];
     shared = (w1s [F,d], w2s [d,F]) or None; logits32 [T,E] float32 replaces the router
     when given (the routing stages are then driven by those exact fp32 values);
-    sel_bias [E] fp32: selection-only bias; order: arrival order for dropping.
+    sel_bias [E] fp32: selection-only bias; order: arrival order for dropping;
+    experts: "exact" (fp64 on the stored values) or "e4m3" (expert_ffn_e4m3, the FP8
+    variant; the router and the combine stay exact).
     """
+    ffn = expert_ffn if experts == "exact" else expert_ffn_e4m3
     x = np.asarray(x)
     T = x.shape[0]
     E = w1.shape[0]
@@ -342,10 +416,10 @@ def moe_forward(x, w_r, b_r, w1, w2, K: int, C: int, alpha: float,
     for e in range(E):
         lo, hi = int(offs[e]), int(offs[e + 1])
         if hi > lo:
-            y_perm[lo:hi], h[lo:hi] = expert_ffn(x_perm[lo:hi], w1[e], w2[e])
+            y_perm[lo:hi], h[lo:hi] = ffn(x_perm[lo:hi], w1[e], w2[e])
     y_shared = None
     if shared is not None:
-        y_shared = dense_ffn(x, shared[0], shared[1])
+        y_shared = ffn(widen(x), shared[0], shared[1])[0]
     y = combine(y_perm, plan["slot"], w, T, y_shared)
     f, P, l_aux = aux_stats(ids, p, E, alpha)
     out = dict(plan)

@@ -27,17 +27,33 @@ cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const
 cudaError_t launch_aux(const int32_t* counts, const float* ppart, int nblk, int E, int Tn, int K,
                        float alpha, float* f, float* P, float* l_aux, double* auxfp, uint32_t* hdr,
                        cudaStream_t st);
-cudaError_t launch_simt_grouped(int dtype, const void* A, const void* B, void* C,
+cudaError_t launch_aux_grad(const float* logits, const float* f, int Tn, int E, float alpha,
+                            float* grad, int num_sms, cudaStream_t st);
+cudaError_t launch_simt_grouped(int dtype, const void* A, const int32_t* gather_src, int gather_k,
+                                int64_t gather_rows, const void* B, void* C,
                                 const int32_t* offsets, int G, int N, int Kd, int64_t rows_cap,
                                 bool gelu, uint32_t* hdr, cudaStream_t st);
 cudaError_t launch_simt_router(int dtype, const void* x, const void* w_r, const float* b_r,
                                float* logits, int T, int E, int d, uint32_t* hdr, cudaStream_t st);
-cudaError_t launch_tc_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets, int G,
-                         int N, int Kd, int64_t rows_cap, int64_t cap_per_group, int pair_mode,
-                         uint32_t* hdr, int num_sms, cudaStream_t st);
+cudaError_t launch_tc_up(const void* a_in, const int32_t* gather_src, int gather_k,
+                         int64_t gather_rows, const void* w1, void* h, const int32_t* offsets,
+                         int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
+                         int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
                            int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
                            int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st);
+cudaError_t launch_tc_up_e4m3(const void* xq, const float* sx, const int32_t* gather_src,
+                              int gather_k, int64_t gather_rows, const void* w1q, const float* sw1,
+                              void* h, const int32_t* offsets, int G, int N, int Kd,
+                              int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr, int num_sms,
+                              cudaStream_t st);
+cudaError_t launch_tc_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
+                                void* y_perm, const int32_t* offsets, int G, int N, int Kd,
+                                int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr,
+                                int num_sms, cudaStream_t st);
+cudaError_t launch_quantize_e4m3(int dtype, const void* src, int64_t rows, int cols,
+                                 const int32_t* rows_dev, void* codes, float* scales, int num_sms,
+                                 cudaStream_t st);
 cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, float* out, int T,
                              int E, int d, int nsplit, uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_bf16_to_f16(const void* src, void* dst, int64_t n, uint32_t* hdr, int num_sms,
@@ -228,19 +244,91 @@ static moe_status_t check_ffn_args(const moe_config* cfg, const void* in, const 
   return MOE_OK;
 }
 
+static moe_status_t expert_up_impl(const moe_config& c, const void* a_in, const int32_t* gather_src,
+                                   const int32_t* offsets, int32_t n_groups, int64_t rows_cap,
+                                   const void* w1, void* h, void* ws, void* stream) {
+  const int64_t gather_rows = gather_src != nullptr ? c.T : 0;
+  if (c.dtype == MOE_BF16)
+    return cuda_status(launch_tc_up(a_in, gather_src, c.K, gather_rows, w1, h, offsets, n_groups,
+                                    c.F, c.d, rows_cap, group_row_bound(c, n_groups, rows_cap),
+                                    g_gemm_pairing.load(), (uint32_t*)ws, num_sms(),
+                                    (cudaStream_t)stream));
+  return cuda_status(launch_simt_grouped(c.dtype, a_in, gather_src, c.K, gather_rows, w1, h, offsets,
+                                         n_groups, c.F, c.d, rows_cap, true, (uint32_t*)ws,
+                                         (cudaStream_t)stream));
+}
+
 moe_status_t moe_expert_up(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                            int32_t n_groups, int64_t rows_cap, const void* w1, void* h, void* ws,
                            void* stream) {
   moe_status_t s = check_ffn_args(cfg, x_perm, offsets, n_groups, rows_cap, w1, h, ws);
   if (s != MOE_OK) return s;
   if (rows_cap == 0) return MOE_OK;
+  return expert_up_impl(*cfg, x_perm, nullptr, offsets, n_groups, rows_cap, w1, h, ws, stream);
+}
+
+moe_status_t moe_expert_up_gather(const moe_config* cfg, const void* x, const int32_t* src,
+                                  const int32_t* offsets, int32_t n_groups, int64_t rows_cap,
+                                  const void* w1, void* h, void* ws, void* stream) {
+  moe_status_t s = check_ffn_args(cfg, x, offsets, n_groups, rows_cap, w1, h, ws);
+  if (s != MOE_OK) return s;
+  if (rows_cap == 0) return MOE_OK;
+  if (src == nullptr || ((uintptr_t)src & 3u)) return MOE_ERR_INVALID;
+  if (cfg->T == 0) return MOE_OK;  // no token rows: every group is empty
+  return expert_up_impl(*cfg, x, src, offsets, n_groups, rows_cap, w1, h, ws, stream);
+}
+
+// E4M3 expert GEMMs: bf16 layers only; the K and N extents must be multiples of 16 (the
+// E4M3 rows are TMA-loaded in 16-byte units).
+static moe_status_t check_e4m3(const moe_config* cfg, const void* scale_a, const void* scale_b) {
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cfg->d % 16 != 0 || cfg->F % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!scale_a || !scale_b || ((uintptr_t)scale_a & 3u) || ((uintptr_t)scale_b & 3u))
+    return MOE_ERR_INVALID;
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_up_e4m3(const moe_config* cfg, const void* xq, const float* x_scale,
+                                const int32_t* src, const int32_t* offsets, int32_t n_groups,
+                                int64_t rows_cap, const void* w1q, const float* w1_scale, void* h,
+                                void* ws, void* stream) {
+  moe_status_t s = check_ffn_args(cfg, xq, offsets, n_groups, rows_cap, w1q, h, ws);
+  if (s != MOE_OK || rows_cap == 0) return s;
+  s = check_e4m3(cfg, x_scale, w1_scale);
+  if (s != MOE_OK) return s;
+  if (src != nullptr && ((uintptr_t)src & 3u)) return MOE_ERR_INVALID;
   const moe_config& c = *cfg;
-  if (c.dtype == MOE_BF16)
-    return cuda_status(launch_tc_up(x_perm, w1, h, offsets, n_groups, c.F, c.d, rows_cap,
-                                    group_row_bound(c, n_groups, rows_cap), g_gemm_pairing.load(),
-                                    (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
-  return cuda_status(launch_simt_grouped(c.dtype, x_perm, w1, h, offsets, n_groups, c.F, c.d,
-                                         rows_cap, true, (uint32_t*)ws, (cudaStream_t)stream));
+  if (src != nullptr && c.T == 0) return MOE_OK;
+  return cuda_status(launch_tc_up_e4m3(xq, x_scale, src, c.K, src != nullptr ? c.T : 0, w1q,
+                                       w1_scale, h, offsets, n_groups, c.F, c.d, rows_cap,
+                                       group_row_bound(c, n_groups, rows_cap), (uint32_t*)ws,
+                                       num_sms(), (cudaStream_t)stream));
+}
+
+moe_status_t moe_expert_down_e4m3(const moe_config* cfg, const void* hq, const float* h_scale,
+                                  const int32_t* offsets, int32_t n_groups, int64_t rows_cap,
+                                  const void* w2q, const float* w2_scale, void* y_perm, void* ws,
+                                  void* stream) {
+  moe_status_t s = check_ffn_args(cfg, hq, offsets, n_groups, rows_cap, w2q, y_perm, ws);
+  if (s != MOE_OK || rows_cap == 0) return s;
+  s = check_e4m3(cfg, h_scale, w2_scale);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  return cuda_status(launch_tc_down_e4m3(hq, h_scale, w2q, w2_scale, y_perm, offsets, n_groups,
+                                         c.d, c.F, rows_cap, group_row_bound(c, n_groups, rows_cap),
+                                         (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
+}
+
+moe_status_t moe_quantize_e4m3(const void* src, int32_t dtype, int64_t rows, int32_t cols,
+                               const int32_t* rows_dev, void* codes, float* scales, void* stream) {
+  if (dtype != MOE_F32 && dtype != MOE_BF16 && dtype != MOE_F16) return MOE_ERR_INVALID;
+  if (rows < 0 || cols <= 0 || cols % 16 != 0) return MOE_ERR_INVALID;
+  if (rows == 0) return MOE_OK;
+  if (!src || !codes || !scales || !aligned16(src) || !aligned16(codes) || ((uintptr_t)scales & 3u))
+    return MOE_ERR_INVALID;
+  if (rows_dev != nullptr && ((uintptr_t)rows_dev & 3u)) return MOE_ERR_INVALID;
+  return cuda_status(launch_quantize_e4m3(dtype, src, rows, cols, rows_dev, codes, scales,
+                                          num_sms(), (cudaStream_t)stream));
 }
 
 moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t* offsets,
@@ -254,8 +342,9 @@ moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t
     return cuda_status(launch_tc_down(h, w2, y_perm, offsets, n_groups, c.d, c.F, rows_cap,
                                       group_row_bound(c, n_groups, rows_cap), g_gemm_pairing.load(),
                                       (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
-  return cuda_status(launch_simt_grouped(c.dtype, h, w2, y_perm, offsets, n_groups, c.d, c.F,
-                                         rows_cap, false, (uint32_t*)ws, (cudaStream_t)stream));
+  return cuda_status(launch_simt_grouped(c.dtype, h, nullptr, 1, 0, w2, y_perm, offsets, n_groups,
+                                         c.d, c.F, rows_cap, false, (uint32_t*)ws,
+                                         (cudaStream_t)stream));
 }
 
 moe_status_t moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
@@ -293,6 +382,19 @@ moe_status_t moe_aux_stats(const moe_config* cfg, const int32_t* counts, const v
   return cuda_status(launch_aux(counts, (const float*)(w + L.ppart), L.nblk_route, c.E, c.T, c.K,
                                 c.alpha, f, P, l_aux, (double*)(w + L.auxfp), (uint32_t*)w,
                                 (cudaStream_t)stream));
+}
+
+moe_status_t moe_aux_loss_grad(const moe_config* cfg, const float* logits, const float* f,
+                               float* grad_logits, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (c.T == 0) return MOE_OK;
+  if (!logits || !f || !grad_logits) return MOE_ERR_INVALID;
+  if (((uintptr_t)logits & 3u) || ((uintptr_t)f & 3u) || ((uintptr_t)grad_logits & 3u))
+    return MOE_ERR_INVALID;
+  return cuda_status(launch_aux_grad(logits, f, c.T, c.E, c.alpha, grad_logits, num_sms(),
+                                     (cudaStream_t)stream));
 }
 
 moe_status_t moe_bf16_to_f16(const void* src, void* dst, int64_t n, void* ws, void* stream) {

@@ -151,6 +151,75 @@ aux_kernel(const int32_t* __restrict__ counts, const float* __restrict__ ppart, 
   }
 }
 
+// Backward of the auxiliary loss ("Load Balancing: The Auxiliary Loss": the loss is
+// added to the task loss and backpropagated).  f_i counts top-K choices and is a step
+// function of the logits (zero derivative away from ties), so only P_i carries gradient:
+//   grad[t,j] = (alpha / T) * p[t,j] * (f_j - sum_i f_i p[t,i]),  p = softmax(logits[t]).
+// One warp per token; the softmax is recomputed in fp32 as in the routing kernel.
+template <int VPT>
+__global__ void __launch_bounds__(256)
+aux_grad_kernel(const float* __restrict__ logits, const float* __restrict__ f, int Tn, int E,
+                float scale, float* __restrict__ grad) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float fv[VPT];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int e = lane + 32 * j;
+    fv[j] = e < E ? f[e] : 0.f;
+  }
+  for (int t = blockIdx.x * 8 + warp; t < Tn; t += gridDim.x * 8) {
+    float v[VPT];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+      m = fmaxf(m, v[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = e < E ? expf(v[j] - m) : 0.f;
+      s += v[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    float mf = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      v[j] = v[j] / s;
+      mf = fmaf(fv[j], v[j], mf);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mf += __shfl_xor_sync(0xffffffffu, mf, o);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) grad[(size_t)t * E + e] = scale * v[j] * (fv[j] - mf);
+    }
+  }
+}
+
+cudaError_t launch_aux_grad(const float* logits, const float* f, int Tn, int E, float alpha,
+                            float* grad, int num_sms, cudaStream_t st) {
+  const int want = (Tn + 7) / 8;
+  const int grid = want < num_sms * 16 ? want : num_sms * 16;
+  const float scale = Tn > 0 ? alpha / (float)Tn : 0.f;
+  if (E <= 32)
+    aux_grad_kernel<1><<<grid, 256, 0, st>>>(logits, f, Tn, E, scale, grad);
+  else if (E <= 64)
+    aux_grad_kernel<2><<<grid, 256, 0, st>>>(logits, f, Tn, E, scale, grad);
+  else if (E <= 128)
+    aux_grad_kernel<4><<<grid, 256, 0, st>>>(logits, f, Tn, E, scale, grad);
+  else
+    aux_grad_kernel<8><<<grid, 256, 0, st>>>(logits, f, Tn, E, scale, grad);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const float* w,
                            const void* ys, void* y, int Tn, int d, int K, int num_sms,
                            cudaStream_t st) {

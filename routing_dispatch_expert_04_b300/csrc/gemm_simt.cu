@@ -23,7 +23,8 @@ __device__ __forceinline__ float gelu_erf(float v) {
 
 template <typename Tin, typename Tout, int EPI>
 __global__ void __launch_bounds__(256)
-simt_gemm_kernel(const Tin* __restrict__ A, const Tin* __restrict__ B, Tout* __restrict__ Cout,
+simt_gemm_kernel(const Tin* __restrict__ A, const int32_t* __restrict__ gather_src, int gather_k,
+                 int64_t gather_rows, const Tin* __restrict__ B, Tout* __restrict__ Cout,
                  const int32_t* __restrict__ offsets, int G, int M, int N, int Kd,
                  int64_t rows_cap, const float* __restrict__ bias, uint32_t* hdr) {
   constexpr int BM = 64, BN = 64, BK = 16;
@@ -85,7 +86,15 @@ simt_gemm_kernel(const Tin* __restrict__ A, const Tin* __restrict__ B, Tout* __r
       const int r = idx / BK, kk = idx % BK;
       const int64_t row = row0 + r;
       const int k = k0 + kk;
-      As[kk][r] = (row < rowend && k < Kd) ? Elem<Tin>::to_f(A[row * Kd + k]) : 0.f;
+      int64_t arow = row;  // A row: the packed row, or the token row it was gathered from
+      if (gather_src != nullptr && row < rowend) {
+        arow = gather_src[row] / gather_k;
+        if (arow < 0 || arow >= gather_rows) {
+          raise_error(hdr, DEV_ERR_BAD_ID);
+          arow = 0;
+        }
+      }
+      As[kk][r] = (row < rowend && k < Kd) ? Elem<Tin>::to_f(A[arow * Kd + k]) : 0.f;
       const int n = n0 + r;
       Bs[kk][r] = (n < N && k < Kd) ? Elem<Tin>::to_f(Bg[(size_t)n * Kd + k]) : 0.f;
     }
@@ -122,7 +131,8 @@ simt_gemm_kernel(const Tin* __restrict__ A, const Tin* __restrict__ B, Tout* __r
 
 // Grouped expert GEMM on CUDA cores.  gelu: GELU epilogue and dtype output (first
 // Linear); otherwise plain fp32 output (second Linear).
-cudaError_t launch_simt_grouped(int dtype, const void* A, const void* B, void* C,
+cudaError_t launch_simt_grouped(int dtype, const void* A, const int32_t* gather_src, int gather_k,
+                                int64_t gather_rows, const void* B, void* C,
                                 const int32_t* offsets, int G, int N, int Kd, int64_t rows_cap,
                                 bool gelu, uint32_t* hdr, cudaStream_t st) {
   const int64_t mt = (rows_cap + 63) / 64 + G;
@@ -130,18 +140,22 @@ cudaError_t launch_simt_grouped(int dtype, const void* A, const void* B, void* C
   if (dtype == MOE_BF16) {
     using T = __nv_bfloat16;
     if (gelu)
-      simt_gemm_kernel<T, T, EPI_GELU><<<grid, 256, 0, st>>>((const T*)A, (const T*)B, (T*)C, offsets,
-                                                             G, 0, N, Kd, rows_cap, nullptr, hdr);
+      simt_gemm_kernel<T, T, EPI_GELU><<<grid, 256, 0, st>>>((const T*)A, gather_src, gather_k, gather_rows,
+                                                             (const T*)B, (T*)C, offsets, G, 0, N,
+                                                             Kd, rows_cap, nullptr, hdr);
     else
       simt_gemm_kernel<T, float, EPI_NONE><<<grid, 256, 0, st>>>(
-          (const T*)A, (const T*)B, (float*)C, offsets, G, 0, N, Kd, rows_cap, nullptr, hdr);
+          (const T*)A, gather_src, gather_k, gather_rows, (const T*)B, (float*)C, offsets, G, 0, N,
+          Kd, rows_cap, nullptr, hdr);
   } else {
     if (gelu)
       simt_gemm_kernel<float, float, EPI_GELU><<<grid, 256, 0, st>>>(
-          (const float*)A, (const float*)B, (float*)C, offsets, G, 0, N, Kd, rows_cap, nullptr, hdr);
+          (const float*)A, gather_src, gather_k, gather_rows, (const float*)B, (float*)C, offsets,
+          G, 0, N, Kd, rows_cap, nullptr, hdr);
     else
       simt_gemm_kernel<float, float, EPI_NONE><<<grid, 256, 0, st>>>(
-          (const float*)A, (const float*)B, (float*)C, offsets, G, 0, N, Kd, rows_cap, nullptr, hdr);
+          (const float*)A, gather_src, gather_k, gather_rows, (const float*)B, (float*)C, offsets,
+          G, 0, N, Kd, rows_cap, nullptr, hdr);
   }
   count_launch();
   return cudaGetLastError();
@@ -154,10 +168,11 @@ cudaError_t launch_simt_router(int dtype, const void* x, const void* w_r, const 
   if (dtype == MOE_BF16) {
     using Tb = __nv_bfloat16;
     simt_gemm_kernel<Tb, float, EPI_BIAS><<<grid, 256, 0, st>>>(
-        (const Tb*)x, (const Tb*)w_r, logits, nullptr, 1, T, E, d, T, b_r, hdr);
+        (const Tb*)x, nullptr, 1, 0, (const Tb*)w_r, logits, nullptr, 1, T, E, d, T, b_r, hdr);
   } else {
     simt_gemm_kernel<float, float, EPI_BIAS><<<grid, 256, 0, st>>>(
-        (const float*)x, (const float*)w_r, logits, nullptr, 1, T, E, d, T, b_r, hdr);
+        (const float*)x, nullptr, 1, 0, (const float*)w_r, logits, nullptr, 1, T, E, d, T, b_r,
+        hdr);
   }
   count_launch();
   return cudaGetLastError();

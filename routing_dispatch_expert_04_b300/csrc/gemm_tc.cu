@@ -31,8 +31,8 @@ constexpr int TC_BM = 128;
 
 template <int BN, int STAGES>
 struct TcLayout {
-  static constexpr int A_BYTES = TC_BM * TC_BK * 2;
-  static constexpr int B_BYTES = BN * TC_BK * 2;
+  static constexpr int A_BYTES = TC_BM * TC_ROW_BYTES;
+  static constexpr int B_BYTES = BN * TC_ROW_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int B_OFF = STAGES * A_BYTES;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
@@ -45,7 +45,7 @@ struct TcLayout {
                                        : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
 };
 
-template <int BN, int STAGES, int EPI, bool F16IN>
+template <int BN, int STAGES, int EPI, int KIND, bool GATHER>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, const TcArgs args) {
@@ -65,7 +65,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
   const int n_tiles = (args.N + BN - 1) / BN;
-  const int nkb = (args.Kd + TC_BK - 1) / TC_BK;
+  constexpr int BKE = OpKind<KIND>::BK;  // K elements per stage
+  const int nkb = (args.Kd + BKE - 1) / BKE;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -96,8 +97,10 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const int total = tab->tpre[G] * ksplit;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (GATHER || lane == 0) {
       // ---------------------------------------------------------------- TMA producer
+      // Plain A: lane 0 issues one box per k-block.  Gathered A: every lane gathers four
+      // of the tile's 128 rows (tile::gather4) into their place in the stage.
       int s = 0;
       uint32_t ph = 0;
       int issued = 0;
@@ -107,16 +110,31 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const int brow = ti.g * args.N + ti.n0;
         const int kb0 = (t % ksplit) * args.kpb;
         const int kb1 = min(nkb, kb0 + args.kpb);
+        int tok[4] = {0, 0, 0, 0};
+        if (GATHER) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tok[i] = gather_row(args, ti.row0 + 4 * lane + i, ti.rowend);
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr)) {
+          bool got = true;
+          if (lane == 0) got = wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr);
+          if (GATHER) got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + s * Lay::A_BYTES;
           uint8_t* sb = smem + Lay::B_OFF + s * Lay::B_BYTES;
-          mbar_arrive_expect_tx(&full[s], Lay::STAGE_BYTES);
-          tma_load_2d(sa, &tmap_a, &full[s], kb * TC_BK, ti.row0);
-          tma_load_2d(sb, &tmap_b, &full[s], kb * TC_BK, brow);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], Lay::STAGE_BYTES);
+            if (!GATHER) tma_load_2d(sa, &tmap_a, &full[s], kb * BKE, ti.row0);
+            tma_load_2d(sb, &tmap_b, &full[s], kb * BKE, brow);
+          }
+          if (GATHER) {
+            __syncwarp();
+            tma_gather4(sa + lane * 4 * TC_ROW_BYTES, &tmap_a, &full[s], kb * BKE, tok[0], tok[1],
+                        tok[2], tok[3]);
+          }
           ++issued;
           if (++s == STAGES) {
             s = 0;
@@ -124,7 +142,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           }
         }
       }
-      if (!ok) {  // let the copies already in flight land before shared memory goes away
+      if (!ok && lane == 0) {  // let the copies already in flight land before shared memory goes away
         for (int i = 0; i < STAGES && i < issued; ++i) {
           if (--s < 0) {
             s = STAGES - 1;
@@ -138,8 +156,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t IDESC = F16IN ? (idesc_bf16_f32(TC_BM, BN) & ~((7u << 7) | (7u << 10)))
-                                       : idesc_bf16_f32(TC_BM, BN);
+      constexpr uint32_t IDESC = KIND == OP_BF16 ? idesc_bf16_f32(TC_BM, BN)
+                                                : idesc_fmt0_f32(TC_BM, BN);
       int s = 0;
       uint32_t ph = 0, acc = 0, aph = 0;
       bool ok = true;
@@ -158,9 +176,13 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
           const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < TC_BK / 16; ++k) {
-            mma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), IDESC,
-                     (kb != kb0 || k != 0) ? 1u : 0u);
+          for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
+            if (KIND == OP_E4M3)
+              mma_e4m3(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), IDESC,
+                       (kb != kb0 || k != 0) ? 1u : 0u);
+            else
+              mma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), IDESC,
+                       (kb != kb0 || k != 0) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
           if (++s == STAGES) {
@@ -191,6 +213,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       tc_fence_after();
       const int row = ti.row0 + r_in_tile;
       const bool valid = row < ti.rowend;
+      float sa = 0.f;  // E4M3: this row's A scale (of its token row when gathered)
+      if (KIND == OP_E4M3 && valid) sa = args.a_scale[GATHER ? gather_row(args, row, ti.rowend) : row];
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         const int col0 = ti.n0 + c * 32;
@@ -199,6 +223,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
         tmem_ld_wait();
         if (!valid) continue;
+        if (KIND == OP_E4M3) apply_scales(r, sa, args.b_scale + (size_t)ti.g * args.N, col0, args.N);
         if (epilogue_chunk<EPI>(r, row, col0, args, slice, bias)) raise_error(args.hdr, DEV_ERR_RANGE);
       }
       tc_fence_before();
@@ -229,27 +254,30 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
   return fn;
 }
 
-bool tc_make_map(CUtensorMap* m, const void* base, bool f16, uint64_t inner, uint64_t outer,
+bool tc_make_map(CUtensorMap* m, const void* base, int kind, uint64_t inner, uint64_t outer,
                  uint32_t box_outer) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = tc_encode_fn();
   if (fn == nullptr) return false;
+  const uint64_t esize = kind == OP_E4M3 ? 1 : 2;
   const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_outer};
+  const cuuint64_t strides[1] = {inner * esize};
+  const cuuint32_t box[2] = {(cuuint32_t)(TC_ROW_BYTES / esize), box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        2, const_cast<void*>(base), dims, strides, box, estr,
+  const CUtensorMapDataType dt = kind == OP_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : kind == OP_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int EPI, bool F16IN>
+template <int BN, int STAGES, int EPI, int KIND, bool GATHER = false>
 static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int num_sms,
                              cudaStream_t st) {
   using Lay = TcLayout<BN, STAGES>;
   static bool attr_set = false;
-  auto kern = tc_grouped_gemm_kernel<BN, STAGES, EPI, F16IN>;
+  auto kern = tc_grouped_gemm_kernel<BN, STAGES, EPI, KIND, GATHER>;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return e;
@@ -257,8 +285,10 @@ static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int 
   }
   CUtensorMap ma, mb;
   const int64_t a_rows = a.rows_cap > 0 ? a.rows_cap : 1;
-  if (!tc_make_map(&ma, A, F16IN, (uint64_t)a.Kd, (uint64_t)a_rows, TC_BM)) return cudaErrorInvalidValue;
-  if (!tc_make_map(&mb, B, F16IN, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN)) return cudaErrorInvalidValue;
+  const bool ok_a = GATHER ? tc_make_map(&ma, A, KIND, (uint64_t)a.Kd, (uint64_t)a.gather_rows, 1)
+                           : tc_make_map(&ma, A, KIND, (uint64_t)a.Kd, (uint64_t)a_rows, TC_BM);
+  if (!ok_a) return cudaErrorInvalidValue;
+  if (!tc_make_map(&mb, B, KIND, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN)) return cudaErrorInvalidValue;
   const int64_t n_tiles = (a.N + BN - 1) / BN;
   const int64_t m_bound = (a.rows_cap + TC_BM - 1) / TC_BM + (a.offsets ? a.G : 0);
   int64_t grid = m_bound * n_tiles * a.ksplit;
@@ -298,7 +328,8 @@ static int pick_bn(int64_t rows_cap, int G, int64_t cap_per_group, int N, int nu
   return best_bn;
 }
 
-cudaError_t launch_tc2_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
+cudaError_t launch_tc2_up(const void* a_in, const int32_t* gather_src, int gather_k,
+                          int64_t gather_rows, const void* w1, void* h, const int32_t* offsets,
                           int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
                           int num_sms, cudaStream_t st);
 cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
@@ -328,30 +359,37 @@ static int gemm_plan(int mode, int64_t rows_cap, int G, int64_t cap_per_group, i
   return rows256 * 100 <= rows128 * 105 ? PLAN_PAIR : PLAN_SINGLE;
 }
 
-template <int EPI, bool F16IN>
-static cudaError_t launch_tc_single(const void* A, const void* B, void* out, const int32_t* offsets,
-                                    int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
-                                    int row_part, uint32_t* hdr, int num_sms, cudaStream_t st) {
-  TcArgs a{offsets, G, 0, N, Kd, rows_cap, out, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
-           row_part};
-  if (pick_bn(rows_cap, G, cap_per_group, N, num_sms) == 192)
-    return launch_tc<192, 5, EPI, F16IN>(A, B, a, num_sms, st);
-  return launch_tc<256, 4, EPI, F16IN>(A, B, a, num_sms, st);
+template <int EPI, int KIND, bool GATHER>
+static cudaError_t launch_tc_single(const void* A, const void* B, const TcArgs& a,
+                                    int64_t cap_per_group, int num_sms, cudaStream_t st) {
+  if (pick_bn(a.rows_cap, a.G, cap_per_group, a.N, num_sms) == 192)
+    return launch_tc<192, 5, EPI, KIND, GATHER>(A, B, a, num_sms, st);
+  return launch_tc<256, 4, EPI, KIND, GATHER>(A, B, a, num_sms, st);
 }
 
-// First expert Linear, bf16 in, GELU fused, fp16 out: h[r] = GELU(x_perm[r] . W1[g]^T).
-cudaError_t launch_tc_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets, int G,
-                         int N, int Kd, int64_t rows_cap, int64_t cap_per_group, int pair_mode,
-                         uint32_t* hdr, int num_sms, cudaStream_t st) {
+// First expert Linear, bf16 in, GELU fused, fp16 out: h[r] = GELU(A[r] . W1[g]^T), with
+// A = x_perm, or with `gather_src` A[r] = x[gather_src[r] / gather_k] gathered from the
+// token matrix x ([gather_rows, Kd]) while the tile is loaded.
+cudaError_t launch_tc_up(const void* a_in, const int32_t* gather_src, int gather_k,
+                         int64_t gather_rows, const void* w1, void* h, const int32_t* offsets,
+                         int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
+                         int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st) {
   const int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
+  const bool gather = gather_src != nullptr;
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
+           TC_ROWS_ALL, gather_src, gather_k, gather_rows};
   if (plan == PLAN_SINGLE)
-    return launch_tc_single<TC_EPI_GELU_F16, false>(x_perm, w1, h, offsets, G, N, Kd, rows_cap,
-                                                    cap_per_group, TC_ROWS_ALL, hdr, num_sms, st);
-  cudaError_t e = launch_tc2_up(x_perm, w1, h, offsets, G, N, Kd, rows_cap,
-                                plan == PLAN_PAIR ? TC_ROWS_ALL : TC_ROWS_FULL256, hdr, num_sms, st);
+    return gather ? launch_tc_single<TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, cap_per_group,
+                                                                  num_sms, st)
+                  : launch_tc_single<TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, cap_per_group,
+                                                                   num_sms, st);
+  cudaError_t e = launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd,
+                                rows_cap, plan == PLAN_PAIR ? TC_ROWS_ALL : TC_ROWS_FULL256, hdr,
+                                num_sms, st);
   if (e != cudaSuccess || plan == PLAN_PAIR) return e;
-  return launch_tc_single<TC_EPI_GELU_F16, false>(x_perm, w1, h, offsets, G, N, Kd, rows_cap,
-                                                  G > 0 ? 255 : 0, TC_ROWS_REST256, hdr, num_sms, st);
+  a.row_part = TC_ROWS_REST256;
+  return gather ? launch_tc_single<TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, 255, num_sms, st)
+                : launch_tc_single<TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, 255, num_sms, st);
 }
 
 // Second expert Linear, fp16 in, fp32 out: y_perm[r] = h[r] . W2[g]^T.
@@ -359,14 +397,43 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
                            int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
                            int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st) {
   const int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
+           TC_ROWS_ALL};
   if (plan == PLAN_SINGLE)
-    return launch_tc_single<TC_EPI_F32, true>(h, w2h, y_perm, offsets, G, N, Kd, rows_cap,
-                                              cap_per_group, TC_ROWS_ALL, hdr, num_sms, st);
+    return launch_tc_single<TC_EPI_F32, OP_F16, false>(h, w2h, a, cap_per_group, num_sms, st);
   cudaError_t e = launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap,
                                   plan == PLAN_PAIR ? TC_ROWS_ALL : TC_ROWS_FULL256, hdr, num_sms, st);
   if (e != cudaSuccess || plan == PLAN_PAIR) return e;
-  return launch_tc_single<TC_EPI_F32, true>(h, w2h, y_perm, offsets, G, N, Kd, rows_cap,
-                                            G > 0 ? 255 : 0, TC_ROWS_REST256, hdr, num_sms, st);
+  a.row_part = TC_ROWS_REST256;
+  return launch_tc_single<TC_EPI_F32, OP_F16, false>(h, w2h, a, 255, num_sms, st);
+}
+
+// First expert Linear on E4M3 operands (codes + per-row scales), GELU fused, fp16 out:
+// h[r] = GELU(sx[a(r)] * sw1[g*N + n] * sum_k xq[a(r), k] w1q[g*N + n, k]) with
+// a(r) = gather_src[r] / gather_k (the token row) when gather_src is given, else r.
+cudaError_t launch_tc_up_e4m3(const void* xq, const float* sx, const int32_t* gather_src,
+                              int gather_k, int64_t gather_rows, const void* w1q, const float* sw1,
+                              void* h, const int32_t* offsets, int G, int N, int Kd,
+                              int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr, int num_sms,
+                              cudaStream_t st) {
+  constexpr int BKE = OpKind<OP_E4M3>::BK;
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + BKE - 1) / BKE, 0,
+           TC_ROWS_ALL, gather_src, gather_k, gather_rows, sx, sw1};
+  if (gather_src != nullptr)
+    return launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, true>(xq, w1q, a, cap_per_group, num_sms, st);
+  return launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, false>(xq, w1q, a, cap_per_group, num_sms, st);
+}
+
+// Second expert Linear on E4M3 operands, fp32 out:
+// y_perm[r] = sh[r] * sw2[g*N + n] * sum_k hq[r, k] w2q[g*N + n, k].
+cudaError_t launch_tc_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
+                                void* y_perm, const int32_t* offsets, int G, int N, int Kd,
+                                int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr,
+                                int num_sms, cudaStream_t st) {
+  constexpr int BKE = OpKind<OP_E4M3>::BK;
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + BKE - 1) / BKE, 0,
+           TC_ROWS_ALL, nullptr, 1, 0, sh, sw2};
+  return launch_tc_single<TC_EPI_F32, OP_E4M3, false>(hq, w2q, a, cap_per_group, num_sms, st);
 }
 
 // Router Linear, bf16 in, fp32 logits: logits[t] = x[t] . W_r^T + b_r.  With nsplit > 1
@@ -380,10 +447,10 @@ cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, f
   TcArgs a{nullptr, 1, T, E, d, (int64_t)T, out, E, b_r, hdr, ks, kpb, (int64_t)T * E,
            TC_ROWS_ALL};
   // the epilogue reads TMEM 32 columns at a time, so the narrowest tile is 32 wide
-  if (E <= 32) return launch_tc<32, 8, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
-  if (E <= 64) return launch_tc<64, 8, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
-  if (E <= 128) return launch_tc<128, 6, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
-  return launch_tc<256, 4, TC_EPI_BIAS_F32, false>(x, w_r, a, num_sms, st);
+  if (E <= 32) return launch_tc<32, 8, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st);
+  if (E <= 64) return launch_tc<64, 8, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st);
+  if (E <= 128) return launch_tc<128, 6, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st);
+  return launch_tc<256, 4, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st);
 }
 
 }  // namespace moe

@@ -27,8 +27,8 @@ constexpr int TC2_CTA_ROWS = 128;
 
 template <int BN, int STAGES>
 struct Tc2Layout {
-  static constexpr int A_BYTES = TC2_CTA_ROWS * TC_BK * 2;
-  static constexpr int B_BYTES = (BN / 2) * TC_BK * 2;
+  static constexpr int A_BYTES = TC2_CTA_ROWS * TC_ROW_BYTES;
+  static constexpr int B_BYTES = (BN / 2) * TC_ROW_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int B_OFF = STAGES * A_BYTES;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
@@ -45,11 +45,12 @@ struct Tc2Layout {
 // barrier) to land before its shared memory is released.
 constexpr uint64_t PAIR_ABORT_SETTLE_NS = 200000ull;
 
-template <int BN, int STAGES, int EPI, bool F16IN>
+template <int BN, int STAGES, int EPI, int KIND, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const TcArgs args) {
   using Lay = Tc2Layout<BN, STAGES>;
+  static_assert(KIND != OP_E4M3, "E4M3 operands run on the one-CTA kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + Lay::BAR_OFF);
@@ -67,7 +68,8 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
   const int G = args.G;
   const int n_tiles = (args.N + BN - 1) / BN;
-  const int nkb = (args.Kd + TC_BK - 1) / TC_BK;
+  constexpr int BKE = OpKind<KIND>::BK;  // K elements per stage
+  const int nkb = (args.Kd + BKE - 1) / BKE;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -98,8 +100,10 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   const int total = tab->tpre[G];
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (GATHER || lane == 0) {
       // ---------------------------------------------------------------- TMA producer
+      // Plain A: lane 0 issues one box per k-block.  Gathered A: every lane gathers four
+      // of this CTA's 128 rows (tile::gather4) into their place in the stage.
       int s = 0;
       uint32_t ph = 0;
       int issued = 0;
@@ -108,17 +112,32 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const TileInfo ti = decode_tile<TC2_BM>(t, G, tab, BN);
         const int arow = ti.row0 + (int)rank * TC2_CTA_ROWS;
         const int brow = ti.g * args.N + ti.n0 + (int)rank * (BN / 2);
+        int tok[4] = {0, 0, 0, 0};
+        if (GATHER) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tok[i] = gather_row(args, arow + 4 * lane + i, ti.rowend);
+        }
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr)) {
+          bool got = true;
+          if (lane == 0) got = wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr);
+          if (GATHER) got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + s * Lay::A_BYTES;
           uint8_t* sb = smem + Lay::B_OFF + s * Lay::B_BYTES;
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Lay::STAGE_BYTES);
           const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's full[s]
-          tma_load_2d_pair(sa, &tmap_a, fb, kb * TC_BK, arow);
-          tma_load_2d_pair(sb, &tmap_b, fb, kb * TC_BK, brow);
+          if (lane == 0) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Lay::STAGE_BYTES);
+            if (!GATHER) tma_load_2d_pair(sa, &tmap_a, fb, kb * BKE, arow);
+            tma_load_2d_pair(sb, &tmap_b, fb, kb * BKE, brow);
+          }
+          if (GATHER) {
+            __syncwarp();
+            tma_gather4_pair(sa + lane * 4 * TC_ROW_BYTES, &tmap_a, fb, kb * BKE, tok[0], tok[1],
+                             tok[2], tok[3]);
+          }
           ++issued;
           if (++s == STAGES) {
             s = 0;
@@ -126,7 +145,7 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         if (rank == 0) {  // the even CTA can see its stages complete
           for (int i = 0; i < STAGES && i < issued; ++i) {
             if (--s < 0) {
@@ -146,8 +165,8 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t IDESC = F16IN ? (idesc_bf16_f32(TC2_BM, BN) & ~((7u << 7) | (7u << 10)))
-                                       : idesc_bf16_f32(TC2_BM, BN);
+      constexpr uint32_t IDESC = KIND == OP_BF16 ? idesc_bf16_f32(TC2_BM, BN)
+                                                : idesc_fmt0_f32(TC2_BM, BN);
       int s = 0;
       uint32_t ph = 0, acc = 0, aph = 0;
       bool ok = true;
@@ -164,7 +183,7 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
           const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < TC_BK / 16; ++k) {
+          for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
             mma_f16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), IDESC,
                          (kb != 0 || k != 0) ? 1u : 0u);
           }
@@ -220,12 +239,12 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   if (warp == 1) tmem_dealloc_pair(tmem_base, Lay::TMEM_COLS);
 }
 
-template <int BN, int STAGES, int EPI, bool F16IN>
+template <int BN, int STAGES, int EPI, int KIND, bool GATHER>
 static cudaError_t launch_tc2(const void* A, const void* B, const TcArgs& a, int num_sms,
                               cudaStream_t st) {
   using Lay = Tc2Layout<BN, STAGES>;
   static bool attr_set = false;
-  auto kern = tc2_grouped_gemm_kernel<BN, STAGES, EPI, F16IN>;
+  auto kern = tc2_grouped_gemm_kernel<BN, STAGES, EPI, KIND, GATHER>;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return e;
@@ -233,9 +252,11 @@ static cudaError_t launch_tc2(const void* A, const void* B, const TcArgs& a, int
   }
   CUtensorMap ma, mb;
   const int64_t a_rows = a.rows_cap > 0 ? a.rows_cap : 1;
-  if (!tc_make_map(&ma, A, F16IN, (uint64_t)a.Kd, (uint64_t)a_rows, TC2_CTA_ROWS))
-    return cudaErrorInvalidValue;
-  if (!tc_make_map(&mb, B, F16IN, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN / 2))
+  const bool ok_a = GATHER ? tc_make_map(&ma, A, KIND, (uint64_t)a.Kd, (uint64_t)a.gather_rows, 1)
+                           : tc_make_map(&ma, A, KIND, (uint64_t)a.Kd, (uint64_t)a_rows,
+                                         TC2_CTA_ROWS);
+  if (!ok_a) return cudaErrorInvalidValue;
+  if (!tc_make_map(&mb, B, KIND, (uint64_t)a.Kd, (uint64_t)a.G * a.N, BN / 2))
     return cudaErrorInvalidValue;
   const int64_t n_tiles = (a.N + BN - 1) / BN;
   const int64_t m_bound = (a.rows_cap + TC2_BM - 1) / TC2_BM + (a.offsets ? a.G : 0);
@@ -248,13 +269,16 @@ static cudaError_t launch_tc2(const void* A, const void* B, const TcArgs& a, int
 }
 
 // First expert Linear on CTA pairs, bf16 in, GELU fused, fp16 out, over the rows that
-// `row_part` selects.
-cudaError_t launch_tc2_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
+// `row_part` selects; with `gather_src` the A rows are gathered from the token matrix.
+cudaError_t launch_tc2_up(const void* a_in, const int32_t* gather_src, int gather_k,
+                          int64_t gather_rows, const void* w1, void* h, const int32_t* offsets,
                           int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
                           int num_sms, cudaStream_t st) {
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
-           row_part};
-  return launch_tc2<256, 6, TC_EPI_GELU_F16, false>(x_perm, w1, a, num_sms, st);
+           row_part, gather_src, gather_k, gather_rows};
+  if (gather_src != nullptr)
+    return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, num_sms, st);
+  return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, num_sms, st);
 }
 
 // Second expert Linear on CTA pairs, fp16 in, fp32 out.
@@ -263,7 +287,7 @@ cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const 
                             int num_sms, cudaStream_t st) {
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            row_part};
-  return launch_tc2<256, 6, TC_EPI_F32, true>(h, w2h, a, num_sms, st);
+  return launch_tc2<256, 6, TC_EPI_F32, OP_F16, false>(h, w2h, a, num_sms, st);
 }
 
 }  // namespace moe

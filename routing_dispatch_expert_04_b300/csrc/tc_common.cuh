@@ -19,6 +19,14 @@
 namespace moe {
 
 constexpr int TC_BK = 64;  // 64 bf16/fp16 = one 128-byte swizzle row
+constexpr int TC_ROW_BYTES = 128;  // bytes of K per stage row (a 128-byte swizzle row)
+
+// Operand kinds of the expert GEMMs.
+enum { OP_BF16 = 0, OP_F16 = 1, OP_E4M3 = 2 };
+template <int KIND> struct OpKind {
+  static constexpr int BYTES = KIND == OP_E4M3 ? 1 : 2;
+  static constexpr int BK = TC_ROW_BYTES / BYTES;  // K elements per stage
+};
 constexpr int TC_THREADS = 192;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
@@ -39,7 +47,24 @@ struct TcArgs {
   int64_t split_stride;    // elements between the partial slices of `out`
   int row_part;            // rows of each group this launch covers: 0 all; 1 the leading
                            //   whole 256-row tiles; 2 the rest (fewer than 256 rows)
+  const int32_t* gather_src;  // non-null: A row r is row gather_src[r] / gather_k of the
+  int gather_k;               //   gathered matrix (token rows of X), which has
+  int64_t gather_rows;        //   gather_rows rows
+  const float* a_scale;    // E4M3 operands: per-row scale of A (per token row when gathered)
+  const float* b_scale;    //   and of B (per row of the stacked weights, g*N + n)
 };
+
+// Token row of packed row r of a gathered A operand (row 0 for rows past the group,
+// whose results are never stored; an out-of-range index is reported and replaced by 0).
+__device__ __forceinline__ int gather_row(const TcArgs& args, int r, int rowend) {
+  if (r >= rowend) return 0;
+  const int tok = args.gather_src[r] / args.gather_k;
+  if (tok < 0 || (int64_t)tok >= args.gather_rows) {
+    raise_error(args.hdr, DEV_ERR_BAD_ID);
+    return 0;
+  }
+  return tok;
+}
 
 constexpr int TC_ROWS_ALL = 0, TC_ROWS_FULL256 = 1, TC_ROWS_REST256 = 2;
 
@@ -152,6 +177,17 @@ __device__ __forceinline__ float gelu_exact(float v) {
   return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
 }
 
+// E4M3 operands: the accumulator holds sum_k qa*qb; the real product is that times the
+// row's A scale and the column's B scale.
+__device__ __forceinline__ void apply_scales(uint32_t (&r)[32], float sa, const float* sb_row,
+                                             int col0, int N) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float sb = (col0 + i < N) ? sb_row[col0 + i] : 0.f;
+    r[i] = __float_as_uint(__uint_as_float(r[i]) * sa * sb);
+  }
+}
+
 // Epilogue for 32 accumulator columns [col0, col0+32) of one output row, held by this
 // thread in r[] (fp32 bit patterns).  Returns true if a GELU output left the fp16 range.
 template <int EPI>
@@ -196,9 +232,9 @@ __device__ __forceinline__ bool epilogue_chunk(const uint32_t (&r)[32], int row,
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn();
 
-// 2-D tensor map of a row-major [outer, inner] 16-bit matrix, box [box_outer, 64],
-// 128-byte swizzle.
-bool tc_make_map(CUtensorMap* m, const void* base, bool f16, uint64_t inner, uint64_t outer,
+// 2-D tensor map of a row-major [outer, inner] matrix of operand kind `kind`, box
+// [box_outer rows, 128 bytes], 128-byte swizzle.
+bool tc_make_map(CUtensorMap* m, const void* base, int kind, uint64_t inner, uint64_t outer,
                  uint32_t box_outer);
 
 }  // namespace moe

@@ -23,8 +23,16 @@ from . import native as N
 class MoELayer:
     def __init__(self, T, d, E, K, F, dtype, capacity_factor, alpha, w_r, b_r, w1, w2,
                  w1s=None, w2s=None, renormalize=False, device="cuda", overlap=True,
-                 drop_order="token", capacity_mode="tokens", sel_bias=None):
-        """``drop_order``: "token" (flat order) or "slot" (first choices first) decides which
+                 drop_order="token", capacity_mode="tokens", sel_bias=None,
+                 fused_dispatch=False, experts="bf16"):
+        """``fused_dispatch``: the first expert Linear gathers its rows from x while loading
+        them (moe_expert_up_gather), so the dispatch step writes only the routing plan;
+        by default the dispatch copies the rows into x_perm first, which measures faster
+        on B300 (TMA row gathers move 512 bytes per instruction).
+        ``experts``: "bf16" (default) or "e4m3": the FP8 variant of the expert Linears
+        (per-row E4M3 operands, moe_expert_up_e4m3 / moe_expert_down_e4m3); bf16 layers
+        only.
+        ``drop_order``: "token" (flat order) or "slot" (first choices first) decides which
         assignments a full expert drops.  ``capacity_mode``: "tokens" gives the capacity as
         printed, C = floor(T/E * cf); "assignments" counts top-K assignments,
         C = floor(T*K/E * cf).  ``sel_bias``: optional [E] fp32 device tensor, a
@@ -54,7 +62,8 @@ class MoELayer:
         self.offsets = torch.empty(E + 1, dtype=i32, device=dev)
         self.slot = torch.empty((T, K), dtype=i32, device=dev)
         self.src = torch.empty(R, dtype=i32, device=dev)
-        self.x_perm = torch.empty((R, d), dtype=dt, device=dev)
+        self.fused_dispatch = fused_dispatch
+        self.x_perm = None if fused_dispatch else torch.empty((R, d), dtype=dt, device=dev)
         # the intermediate activation is fp16 for bf16 layers (see moe_expert_up)
         self.h_dtype = torch.float16 if dtype == "bf16" else torch.float32
         self.h = torch.empty((R, F), dtype=self.h_dtype, device=dev)
@@ -69,13 +78,40 @@ class MoELayer:
         self.overlap = overlap
         self.side = torch.cuda.Stream(device=dev) if overlap else None
         self.graph = None
-        self.w2 = self._down_weights(w2)
+        if experts not in ("bf16", "e4m3") or (experts == "e4m3" and dtype != "bf16"):
+            raise ValueError(f"experts={experts!r} with dtype={dtype!r}")
+        self.experts = experts
         self.shared = w1s is not None
-        self.w2s = self._down_weights(w2s) if self.shared else None
         if self.shared:
             self.shared_offsets = torch.tensor([0, T], dtype=i32, device=dev)
             self.h_s = torch.empty((max(T, 1), F), dtype=self.h_dtype, device=dev)
             self.y_s = torch.empty((max(T, 1), d), dtype=f32, device=dev)
+        if experts == "bf16":
+            self.w2 = self._down_weights(w2)
+            self.w2s = self._down_weights(w2s) if self.shared else None
+            return
+        # E4M3 experts: weights quantised once per output channel, activation buffers
+        u8 = torch.uint8
+        self.w1q, self.w1_sc = self._quantized(w1.reshape(E * F, d))
+        self.w2q, self.w2_sc = self._quantized(w2.reshape(E * d, F))
+        xrows = T if fused_dispatch else R
+        self.xq = torch.empty((max(xrows, 1), d), dtype=u8, device=dev)
+        self.x_sc = torch.empty(max(xrows, 1), dtype=f32, device=dev)
+        self.hq = torch.empty((R, F), dtype=u8, device=dev)
+        self.h_sc = torch.empty(R, dtype=f32, device=dev)
+        if self.shared:
+            self.w1sq, self.w1s_sc = self._quantized(w1s.reshape(F, d))
+            self.w2sq, self.w2s_sc = self._quantized(w2s.reshape(d, F))
+            self.xsq = torch.empty((max(T, 1), d), dtype=u8, device=dev)
+            self.xs_sc = torch.empty(max(T, 1), dtype=f32, device=dev)
+            self.hsq = torch.empty((max(T, 1), F), dtype=u8, device=dev)
+            self.hs_sc = torch.empty(max(T, 1), dtype=f32, device=dev)
+
+    def _quantized(self, w):
+        codes = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+        scales = torch.empty(w.shape[0], dtype=torch.float32, device=w.device)
+        N.quantize_e4m3(w, codes, scales)
+        return codes, scales
 
     def _down_weights(self, w2):
         """Second-Linear weights in the operand type the kernels take: an fp16 copy of bf16
@@ -91,12 +127,13 @@ class MoELayer:
 
     @classmethod
     def from_workload(cls, wl, inputs, device="cuda", renormalize=False, overlap=True,
-                      drop_order="token", capacity_mode="tokens", sel_bias=None):
+                      drop_order="token", capacity_mode="tokens", sel_bias=None,
+                      fused_dispatch=False, experts="bf16"):
         return cls(wl.T, wl.d, wl.E, wl.K, wl.F, wl.dtype, wl.capacity_factor, wl.alpha,
                    inputs["w_r"], inputs["b_r"], inputs["w1"], inputs["w2"],
                    inputs.get("w1s"), inputs.get("w2s"), renormalize=renormalize, device=device,
                    overlap=overlap, drop_order=drop_order, capacity_mode=capacity_mode,
-                   sel_bias=sel_bias)
+                   sel_bias=sel_bias, fused_dispatch=fused_dispatch, experts=experts)
 
     # ---------------------------------------------------------------- stages
     def route(self, x, stream=None, logits_in=None):
@@ -121,18 +158,49 @@ class MoELayer:
         N.adjust_select_bias(self.cfg, self.counts, self.sel_bias, gamma, stream)
 
     def dispatch(self, x, stream=None):
-        N.dispatch(self.cfg, x, self.ids, self.counts, self.offsets, self.slot, self.src,
-                   None if x is None else self.x_perm, self.ws, stream)
+        """Routing plan (counts, offsets, slot, src); with the unfused dispatch also the
+        row copy into x_perm."""
+        copy = x is not None and not self.fused_dispatch
+        N.dispatch(self.cfg, x if copy else None, self.ids, self.counts, self.offsets, self.slot,
+                   self.src, self.x_perm if copy else None, self.ws, stream)
 
-    def experts_up(self, stream=None):
-        N.expert_up(self.cfg, self.x_perm, self.offsets, self.E, self.rows_cap, self.w1, self.h,
-                    self.ws, stream)
+    def experts_up(self, x, stream=None):
+        if self.experts == "e4m3":
+            kept = self.offsets[self.E:]  # rows actually packed (device)
+            if self.fused_dispatch:
+                N.quantize_e4m3(x, self.xq, self.x_sc, None, stream)
+                N.expert_up_e4m3(self.cfg, self.xq, self.x_sc, self.src, self.offsets, self.E,
+                                 self.rows_cap, self.w1q, self.w1_sc, self.h, self.ws, stream)
+            else:
+                N.quantize_e4m3(self.x_perm, self.xq, self.x_sc, kept, stream)
+                N.expert_up_e4m3(self.cfg, self.xq, self.x_sc, None, self.offsets, self.E,
+                                 self.rows_cap, self.w1q, self.w1_sc, self.h, self.ws, stream)
+            return
+        if self.fused_dispatch:
+            N.expert_up_gather(self.cfg, x, self.src, self.offsets, self.E, self.rows_cap,
+                               self.w1, self.h, self.ws, stream)
+        else:
+            N.expert_up(self.cfg, self.x_perm, self.offsets, self.E, self.rows_cap, self.w1,
+                        self.h, self.ws, stream)
 
     def experts_down(self, stream=None):
+        if self.experts == "e4m3":
+            N.quantize_e4m3(self.h, self.hq, self.h_sc, self.offsets[self.E:], stream)
+            N.expert_down_e4m3(self.cfg, self.hq, self.h_sc, self.offsets, self.E, self.rows_cap,
+                               self.w2q, self.w2_sc, self.y_perm, self.ws, stream)
+            return
         N.expert_down(self.cfg, self.h, self.offsets, self.E, self.rows_cap, self.w2, self.y_perm,
                       self.ws, stream)
 
     def shared_expert(self, x, stream=None):
+        if self.experts == "e4m3":
+            N.quantize_e4m3(x, self.xsq, self.xs_sc, None, stream)
+            N.expert_up_e4m3(self.cfg, self.xsq, self.xs_sc, None, self.shared_offsets, 1, self.T,
+                             self.w1sq, self.w1s_sc, self.h_s, self.ws, stream)
+            N.quantize_e4m3(self.h_s, self.hsq, self.hs_sc, None, stream)
+            N.expert_down_e4m3(self.cfg, self.hsq, self.hs_sc, self.shared_offsets, 1, self.T,
+                               self.w2sq, self.w2s_sc, self.y_s, self.ws, stream)
+            return
         N.expert_up(self.cfg, x, self.shared_offsets, 1, self.T, self.w1s, self.h_s, self.ws, stream)
         N.expert_down(self.cfg, self.h_s, self.shared_offsets, 1, self.T, self.w2s, self.y_s, self.ws,
                       stream)
@@ -171,7 +239,7 @@ class MoELayer:
             mark(1)
             self.dispatch(x, stream)
             mark(2)
-            self.experts_up(stream)
+            self.experts_up(x, stream)
             mark(3)
             self.experts_down(stream)
             i = 4
@@ -205,7 +273,7 @@ class MoELayer:
         joined = torch.cuda.Event()
         joined.record(side)
         mark(2)
-        self.experts_up()
+        self.experts_up(x)
         mark(3)
         self.experts_down()
         mark(4)

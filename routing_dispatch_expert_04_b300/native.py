@@ -16,15 +16,16 @@ from fractions import Fraction
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 
-MOE_F32, MOE_BF16 = 0, 1
+MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
           4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_DEVICE"}
 
 EXPORTS = ("moe_workspace_size", "moe_rows_capacity", "moe_route", "moe_route_select_bias",
            "moe_adjust_select_bias", "moe_dispatch",
            "moe_dispatch_noalloc",
-           "moe_expert_up", "moe_expert_down", "moe_grouped_ffn", "moe_combine",
-           "moe_aux_stats", "moe_bf16_to_f16", "moe_sync_status", "moe_status_string", "moe_launch_count",
+           "moe_expert_up", "moe_expert_up_gather", "moe_expert_down", "moe_quantize_e4m3",
+           "moe_expert_up_e4m3", "moe_expert_down_e4m3", "moe_grouped_ffn", "moe_combine",
+           "moe_aux_stats", "moe_aux_loss_grad", "moe_bf16_to_f16", "moe_sync_status", "moe_status_string", "moe_launch_count",
            "moe_test_arm_scan_timeout", "moe_set_gemm_pairing")
 
 
@@ -53,11 +54,20 @@ _SIGS = {
     "moe_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_up": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P]),
+    "moe_expert_up_gather": (ctypes.c_int, [_CFG, _P, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P,
+                                            _P, _P]),
     "moe_expert_down": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P]),
+    "moe_quantize_e4m3": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _P, _P, _P,
+                                         _P]),
+    "moe_expert_up_e4m3": (ctypes.c_int, [_CFG, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P,
+                                          _P, _P, _P]),
+    "moe_expert_down_e4m3": (ctypes.c_int, [_CFG, _P, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P,
+                                            _P, _P, _P]),
     "moe_grouped_ffn": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P,
                                        _P, _P]),
     "moe_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_aux_stats": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
+    "moe_aux_loss_grad": (ctypes.c_int, [_CFG, _P, _P, _P, _P]),
     "moe_bf16_to_f16": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, _P]),
     "moe_sync_status": (ctypes.c_int, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -171,6 +181,37 @@ def expert_up(cfg, x_perm, offsets, n_groups, rows_cap, w1, h, ws, stream=None):
                                                  rows_cap, _ptr(w1), _ptr(h), _ptr(ws), _stream(stream)))
 
 
+def expert_up_gather(cfg, x, src, offsets, n_groups, rows_cap, w1, h, ws, stream=None):
+    """First expert Linear with the dispatch fused in: rows gathered from x by src."""
+    _check("moe_expert_up_gather", lib().moe_expert_up_gather(
+        ctypes.byref(cfg), _ptr(x), _ptr(src), _ptr(offsets), n_groups, rows_cap, _ptr(w1),
+        _ptr(h), _ptr(ws), _stream(stream)))
+
+
+def quantize_e4m3(src, codes, scales, rows_dev=None, stream=None):
+    """Per-row E4M3 codes (uint8 tensor shaped like src) and fp32 scales of a 2-D fp32,
+    bf16 or fp16 tensor; ``rows_dev``: optional device int32 bounding the rows done."""
+    import torch
+    dt = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16, torch.float16: MOE_F16}[src.dtype]
+    rows, cols = src.shape
+    _check("moe_quantize_e4m3", lib().moe_quantize_e4m3(_ptr(src), dt, rows, cols, _ptr(rows_dev),
+                                                         _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def expert_up_e4m3(cfg, xq, x_scale, src, offsets, n_groups, rows_cap, w1q, w1_scale, h, ws,
+                   stream=None):
+    _check("moe_expert_up_e4m3", lib().moe_expert_up_e4m3(
+        ctypes.byref(cfg), _ptr(xq), _ptr(x_scale), _ptr(src), _ptr(offsets), n_groups, rows_cap,
+        _ptr(w1q), _ptr(w1_scale), _ptr(h), _ptr(ws), _stream(stream)))
+
+
+def expert_down_e4m3(cfg, hq, h_scale, offsets, n_groups, rows_cap, w2q, w2_scale, y_perm, ws,
+                     stream=None):
+    _check("moe_expert_down_e4m3", lib().moe_expert_down_e4m3(
+        ctypes.byref(cfg), _ptr(hq), _ptr(h_scale), _ptr(offsets), n_groups, rows_cap, _ptr(w2q),
+        _ptr(w2_scale), _ptr(y_perm), _ptr(ws), _stream(stream)))
+
+
 def expert_down(cfg, h, offsets, n_groups, rows_cap, w2, y_perm, ws, stream=None):
     _check("moe_expert_down", lib().moe_expert_down(ctypes.byref(cfg), _ptr(h), _ptr(offsets), n_groups,
                                                      rows_cap, _ptr(w2), _ptr(y_perm), _ptr(ws),
@@ -191,6 +232,12 @@ def combine(cfg, y_perm, slot, topk_w, y_shared, y, stream=None):
 def aux_stats(cfg, counts, ws, f, P, l_aux, stream=None):
     _check("moe_aux_stats", lib().moe_aux_stats(ctypes.byref(cfg), _ptr(counts), _ptr(ws), _ptr(f),
                                                  _ptr(P), _ptr(l_aux), _stream(stream)))
+
+
+def aux_loss_grad(cfg, logits, f, grad_logits, stream=None):
+    """Gradient of the auxiliary loss with respect to the router logits."""
+    _check("moe_aux_loss_grad", lib().moe_aux_loss_grad(ctypes.byref(cfg), _ptr(logits), _ptr(f),
+                                                         _ptr(grad_logits), _stream(stream)))
 
 
 def bf16_to_f16(src, dst, ws, stream=None):

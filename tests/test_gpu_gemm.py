@@ -158,3 +158,60 @@ def test_single_and_pair_kernels_agree_bitwise(fn):
         outs.append(out.cpu())
     assert torch.equal(outs[0], outs[1])
     assert torch.equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("offs,T,K", [([0, 128], 300, 2), ([0, 0, 130, 131, 400, 520], 700, 3),
+                                      ([0, 600, 600, 856, 1111, 1367], 900, 2)])
+def test_expert_up_gather(offs, T, K, dtype, pairing):
+    """Dispatch fused into the first expert Linear: packed row r is gathered from token
+    row src[r] // K of x while the tile loads.  Against the oracle, and bit for bit
+    against the same GEMM on rows copied in advance."""
+    if dtype == "f32" and pairing != N.GEMM_SINGLE:
+        pytest.skip("fp32 layers run on the CUDA cores; pairing does not apply")
+    G = len(offs) - 1
+    rows = int(offs[-1])
+    rows_cap = rows + 32
+    Kd, Nn = 192, 512
+    cfg = N.make_config(T, Kd, max(G, K), K, Nn, dtype, -1)  # K <= E; G groups are passed
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    hdt = torch.float16 if dtype == "bf16" else torch.float32
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    x = _gen((T, Kd), 1.0, 21, tdt)
+    w1 = _gen((G, Nn, Kd), Kd ** -0.5, 22, tdt)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(23)
+    src = torch.randint(0, T * K, (rows_cap,), generator=g, device="cuda", dtype=torch.int32)
+    off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
+    h = torch.full((rows_cap, Nn), 7.0, dtype=hdt, device="cuda")
+    N.expert_up_gather(cfg, x, src, off_t, G, rows_cap, w1, h, ws)
+    assert N.sync_status(ws) == 0
+    xp = x[(src.long() // K)].contiguous()   # the same rows, copied (test input only)
+    h2 = torch.full((rows_cap, Nn), 7.0, dtype=hdt, device="cuda")
+    N.expert_up(cfg, xp, off_t, G, rows_cap, w1, h2, ws)
+    assert N.sync_status(ws) == 0
+    assert torch.equal(h[:rows], h2[:rows])
+    hn, xn, wn, sn = h.float().cpu().numpy(), to_np(x), to_np(w1), src.cpu().numpy()
+    for gi in range(G):
+        lo, hi = int(offs[gi]), int(offs[gi + 1])
+        if hi > lo:
+            ref = O.gelu(O.linear(xn[sn[lo:hi] // K], wn[gi]))
+            if dtype == "bf16":
+                assert_rounded_to(hn[lo:hi], ref, "f16")
+            else:
+                assert rel_rms_err(hn[lo:hi], ref) <= 1e-4
+    assert (hn[rows:] == 7.0).all()
+
+
+def test_expert_up_gather_bad_index_reported():
+    T, K, G, Kd, Nn = 64, 2, 1, 64, 256
+    cfg = N.make_config(T, Kd, K, K, Nn, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    x = _gen((T, Kd), 1.0, 31, torch.bfloat16)
+    w1 = _gen((G, Nn, Kd), Kd ** -0.5, 32, torch.bfloat16)
+    src = torch.arange(100, dtype=torch.int32, device="cuda")
+    src[7] = T * K + 5                       # token T + 2: out of range
+    off_t = torch.tensor([0, 100], dtype=torch.int32, device="cuda")
+    h = torch.empty((100, Nn), dtype=torch.float16, device="cuda")
+    N.expert_up_gather(cfg, x, src, off_t, G, 100, w1, h, ws)
+    assert N.sync_status(ws) == 5  # MOE_ERR_DEVICE

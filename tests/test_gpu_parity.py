@@ -157,6 +157,24 @@ def test_adjust_selection_bias_matches_oracle():
         N.adjust_select_bias(cfg, counts, bias, -1.0)
 
 
+@pytest.mark.parametrize("T,E,K", [(4096, 8, 2), (8192, 256, 8), (16384, 128, 8), (37, 5, 5),
+                                   (1, 1, 1)])
+def test_aux_loss_grad(T, E, K):
+    """Backward of the aux loss against the oracle's fp64 gradient.  Every entry is
+    (alpha/T) p (f_j - sum_i f_i p_i) with p, f <= 1, computed in fp32: the bound is
+    1e-5 of alpha/T (the gradient itself vanishes when every expert is chosen equally)."""
+    L32 = make_logits(T, E, seed=T + 3 * E).numpy()
+    g = _routing_only(T, E, K, -1, L32)
+    cfg = N.make_config(T, 8, E, K, 8, "bf16", -1, False, 0.01)
+    logits = torch.from_numpy(L32).cuda()
+    f = torch.from_numpy(g["f"]).cuda()
+    grad = torch.full((T, E), 7.0, dtype=torch.float32, device="cuda")
+    N.aux_loss_grad(cfg, logits, f, grad)
+    torch.cuda.synchronize()
+    ref = O.aux_loss_grad_logits(L32, O.top_k(L32, K), 0.01)
+    assert np.max(np.abs(grad.cpu().numpy() - ref)) <= 1e-5 * 0.01 / T
+
+
 def test_scan_spans_many_blocks_all_one_expert():
     """Every assignment to one expert (collapsed router): the look-back carries one
     expert's running count across all scan blocks."""
@@ -211,9 +229,9 @@ def test_out_of_range_expert_id_reported():
 
 
 # ------------------------------------------------------------------ whole layer
-def _layer_case(wl: Workload, seed=0, logits_from_oracle=False, renorm=False):
+def _layer_case(wl: Workload, seed=0, logits_from_oracle=False, renorm=False, fused=True):
     inp = make_inputs(wl, "cuda", seed=seed)
-    layer = MoELayer.from_workload(wl, inp, renormalize=renorm)
+    layer = MoELayer.from_workload(wl, inp, renormalize=renorm, fused_dispatch=fused)
     x_np = to_np(inp["x"])
     b_np = None if inp["b_r"] is None else to_np(inp["b_r"])
     _, L32 = O.router_logits(x_np, to_np(inp["w_r"]), b_np)
@@ -240,9 +258,10 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_dispatch", "copy_dispatch"])
 @pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
-def test_layer_end_to_end_small(wl):
-    layer, ref, L32, C = _layer_case(wl)
+def test_layer_end_to_end_small(wl, fused):
+    layer, ref, L32, C = _layer_case(wl, fused=fused)
     # router logits themselves
     Lg = to_np(layer.logits)
     assert np.max(np.abs(Lg - L32) / (1 + np.abs(L32))) <= (1e-5 if wl.dtype == "bf16" else 1e-5)
@@ -255,17 +274,20 @@ def test_layer_end_to_end_small(wl):
     assert np.array_equal(to_np(layer.ids)[keep], ref["ids"][keep])
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_dispatch", "copy_dispatch"])
 @pytest.mark.parametrize("wl", SMALL[:6], ids=[w.name for w in SMALL[:6]])
-def test_layer_stages_with_oracle_logits(wl):
+def test_layer_stages_with_oracle_logits(wl, fused):
     """Fed the oracle's logits, every stage matches: routing bit-exact, packed rows
-    exact, h and y_perm within tolerance, combine within tolerance, aux stats."""
-    layer, ref, L32, C = _layer_case(wl, logits_from_oracle=True)
+    exact (copied dispatch), h and y_perm within tolerance, combine within tolerance,
+    aux stats."""
+    layer, ref, L32, C = _layer_case(wl, logits_from_oracle=True, fused=fused)
     R = ref["R"]
     assert np.array_equal(to_np(layer.ids), ref["ids"])
     assert np.array_equal(to_np(layer.offsets), ref["offsets"])
     assert np.array_equal(to_np(layer.slot), ref["slot"].reshape(wl.T, wl.K))
     assert np.array_equal(to_np(layer.src)[:R], ref["src"])
-    assert np.array_equal(to_np(layer.x_perm)[:R], ref["x_perm"])
+    if not fused:
+        assert np.array_equal(to_np(layer.x_perm)[:R], ref["x_perm"])
     tol = TOL[wl.dtype]
     hdt = "f16" if wl.dtype == "bf16" else "f32"
     assert_rounded_to(to_np(layer.h)[:R], ref["h"], hdt)

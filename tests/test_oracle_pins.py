@@ -462,3 +462,123 @@ def test_capacity_counting_assignments_balanced_load_never_drops():
     assert C == 16 and plan["R"] == T * K and (plan["slot"] >= 0).all()
     # the capacity as printed (tokens) drops K-1 of every K assignments here
     assert O.dispatch_plan(ids, E, O.capacity(T, E, 1.0))["R"] == E * (T // E)
+
+
+# ---------------------------------------------------------------- aux-loss backward
+def _l_aux_full(L, K, alpha):
+    """L_aux recomputed from scratch (routing included) for finite differences."""
+    L32 = np.asarray(L, dtype=np.float64)
+    z = L32 - L32.max(axis=1, keepdims=True)
+    p = np.exp(z) / np.exp(z).sum(axis=1, keepdims=True)
+    ids = np.argsort(-L32, axis=1, kind="stable")[:, :K]
+    T, E = L32.shape
+    f = np.bincount(ids.reshape(-1), minlength=E) / (T * K)
+    return alpha * float(np.sum(f * p.mean(axis=0)))
+
+
+@pytest.mark.parametrize("seed,T,E,K", [(0, 6, 5, 2), (1, 4, 8, 1), (2, 9, 3, 3)])
+def test_aux_grad_matches_finite_differences(seed, T, E, K):
+    """Central differences of the whole L_aux (top-K counts recomputed) equal the
+    analytic gradient: steps far smaller than every logit gap cross no tie."""
+    rng = np.random.default_rng(seed)
+    L = rng.standard_normal((T, E))
+    ids = O.top_k(L.astype(np.float32), K)
+    g = O.aux_loss_grad_logits(L, ids, 0.01)
+    srt = np.sort(L, axis=1)
+    h = 1e-3 * np.min(np.diff(srt, axis=1))
+    num = np.zeros_like(L)
+    for t in range(T):
+        for j in range(E):
+            Lp, Lm = L.copy(), L.copy()
+            Lp[t, j] += h
+            Lm[t, j] -= h
+            num[t, j] = (_l_aux_full(Lp, K, 0.01) - _l_aux_full(Lm, K, 0.01)) / (2 * h)
+    assert np.allclose(g, num, rtol=1e-5, atol=1e-12)
+
+
+def test_aux_grad_rows_sum_to_zero_and_balanced_is_zero():
+    """Softmax is shift-invariant, so each token's gradient sums to zero; with f uniform
+    (balanced routing) the gradient vanishes."""
+    rng = np.random.default_rng(4)
+    L = rng.standard_normal((12, 6))
+    g = O.aux_loss_grad_logits(L, O.top_k(L.astype(np.float32), 2), 0.01)
+    assert np.allclose(g.sum(axis=1), 0.0, atol=1e-18)
+    ids = (np.arange(24) % 6).reshape(12, 2)
+    assert np.allclose(O.aux_loss_grad_logits(L, ids, 0.01), 0.0, atol=1e-18)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) quantisation
+def _e4m3_table():
+    """Every finite E4M3 value, enumerated from the bit fields (bias 7; exponent field 0
+    is subnormal; S.1111.111 is NaN and left out)."""
+    vals = set()
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue
+            mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+            vals.add(mag)
+            vals.add(-mag)
+    return np.array(sorted(vals))
+
+
+def test_e4m3_values_are_the_format():
+    t = _e4m3_table()
+    assert t.max() == 448.0 and np.min(t[t > 0]) == 2.0 ** -9
+    assert np.array_equal(O.round_e4m3(t), t)
+
+
+def test_e4m3_rounding_nearest_even_and_saturating():
+    t = _e4m3_table()
+    rng = np.random.default_rng(0)
+    v = np.concatenate([rng.uniform(-460, 460, 4000), rng.uniform(-0.05, 0.05, 4000),
+                        (t[1:] + t[:-1]) / 2])                  # exact midpoints
+    q = O.round_e4m3(v)
+    for x, y in zip(v, q):
+        if abs(x) >= 448:
+            assert y == np.sign(x) * 448
+            continue
+        d = np.abs(t - x)
+        best = t[d == d.min()]
+        if best.size == 1:
+            assert y == best[0]
+        else:   # tie: the candidate whose 3-bit mantissa is even
+            def even(c):
+                a = abs(c)
+                if a < 2.0 ** -6:
+                    return int(round(a / 2.0 ** -9)) % 2 == 0
+                e = np.floor(np.log2(a))
+                return int(round(a / 2.0 ** (e - 3))) % 2 == 0
+            assert y in best and even(y)
+
+
+def test_quantize_rows_reconstructs_within_half_step():
+    rng = np.random.default_rng(1)
+    m = (rng.standard_normal((20, 64)) * rng.uniform(0.01, 50, (20, 1))).astype(np.float32)
+    m[3] = 0.0
+    codes, scale = O.quantize_rows_e4m3(m)
+    assert scale[3] == 0 and (codes[3] == 0).all()
+    assert (np.abs(codes).max(axis=1)[np.arange(20) != 3] == 448.0).all()  # amax maps to 448
+    rec = codes * scale[:, None]
+    # relative spacing of E4M3 normals is 2^-3: rounding error <= 2^-4 of |x| (plus the
+    # subnormal spacing 2^-10 * scale for tiny entries)
+    assert (np.abs(rec - m) <= 2.0 ** -4 * np.abs(m) + 2.0 ** -10 * scale[:, None] * 1.0001).all()
+
+
+def test_e4m3_expert_ffn_reduces_to_exact_on_representable_inputs():
+    """When every row's entries are E4M3 values times a power of two whose row maximum is
+    448 times it, quantisation is exact and the FP8 expert equals the fp64 expert up to
+    the fp16 store and quantisation of h (checked by applying both to the exact h)."""
+    rng = np.random.default_rng(7)
+    t = _e4m3_table()
+    def rep(shape):
+        m = rng.choice(t[np.abs(t) <= 64], size=shape)
+        m[:, 0] = 448.0
+        return (m * 2.0 ** -7).astype(np.float32)
+    x, w1, w2 = rep((6, 16)), rep((8, 16)), rep((16, 8))
+    y8, h8 = O.expert_ffn_e4m3(x, w1, w2)
+    h = O.gelu(O.linear(x, w1))
+    assert np.allclose(h8, h, rtol=1e-15, atol=0)
+    hq, sh = O.quantize_rows_e4m3(h.astype(np.float16).astype(np.float32))
+    y = (hq * sh[:, None].astype(np.float64)) @ O.widen(w2).T
+    assert np.allclose(y8, y, rtol=1e-12, atol=1e-300)
