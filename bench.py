@@ -286,10 +286,10 @@ def run_ours(args, wl):
     dom = "expert_up" if avg["expert_up"] >= avg["expert_down"] else "expert_down"
     dom_flops = flops_up if dom == "expert_up" else flops_down
     achieved_tf = dom_flops / (avg[dom] * 1e-3) / 1e12
-    kernel_src = "routing_dispatch_expert_04_b300/csrc/gemm_tc.cu"
-    if not os.path.exists(os.path.join(ROOT, kernel_src)):
-        kernel_src = "routing_dispatch_expert_04_b300/csrc/gemm_simt.cu"
-    traffic = recorded_traffic(f"{dom}:{wl.name}", source_digest(kernel_src))
+    kernel_srcs = ["routing_dispatch_expert_04_b300/csrc/" + f
+                   for f in ("gemm_tc.cu", "gemm_tc2.cu", "tc_common.cuh", "tc_ptx.cuh")]
+    traffic = recorded_traffic(f"{dom}:{wl.name}:{args.experts}:{args.gemm}",
+                               source_digest(*kernel_srcs))
     if args.experts == "e4m3":
         # FP8 contraction: the measured bf16 peak times the nominal fp8/bf16 ratio (2)
         peak_tf, peak_src = 2.0 * pk["bf16_tflops"], f"{pk['source']} bf16 dense (burst) x 2 (nominal e4m3/bf16)"
@@ -309,7 +309,7 @@ def run_ours(args, wl):
         "ms_median": {n: round(v, 4) for n, v in med.items()},
         "expert_up_tflops": round(flops_up / (avg["expert_up"] * 1e-3) / 1e12, 2),
         "expert_down_tflops": round(flops_down / (avg["expert_down"] * 1e-3) / 1e12, 2),
-        "grouped_gemm_frac_of_bf16_peak": round(
+        "grouped_gemm_frac_of_peak": round(
             (flops_up + flops_down) / ((avg["expert_up"] + avg["expert_down"]) * 1e-3) / 1e12
             / peak_tf, 4),
         "dispatch_gbs": round(gbs(bytes_dispatch, avg["dispatch"]), 1),

@@ -25,7 +25,7 @@
 //
 // dispatch_kernel -- one warp per token: turns positions into packed rows (slot, src)
 // and copies the token's row once from HBM into each of its kept packed rows with
-// 16-byte loads and stores.
+// 16-byte loads and stores (a token with no kept row is not read).
 #include "common.cuh"
 
 namespace moe {
@@ -195,8 +195,10 @@ dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids,
       if (s >= 0) src[s] = (int32_t)a;
       s_slot[warp][lane] = s;
     }
+    // a token whose assignments were all dropped is not read at all
+    const bool kept_any = __any_sync(0xffffffffu, lane < K && s_slot[warp][lane < K ? lane : 0] >= 0);
     __syncwarp();
-    if (xp != nullptr) {
+    if (xp != nullptr && kept_any) {
       const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
       int j = lane;
       for (; j + 96 < nvec; j += 128) {
