@@ -218,7 +218,7 @@ def run_ours(args, wl):
     pk = peaks()
 
     N.set_gemm_pairing({"auto": N.GEMM_AUTO, "single": N.GEMM_SINGLE, "pair": N.GEMM_PAIR,
-                        "split": N.GEMM_SPLIT}[args.gemm])
+                        "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T}[args.gemm])
     inp = make_inputs(wl, dev, seed=0)
     layer = MoELayer.from_workload(wl, inp, device=dev, fused_dispatch=args.dispatch == "fused",
                                    experts=args.experts)
@@ -425,10 +425,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral", choices=sorted(WORKLOADS))
-    ap.add_argument("--gemm", choices=["auto", "single", "pair", "split"], default="auto",
+    ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t"], default="auto",
                     help="expert GEMM kernels: one CTA per 128-row tile, CTA pairs per "
                          "256-row tile, pairs for whole 256-row tiles + one CTA for the "
-                         "rest, or the library's choice")
+                         "rest, pairs with the tokens on the MMA's N side, or the "
+                         "library's choice")
     ap.add_argument("--dispatch", choices=["fused", "copy"], default="copy",
                     help="fused: the first expert GEMM gathers its rows from x while loading "
                          "them; copy: the dispatch step copies them into a packed buffer")

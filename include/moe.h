@@ -288,16 +288,22 @@ moe_status_t moe_sync_status(void* ws, void* stream);
  *                   to a multiple of 256 rows;
  *   MOE_GEMM_SPLIT  pairs for each group's whole 256-row tiles, then one CTA per 128-row
  *                   tile for the remaining rows (two launches on the stream);
+ *   MOE_GEMM_PAIR_T two CTAs per tile computing the transpose: 256 weight rows (output
+ *                   columns) on the MMA's M side and up to 256 of a group's rows on its
+ *                   N side, sized to the group (rounded up to 32), so no group is padded
+ *                   to 256 rows; row-gathered and E4M3 calls use the other kernels;
  *   MOE_GEMM_AUTO   (default) pairs when the 256-row padding is at most 5% of the rows
- *                   (judged from the capacity; the output width must be a multiple of
- *                   256), one CTA otherwise.
+ *                   (judged from the capacity), transposed pairs when the groups have
+ *                   no capacity bound, one CTA otherwise (pairs of either kind need the
+ *                   output width to be a multiple of 256).
  * Every choice sums the same products in the same order, so results are identical.
  * Returns MOE_ERR_INVALID for any other value.  Calls already enqueued are unaffected. */
 typedef enum {
   MOE_GEMM_AUTO = 0,
   MOE_GEMM_SINGLE = 1,
   MOE_GEMM_PAIR = 2,
-  MOE_GEMM_SPLIT = 3
+  MOE_GEMM_SPLIT = 3,
+  MOE_GEMM_PAIR_T = 4
 } moe_gemm_pairing_t;
 moe_status_t moe_set_gemm_pairing(int32_t mode);
 

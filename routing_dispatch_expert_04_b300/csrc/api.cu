@@ -437,7 +437,7 @@ uint64_t moe_launch_count(void) { return g_launches.load(); }
 
 moe_status_t moe_set_gemm_pairing(int32_t mode) {
   if (mode != MOE_GEMM_AUTO && mode != MOE_GEMM_SINGLE && mode != MOE_GEMM_PAIR &&
-      mode != MOE_GEMM_SPLIT)
+      mode != MOE_GEMM_SPLIT && mode != MOE_GEMM_PAIR_T)
     return MOE_ERR_INVALID;
   g_gemm_pairing.store(mode);
   return MOE_OK;

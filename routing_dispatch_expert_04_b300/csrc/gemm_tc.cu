@@ -345,14 +345,27 @@ cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const 
 // 256 rows, and the split's second launch waits for the first one's tail.  Measured on
 // the layer shapes (B300), pairs win only where that padding is small, so MOE_GEMM_AUTO
 // takes pairs when the padding is at most 5% (judged from the per-group row bound, when
-// known, and with N filling 256-wide tiles) and one CTA otherwise.
-enum { PLAN_SINGLE = 0, PLAN_PAIR = 1, PLAN_SPLIT = 2 };
+// known, and with N filling 256-wide tiles) and one CTA otherwise; groups of unknown
+// size (no capacity) go to the transposed pairs, which size the token side of each tile
+// to the group (measured fastest on the DeepSeek-V3-shaped layer).
+enum { PLAN_SINGLE = 0, PLAN_PAIR = 1, PLAN_SPLIT = 2, PLAN_PAIR_T = 3 };
+
+cudaError_t launch_tc2t_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
+                           int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                           cudaStream_t st);
+cudaError_t launch_tc2t_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
+                             int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                             cudaStream_t st);
 
 static int gemm_plan(int mode, int64_t rows_cap, int G, int64_t cap_per_group, int N) {
   if (mode == MOE_GEMM_SINGLE) return PLAN_SINGLE;
   if (mode == MOE_GEMM_PAIR) return PLAN_PAIR;
   if (mode == MOE_GEMM_SPLIT) return PLAN_SPLIT;
-  if (N % 256 != 0 || cap_per_group <= 0) return PLAN_SINGLE;
+  if (mode == MOE_GEMM_PAIR_T) return PLAN_PAIR_T;
+  if (N % 256 != 0) return PLAN_SINGLE;
+  // groups of unknown size (no capacity): the transposed pairs size each token tile to
+  // the group, so ragged groups pad to 32 rows, not 128 or 256
+  if (cap_per_group <= 0) return PLAN_PAIR_T;
   const int64_t per = cap_per_group < rows_cap ? cap_per_group : rows_cap;
   const int64_t rows128 = (int64_t)G * ((per + 127) / 128) * 128;
   const int64_t rows256 = (int64_t)G * ((per + 255) / 256) * 256;
@@ -374,8 +387,11 @@ cudaError_t launch_tc_up(const void* a_in, const int32_t* gather_src, int gather
                          int64_t gather_rows, const void* w1, void* h, const int32_t* offsets,
                          int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
                          int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st) {
-  const int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
+  int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
   const bool gather = gather_src != nullptr;
+  if (plan == PLAN_PAIR_T && gather) plan = PLAN_PAIR;  // row gathers need rows on the M side
+  if (plan == PLAN_PAIR_T)
+    return launch_tc2t_up(a_in, w1, h, offsets, G, N, Kd, rows_cap, hdr, num_sms, st);
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            TC_ROWS_ALL, gather_src, gather_k, gather_rows};
   if (plan == PLAN_SINGLE)
@@ -397,6 +413,8 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
                            int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
                            int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st) {
   const int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_PAIR_T)
+    return launch_tc2t_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, hdr, num_sms, st);
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            TC_ROWS_ALL};
   if (plan == PLAN_SINGLE)

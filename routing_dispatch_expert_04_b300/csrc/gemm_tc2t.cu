@@ -1,0 +1,349 @@
+// Grouped GEMM on CTA pairs with the tokens on the MMA's N side, sm_103a.
+//
+// Same computation as the other expert-GEMM kernels -- the expert FFN of "Expert
+// Parallelism (MoE)", "MoE Layer Structure", for all experts in one launch:
+//   C[r, n] = epi( sum_k A[r, k] * B[g*N + n, k] ),  r in [offsets[g], offsets[g+1]) --
+// computed as its transpose, C^T = B . A^T, on CTA pairs (tcgen05.mma.cta_group::2):
+//   - the MMA's M side (256 rows, 128 per CTA) is a tile of 256 weight rows (output
+//     columns n), which always fills it when N is a multiple of 256;
+//   - the N side is a tile of up to 256 of the group's rows (tokens), each CTA staging
+//     half of them; the instruction's N is the tile's row count rounded up to 32, so a
+//     group of 640 rows runs as 256 + 256 + 128 columns instead of three 256-row tiles;
+//   - each CTA's TMEM holds its 128 weight rows x the tile's tokens, and the epilogue
+//     writes the transpose: lane l of a warp owns output column n and stores the 32
+//     tokens of a chunk one by one, so a warp store covers 32 consecutive columns of one
+//     output row (64 B of fp16, 128 B of fp32).
+// Pipeline, barriers, bounded waits and teardown as in gemm_tc2.cu: warp 0 TMA producer,
+// warp 1 TMEM owner + MMA issuer (even CTA), warps 2..5 epilogue; both CTAs' copies
+// signal the even CTA's "full" barrier, its commits arrive on both CTAs' "empty" and
+// "accumulator full" barriers, both CTAs' epilogues arrive on its "accumulator empty".
+// Tiles are (group, weight tile, token tile) with token tiles fastest, so the pairs that
+// run together share the weight tile through L2.
+#include "tc_common.cuh"
+
+namespace moe {
+using namespace tc;
+
+constexpr int T2T_TILE = 256;    // weight rows per tile (M) and most tokens per tile (N)
+constexpr int T2T_CTA_ROWS = 128;
+
+template <int STAGES>
+struct Tc2tLayout {
+  static constexpr int W_BYTES = T2T_CTA_ROWS * TC_ROW_BYTES;  // this CTA's weight rows
+  static constexpr int X_BYTES = T2T_CTA_ROWS * TC_ROW_BYTES;  // this CTA's token rows
+  static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+  static constexpr int X_OFF = STAGES * W_BYTES;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NBAR = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], done
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int GRP_OFF = MISC_OFF + 16;
+  static constexpr int TOTAL = GRP_OFF + (int)sizeof(GroupTable);
+  static constexpr int ALLOC = TOTAL + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * T2T_TILE;
+};
+
+constexpr uint64_t T2T_ABORT_SETTLE_NS = 200000ull;
+
+// Group table for this kernel: mt[g] = token tiles of group g; tiles per group =
+// mt[g] * weight tiles.
+__device__ __forceinline__ void build_token_tiles(GroupTable* tab, const TcArgs& args, int w_tiles,
+                                                  int lane) {
+  int carry = 0;
+  for (int base = 0; base < args.G; base += 32) {
+    const int g = base + lane;
+    int lo = 0, hi = 0, nt = 0;
+    if (g < args.G) {
+      lo = args.offsets[g];
+      hi = args.offsets[g + 1];
+      if (hi > args.rows_cap) {
+        raise_error(args.hdr, DEV_ERR_OVERFLOW);
+        hi = (int)args.rows_cap;
+      }
+      if (lo < 0) lo = 0;
+      if (lo > hi) lo = hi;
+      nt = (hi - lo + T2T_TILE - 1) / T2T_TILE;
+      tab->lo[g] = lo;
+      tab->hi[g] = hi;
+      tab->mt[g] = nt;
+    }
+    int v = nt * w_tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (g < args.G) tab->tpre[g + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+  if (lane == 0) tab->tpre[0] = 0;
+}
+
+struct TTile {
+  int g;
+  int tok0;   // first token row of the tile
+  int ntok;   // token rows in the tile (<= 256)
+  int ninst;  // instruction N: ntok rounded up to 32
+  int w0;     // first weight row (output column) of the tile within the group
+};
+
+__device__ __forceinline__ TTile decode_ttile(int t, int G, const GroupTable* tab) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tab->tpre[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int g = lo;
+  const int local = t - tab->tpre[g];
+  const int nt = tab->mt[g];
+  TTile ti;
+  ti.g = g;
+  ti.tok0 = tab->lo[g] + (local % nt) * T2T_TILE;
+  ti.ntok = min(T2T_TILE, tab->hi[g] - ti.tok0);
+  ti.ninst = (ti.ntok + 31) & ~31;
+  ti.w0 = (local / nt) * T2T_TILE;
+  return ti;
+}
+
+// Epilogue of the transposed tile: r[j] = C[tok0 + c0 + j, col] for j < 32.
+template <int EPI>
+__device__ __forceinline__ bool epilogue_chunk_t(const uint32_t (&r)[32], int col, int tok_first,
+                                                 int tok_end, const TcArgs& args) {
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int tok = tok_first + j;
+    if (tok >= tok_end) break;
+    const float v = __uint_as_float(r[j]);
+    if (EPI == TC_EPI_GELU_F16) {
+      const float a = gelu_exact(v);
+      bad |= !(fabsf(a) <= 65504.f);
+      ((__half*)args.out)[(size_t)tok * args.ldo + col] = __float2half_rn(a);
+    } else {
+      ((float*)args.out)[(size_t)tok * args.ldo + col] = v;
+    }
+  }
+  return bad;
+}
+
+template <int STAGES, int EPI, int KIND>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                         const __grid_constant__ CUtensorMap tmap_w, const TcArgs args) {
+  using Lay = Tc2tLayout<STAGES>;
+  static_assert(KIND != OP_E4M3, "E4M3 operands run on the one-CTA kernel");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + Lay::BAR_OFF);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* done = bars + 2 * STAGES + 4;
+  uint32_t* s_tmem = (uint32_t*)(smem + Lay::MISC_OFF);
+  volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
+  GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int G = args.G;
+  const int w_tiles = (args.N + T2T_TILE - 1) / T2T_TILE;
+  constexpr int BKE = OpKind<KIND>::BK;
+  const int nkb = (args.Kd + BKE - 1) / BKE;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 8);
+    }
+    mbar_init(done, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(&tmap_w);
+  }
+  if (warp == 0) {
+    build_token_tiles(tab, args, w_tiles, lane);
+  } else if (warp == 1) {
+    tmem_alloc_pair(s_tmem, Lay::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total = tab->tpre[G];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = cluster; t < total && ok; t += n_clusters) {
+        const TTile ti = decode_ttile(t, G, tab);
+        const int wrow = ti.g * args.N + ti.w0 + (int)rank * T2T_CTA_ROWS;
+        const int xrow = ti.tok0 + (int)rank * (ti.ninst >> 1);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sw = smem + s * Lay::W_BYTES;
+          uint8_t* sx = smem + Lay::X_OFF + s * Lay::X_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Lay::STAGE_BYTES);
+          const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's full[s]
+          tma_load_2d_pair(sw, &tmap_w, fb, kb * BKE, wrow);
+          tma_load_2d_pair(sx, &tmap_x, fb, kb * BKE, xrow);
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        if (rank == 0) {
+          for (int i = 0; i < STAGES && i < issued; ++i) {
+            if (--s < 0) {
+              s = STAGES - 1;
+              ph ^= 1u;
+            }
+            drain_wait(&full[s], ph);
+          }
+        } else {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < T2T_ABORT_SETTLE_NS) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      const uint32_t idesc0 =
+          KIND == OP_BF16 ? idesc_bf16_f32(T2T_TILE, 0) : idesc_fmt0_f32(T2T_TILE, 0);
+      int s = 0;
+      uint32_t ph = 0, acc = 0, aph = 0;
+      bool ok = true;
+      for (int t = cluster; t < total && ok; t += n_clusters) {
+        const TTile ti = decode_ttile(t, G, tab);
+        const uint32_t idesc = idesc0 | ((uint32_t)(ti.ninst >> 3) << 17);
+        if (!wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * T2T_TILE;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_phase(&full[s], ph, s_abort, args.hdr)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w_addr = smem_u32(smem + s * Lay::W_BYTES);
+          const uint32_t x_addr = smem_u32(smem + Lay::X_OFF + s * Lay::X_BYTES);
+#pragma unroll
+          for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
+            mma_f16_pair(d_tmem, sdesc_sw128(w_addr + k * 32), sdesc_sw128(x_addr + k * 32), idesc,
+                         (kb != 0 || k != 0) ? 1u : 0u);
+          }
+          mma_commit_pair_mc(&empty[s], (uint16_t)3);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(&tfull[acc], (uint16_t)3);
+        acc ^= 1u;
+        if (acc == 0) aph ^= 1u;
+      }
+      mma_commit_pair_local(done);
+      drain_wait(done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int wl = (int)rank * T2T_CTA_ROWS + q * 32 + lane;  // weight row within the tile
+    uint32_t acc = 0, aph = 0;
+    for (int t = cluster; t < total; t += n_clusters) {
+      const TTile ti = decode_ttile(t, G, tab);
+      if (!wait_phase(&tfull[acc], aph, s_abort, args.hdr)) break;
+      tc_fence_after();
+      const int col = ti.w0 + wl;
+      const bool valid = col < args.N;
+      const int tok_end = ti.tok0 + ti.ntok;
+#pragma unroll 1
+      for (int c = 0; c < ti.ninst; c += 32) {  // warp-uniform
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * T2T_TILE + c, r);
+        tmem_ld_wait();
+        if (!valid) continue;
+        if (epilogue_chunk_t<EPI>(r, col, ti.tok0 + c, tok_end, args))
+          raise_error(args.hdr, DEV_ERR_RANGE);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      acc ^= 1u;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, Lay::TMEM_COLS);
+}
+
+template <int STAGES, int EPI, int KIND>
+static cudaError_t launch_tc2t(const void* X, const void* W, const TcArgs& a, int num_sms,
+                               cudaStream_t st) {
+  using Lay = Tc2tLayout<STAGES>;
+  static bool attr_set = false;
+  auto kern = tc2t_grouped_gemm_kernel<STAGES, EPI, KIND>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap mx, mw;
+  const int64_t x_rows = a.rows_cap > 0 ? a.rows_cap : 1;
+  if (!tc_make_map(&mx, X, KIND, (uint64_t)a.Kd, (uint64_t)x_rows, T2T_CTA_ROWS))
+    return cudaErrorInvalidValue;
+  if (!tc_make_map(&mw, W, KIND, (uint64_t)a.Kd, (uint64_t)a.G * a.N, T2T_CTA_ROWS))
+    return cudaErrorInvalidValue;
+  const int64_t w_tiles = (a.N + T2T_TILE - 1) / T2T_TILE;
+  const int64_t t_bound = (a.rows_cap + T2T_TILE - 1) / T2T_TILE + a.G;
+  int64_t clusters = w_tiles * t_bound;
+  if (clusters > num_sms / 2) clusters = num_sms / 2;
+  if (clusters < 1) clusters = 1;
+  kern<<<(unsigned)(2 * clusters), TC_THREADS, Lay::ALLOC, st>>>(mx, mw, a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// First expert Linear, tokens on the N side: h = GELU(x_perm . W1[g]^T), fp16 out.
+cudaError_t launch_tc2t_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
+                           int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                           cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, 0, 0, TC_ROWS_ALL};
+  return launch_tc2t<6, TC_EPI_GELU_F16, OP_BF16>(x_perm, w1, a, num_sms, st);
+}
+
+// Second expert Linear, tokens on the N side: y_perm = h . W2[g]^T, fp32 out.
+cudaError_t launch_tc2t_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
+                             int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                             cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, 0, 0, TC_ROWS_ALL};
+  return launch_tc2t<6, TC_EPI_F32, OP_F16>(h, w2h, a, num_sms, st);
+}
+
+}  // namespace moe

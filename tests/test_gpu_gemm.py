@@ -30,9 +30,11 @@ def _gen(shape, std, seed, dtype):
     return (torch.randn(*shape, generator=g, device="cuda") * std).to(dtype)
 
 
-@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT], ids=["single", "pair", "split"])
+@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T],
+                ids=["single", "pair", "split", "pair_t"])
 def pairing(request):
-    """Run the case on the one-CTA kernel, the CTA-pair kernel and the split of the two."""
+    """Run the case on the one-CTA kernel, the CTA-pair kernel, the split of the two and
+    the transposed pair kernel."""
     N.set_gemm_pairing(request.param)
     yield request.param
     N.set_gemm_pairing(N.GEMM_AUTO)
@@ -139,7 +141,7 @@ def test_single_and_pair_kernels_agree_bitwise(fn):
     ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
     off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
     outs = []
-    for mode in (N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT):
+    for mode in (N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T):
         N.set_gemm_pairing(mode)
         try:
             if fn == "up":
@@ -158,6 +160,7 @@ def test_single_and_pair_kernels_agree_bitwise(fn):
         outs.append(out.cpu())
     assert torch.equal(outs[0], outs[1])
     assert torch.equal(outs[0], outs[2])
+    assert torch.equal(outs[0], outs[3])
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -167,7 +170,7 @@ def test_expert_up_gather(offs, T, K, dtype, pairing):
     """Dispatch fused into the first expert Linear: packed row r is gathered from token
     row src[r] // K of x while the tile loads.  Against the oracle, and bit for bit
     against the same GEMM on rows copied in advance."""
-    if dtype == "f32" and pairing != N.GEMM_SINGLE:
+    if dtype == "f32" and pairing not in (N.GEMM_SINGLE,):
         pytest.skip("fp32 layers run on the CUDA cores; pairing does not apply")
     G = len(offs) - 1
     rows = int(offs[-1])
