@@ -31,13 +31,22 @@ constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_IPT = 16;
 constexpr int SCAN_ITEMS = SCAN_THREADS * SCAN_IPT;  // assignments per scan block
 constexpr int ROUTE_WARPS = 8;
-constexpr int ROUTE_TPW = 1;                          // tokens per warp
-constexpr int ROUTE_TOKENS = ROUTE_WARPS * ROUTE_TPW; // tokens per route block
+
+// Tokens per warp of the softmax/top-K kernel: four (more loads in flight per warp)
+// when the batch has enough tokens to keep every SM busy with a quarter as many warps,
+// one otherwise (measured: 4 is faster at T >= 16384, 1 at T <= 8192).
+inline int route_tpw(int T) { return T >= 16384 ? 4 : 1; }
 
 struct WsLayout {
   size_t desc, pos, ppart, auxfp, lpart, total;
   int nblk_scan, nblk_route, router_splits;
 };
+
+// CTAs of the tensor-core router that share one SM: its E <= 64 variants stage in at
+// most 100 KB of shared memory and hold at most 128 TMEM columns, so two fit (measured
+// faster on the 64K-token layer); the wider variants take a whole SM (for E = 128, two
+// 3-stage CTAs per SM measured slower than one 6-stage CTA).
+inline int router_ctas_per_sm(int E) { return E <= 64 ? 2 : 1; }
 
 // K splits of the tensor-core router: enough CTAs to cover the SMs when T/128 row tiles
 // alone would not (planned for 148 SMs; a smaller GPU just runs more waves).  Every
@@ -60,7 +69,8 @@ inline WsLayout ws_layout(const moe_config& c) {
   WsLayout L;
   int64_t A = (int64_t)c.T * c.K;
   L.nblk_scan = (int)((A + SCAN_ITEMS - 1) / SCAN_ITEMS);
-  L.nblk_route = (int)(((int64_t)c.T + ROUTE_TOKENS - 1) / ROUTE_TOKENS);
+  const int route_tokens = ROUTE_WARPS * route_tpw(c.T);  // tokens per route block
+  L.nblk_route = (int)(((int64_t)c.T + route_tokens - 1) / route_tokens);
   size_t off = 256;
   L.desc = off;
   off = align_up(off + (size_t)L.nblk_scan * c.E * 8, 256);

@@ -274,13 +274,18 @@ bool tc_make_map(CUtensorMap* m, const void* base, int kind, uint64_t inner, uin
 
 template <int BN, int STAGES, int EPI, int KIND, bool GATHER = false>
 static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int num_sms,
-                             cudaStream_t st) {
+                             cudaStream_t st, int ctas_per_sm = 1) {
   using Lay = TcLayout<BN, STAGES>;
   static bool attr_set = false;
   auto kern = tc_grouped_gemm_kernel<BN, STAGES, EPI, KIND, GATHER>;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::ALLOC);
     if (e != cudaSuccess) return e;
+    if (ctas_per_sm > 1) {  // room for several CTAs' stages on one SM
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   CUtensorMap ma, mb;
@@ -292,7 +297,7 @@ static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int 
   const int64_t n_tiles = (a.N + BN - 1) / BN;
   const int64_t m_bound = (a.rows_cap + TC_BM - 1) / TC_BM + (a.offsets ? a.G : 0);
   int64_t grid = m_bound * n_tiles * a.ksplit;
-  if (grid > num_sms) grid = num_sms;
+  if (grid > (int64_t)num_sms * ctas_per_sm) grid = (int64_t)num_sms * ctas_per_sm;
   if (grid < 1) grid = 1;
   kern<<<(unsigned)grid, TC_THREADS, Lay::ALLOC, st>>>(ma, mb, a);
   count_launch();
@@ -464,9 +469,11 @@ cudaError_t launch_tc_router(const void* x, const void* w_r, const float* b_r, f
   const int ks = (nkb + kpb - 1) / kpb;
   TcArgs a{nullptr, 1, T, E, d, (int64_t)T, out, E, b_r, hdr, ks, kpb, (int64_t)T * E,
            TC_ROWS_ALL};
-  // the epilogue reads TMEM 32 columns at a time, so the narrowest tile is 32 wide
-  if (E <= 32) return launch_tc<32, 8, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st);
-  if (E <= 64) return launch_tc<64, 8, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st);
+  // the epilogue reads TMEM 32 columns at a time, so the narrowest tile is 32 wide; the
+  // E <= 64 variants keep their stages within 100 KB so that two CTAs share an SM
+  const int per_sm = router_ctas_per_sm(E);
+  if (E <= 32) return launch_tc<32, 4, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st, per_sm);
+  if (E <= 64) return launch_tc<64, 4, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st, per_sm);
   if (E <= 128) return launch_tc<128, 6, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st);
   return launch_tc<256, 4, TC_EPI_BIAS_F32, OP_BF16>(x, w_r, a, num_sms, st);
 }

@@ -8,7 +8,11 @@
 //     columns n), which always fills it when N is a multiple of 256;
 //   - the N side is a tile of up to 256 of the group's rows (tokens), each CTA staging
 //     half of them; the instruction's N is the tile's row count rounded up to 32, so a
-//     group of 640 rows runs as 256 + 256 + 128 columns instead of three 256-row tiles;
+//     group of 640 rows runs as 256 + 256 + 128 columns instead of three 256-row tiles
+//     (cutting a group into equal tiles, 224 + 224 + 192, measured no faster: the tensor
+//     pipe appears to spend a 256-column instruction's time on 192 or 224 columns);
+//     each CTA loads its half of the tile with the smallest of three boxes (128, 64 or
+//     32 rows) that covers it, so the bytes staged follow the tile;
 //   - each CTA's TMEM holds its 128 weight rows x the tile's tokens, and the epilogue
 //     writes the transpose: lane l of a warp owns output column n and stores the 32
 //     tokens of a chunk one by one, so a warp store covers 32 consecutive columns of one
@@ -84,6 +88,7 @@ struct TTile {
   int ntok;   // token rows in the tile (<= 256)
   int ninst;  // instruction N: ntok rounded up to 32
   int w0;     // first weight row (output column) of the tile within the group
+  int box;    // token box of each CTA: 0 (128 rows), 1 (64) or 2 (32) -- covers ninst/2
 };
 
 __device__ __forceinline__ TTile decode_ttile(int t, int G, const GroupTable* tab) {
@@ -102,6 +107,8 @@ __device__ __forceinline__ TTile decode_ttile(int t, int G, const GroupTable* ta
   ti.ntok = min(T2T_TILE, tab->hi[g] - ti.tok0);
   ti.ninst = (ti.ntok + 31) & ~31;
   ti.w0 = (local / nt) * T2T_TILE;
+  const int half = ti.ninst >> 1;
+  ti.box = half > 64 ? 0 : (half > 32 ? 1 : 2);
   return ti;
 }
 
@@ -128,7 +135,9 @@ __device__ __forceinline__ bool epilogue_chunk_t(const uint32_t (&r)[32], int co
 
 template <int STAGES, int EPI, int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
-tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
+                         const __grid_constant__ CUtensorMap tmap_x64,
+                         const __grid_constant__ CUtensorMap tmap_x32,
                          const __grid_constant__ CUtensorMap tmap_w, const TcArgs args) {
   using Lay = Tc2tLayout<STAGES>;
   static_assert(KIND != OP_E4M3, "E4M3 operands run on the one-CTA kernel");
@@ -164,7 +173,9 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
     mbar_init(done, 1);
     *s_abort = 0;
     fence_barrier_init();
-    tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(&tmap_x128);
+    tma_prefetch_desc(&tmap_x64);
+    tma_prefetch_desc(&tmap_x32);
     tma_prefetch_desc(&tmap_w);
   }
   if (warp == 0) {
@@ -190,6 +201,8 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
         const TTile ti = decode_ttile(t, G, tab);
         const int wrow = ti.g * args.N + ti.w0 + (int)rank * T2T_CTA_ROWS;
         const int xrow = ti.tok0 + (int)rank * (ti.ninst >> 1);
+        const CUtensorMap* xmap = ti.box == 0 ? &tmap_x128 : (ti.box == 1 ? &tmap_x64 : &tmap_x32);
+        const uint32_t stage_bytes = Lay::W_BYTES + ((uint32_t)T2T_CTA_ROWS >> ti.box) * TC_ROW_BYTES;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_phase(&empty[s], ph ^ 1u, s_abort, args.hdr)) {
             ok = false;
@@ -197,10 +210,10 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
           }
           uint8_t* sw = smem + s * Lay::W_BYTES;
           uint8_t* sx = smem + Lay::X_OFF + s * Lay::X_BYTES;
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Lay::STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * stage_bytes);
           const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);  // the even CTA's full[s]
           tma_load_2d_pair(sw, &tmap_w, fb, kb * BKE, wrow);
-          tma_load_2d_pair(sx, &tmap_x, fb, kb * BKE, xrow);
+          tma_load_2d_pair(sx, xmap, fb, kb * BKE, xrow);
           ++issued;
           if (++s == STAGES) {
             s = 0;
@@ -314,9 +327,11 @@ static cudaError_t launch_tc2t(const void* X, const void* W, const TcArgs& a, in
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap mx, mw;
+  CUtensorMap mx128, mx64, mx32, mw;
   const int64_t x_rows = a.rows_cap > 0 ? a.rows_cap : 1;
-  if (!tc_make_map(&mx, X, KIND, (uint64_t)a.Kd, (uint64_t)x_rows, T2T_CTA_ROWS))
+  if (!tc_make_map(&mx128, X, KIND, (uint64_t)a.Kd, (uint64_t)x_rows, 128) ||
+      !tc_make_map(&mx64, X, KIND, (uint64_t)a.Kd, (uint64_t)x_rows, 64) ||
+      !tc_make_map(&mx32, X, KIND, (uint64_t)a.Kd, (uint64_t)x_rows, 32))
     return cudaErrorInvalidValue;
   if (!tc_make_map(&mw, W, KIND, (uint64_t)a.Kd, (uint64_t)a.G * a.N, T2T_CTA_ROWS))
     return cudaErrorInvalidValue;
@@ -325,7 +340,7 @@ static cudaError_t launch_tc2t(const void* X, const void* W, const TcArgs& a, in
   int64_t clusters = w_tiles * t_bound;
   if (clusters > num_sms / 2) clusters = num_sms / 2;
   if (clusters < 1) clusters = 1;
-  kern<<<(unsigned)(2 * clusters), TC_THREADS, Lay::ALLOC, st>>>(mx, mw, a);
+  kern<<<(unsigned)(2 * clusters), TC_THREADS, Lay::ALLOC, st>>>(mx128, mx64, mx32, mw, a);
   count_launch();
   return cudaGetLastError();
 }

@@ -20,7 +20,15 @@
 
 namespace moe {
 
-template <int VPT>
+// Integer key whose unsigned order is the fp32 order of the score (-0 and +0 map to
+// the same key, as they compare equal); never 0 for a finite or infinite score.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  if (f == 0.f) f = 0.f;
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int VPT, int TPW>
 __global__ void __launch_bounds__(ROUTE_WARPS * 32)
 softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
                     int32_t* __restrict__ ids, float* __restrict__ wout,
@@ -37,14 +45,14 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
     sb[j] = (sel_bias != nullptr && e < E) ? sel_bias[e] : 0.f;
   }
 
-  const int t0 = blockIdx.x * ROUTE_TOKENS + warp * ROUTE_TPW;
+  const int t0 = (blockIdx.x * ROUTE_WARPS + warp) * TPW;
   // the warp's token rows are loaded up front: one memory latency for all of them.  With
   // a split-K router the logits are the partial slices summed in slice order, plus the
   // bias; they are written back to `logits`.
-  float vv[ROUTE_TPW][VPT];
+  float vv[TPW][VPT];
   const size_t stride = (size_t)T * E;
 #pragma unroll
-  for (int i = 0; i < ROUTE_TPW; ++i) {
+  for (int i = 0; i < TPW; ++i) {
     const int t = t0 + i;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
@@ -65,7 +73,7 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
     }
   }
 #pragma unroll
-  for (int i = 0; i < ROUTE_TPW; ++i) {
+  for (int i = 0; i < TPW; ++i) {
     const int t = t0 + i;
     if (t >= T) break;  // warp-uniform
     float v[VPT];
@@ -100,26 +108,24 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
     uint32_t taken = 0;
     int my_id = 0;
     float my_w = 0.f, wsum = 0.f;
+    uint32_t key[VPT];  // order-preserving integer image of each score (0: no candidate)
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) key[j] = (lane + 32 * j < E) ? score_key(sc[j]) : 0u;
     for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
+      // each lane's best untaken score (equal scores: the lower j, i.e. the lower id),
+      // then the warp's largest key and, among the lanes holding it, the lowest id
+      uint32_t bk = 0;
+      int be = INT_MAX;
 #pragma unroll
       for (int j = 0; j < VPT; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u) && (sc[j] > bv || (sc[j] == bv && e < bi))) {
-          bv = sc[j];
-          bi = e;
+        const uint32_t kj = ((taken >> j) & 1u) ? 0u : key[j];
+        if (kj > bk) {
+          bk = kj;
+          be = lane + 32 * j;
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
+      const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
+      const int bi = (int)__reduce_min_sync(0xffffffffu, bk == top ? (uint32_t)be : 0xffffffffu);
       const int owner = bi & 31, jw = bi >> 5;
       float mine = 0.f;
 #pragma unroll
@@ -156,14 +162,20 @@ cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, 
                                 float* w, float* ppart, int nblk, const float* lpart, int nsplit,
                                 const float* bias, const float* sel_bias, cudaStream_t st) {
   const dim3 grid(nblk), block(ROUTE_WARPS * 32);
-  if (E <= 32)
-    softmax_topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias, sel_bias);
-  else if (E <= 64)
-    softmax_topk_kernel<2><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias, sel_bias);
-  else if (E <= 128)
-    softmax_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias, sel_bias);
-  else
-    softmax_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, nsplit, bias, sel_bias);
+#define MOE_SOFTMAX_TOPK(V, P)                                                                  \
+  softmax_topk_kernel<V, P><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, \
+                                                    nsplit, bias, sel_bias)
+  const bool four = route_tpw(T) == 4;
+  if (E <= 32) {
+    if (four) MOE_SOFTMAX_TOPK(1, 4); else MOE_SOFTMAX_TOPK(1, 1);
+  } else if (E <= 64) {
+    if (four) MOE_SOFTMAX_TOPK(2, 4); else MOE_SOFTMAX_TOPK(2, 1);
+  } else if (E <= 128) {
+    if (four) MOE_SOFTMAX_TOPK(4, 4); else MOE_SOFTMAX_TOPK(4, 1);
+  } else {
+    if (four) MOE_SOFTMAX_TOPK(8, 4); else MOE_SOFTMAX_TOPK(8, 1);
+  }
+#undef MOE_SOFTMAX_TOPK
   count_launch();
   return cudaGetLastError();
 }

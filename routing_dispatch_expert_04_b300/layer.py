@@ -205,12 +205,14 @@ class MoELayer:
         N.expert_down(self.cfg, self.h_s, self.shared_offsets, 1, self.T, self.w2s, self.y_s, self.ws,
                       stream)
 
-    def combine(self, stream=None):
-        N.combine(self.cfg, self.y_perm, self.slot, self.w, self.y_s if self.shared else None, self.y,
-                  stream)
+    def combine(self, stream=None, y=None):
+        N.combine(self.cfg, self.y_perm, self.slot, self.w, self.y_s if self.shared else None,
+                  self.y if y is None else y, stream)
 
-    def aux(self, stream=None):
-        N.aux_stats(self.cfg, self.counts, self.ws, self.f, self.P, self.l_aux, stream)
+    def aux(self, stream=None, stats=None):
+        """stats: optional (f, P, l_aux) output tensors instead of the layer's own."""
+        f, P, l_aux = (self.f, self.P, self.l_aux) if stats is None else stats
+        N.aux_stats(self.cfg, self.counts, self.ws, f, P, l_aux, stream)
 
     # ---------------------------------------------------------------- whole layer
     def stage_names(self):
@@ -223,8 +225,9 @@ class MoELayer:
             names.append("shared_expert")
         return names + ["combine", "aux"]
 
-    def forward(self, x, stream=None, logits_in=None, marks=None):
-        """Enqueue the whole layer; returns the output buffer ``self.y``.
+    def forward(self, x, stream=None, logits_in=None, marks=None, y=None, stats=None):
+        """Enqueue the whole layer; returns the output buffer (``self.y`` unless ``y`` is
+        given; ``stats`` = (f, P, l_aux) redirects the aux statistics the same way).
 
         With ``overlap`` the work goes on the current stream plus the layer's side stream,
         forked and joined with events (so it can be captured in a CUDA graph); otherwise
@@ -248,11 +251,11 @@ class MoELayer:
                 self.shared_expert(x, stream)
                 i += 1
             mark(i)
-            self.combine(stream)
+            self.combine(stream, y)
             mark(i + 1)
-            self.aux(stream)
+            self.aux(stream, stats)
             mark(i + 2)
-            return self.y
+            return self.y if y is None else y
         main = torch.cuda.current_stream()
         side = self.side
         if self.shared:
@@ -269,7 +272,7 @@ class MoELayer:
         routed.record(main)
         side.wait_event(routed)
         with torch.cuda.stream(side):
-            self.aux()
+            self.aux(None, stats)
         joined = torch.cuda.Event()
         joined.record(side)
         mark(2)
@@ -278,9 +281,9 @@ class MoELayer:
         self.experts_down()
         mark(4)
         main.wait_event(joined)
-        self.combine()
+        self.combine(None, y)
         mark(5)
-        return self.y
+        return self.y if y is None else y
 
     def capture(self, x, marks=None):
         """Record the whole forward on the input buffer ``x`` as one CUDA graph, so a step
@@ -320,3 +323,63 @@ class MoELayer:
         st = N.sync_status(self.ws)
         if st != 0:
             raise N.MoeError("moe_sync_status", st)
+
+
+class HostStream:
+    """Layer forwards on batches that live in pinned host memory, pipelined.
+
+    Batch i is uploaded on a copy stream, run through the layer (one CUDA-graph replay)
+    on the compute stream, and its output and aux statistics are downloaded on a second
+    copy stream.  Two device input slots and two output slots alternate, so batch i+1's
+    upload and batch i-1's download overlap batch i's compute; events order every reuse
+    of a slot.  All work is enqueued; :meth:`run` returns without synchronising."""
+
+    def __init__(self, layer: MoELayer, x_like):
+        self.layer = layer
+        dev = layer.device
+        E = layer.E
+        self.xb = [x_like.clone() for _ in range(2)]  # valid data for the warm-up forward
+        self.yb = [torch.empty_like(layer.y) for _ in range(2)]
+        self.sb = [(torch.empty(E, dtype=torch.float32, device=dev),
+                    torch.empty(E, dtype=torch.float32, device=dev),
+                    torch.empty(1, dtype=torch.float32, device=dev)) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.uploaded = [torch.cuda.Event() for _ in range(2)]
+        self.downloaded = [torch.cuda.Event() for _ in range(2)]
+        self.graphs = []
+        for s in range(2):
+            layer.forward(self.xb[s], y=self.yb[s], stats=self.sb[s])  # outside capture first
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                layer.forward(self.xb[s], y=self.yb[s], stats=self.sb[s])
+            self.graphs.append(g)
+        self.i = 0
+
+    def run(self, x_host, y_host, stats_host=None):
+        """Enqueue one batch: x_host (pinned, like x) in, y_host (pinned, like y) and
+        optionally stats_host (pinned fp32 [2E+1]: f, P, l_aux) out."""
+        s = self.i & 1
+        self.i += 1
+        main = torch.cuda.current_stream()
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.computed[s])        # the slot's previous batch is done
+            self.xb[s].copy_(x_host, non_blocking=True)
+            self.uploaded[s].record(self.h2d)
+        main.wait_event(self.uploaded[s])
+        main.wait_event(self.downloaded[s])              # the slot's previous output is out
+        self.graphs[s].replay()
+        self.computed[s].record(main)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.computed[s])
+            y_host.copy_(self.yb[s], non_blocking=True)
+            if stats_host is not None:
+                E = self.layer.E
+                f, P, l_aux = self.sb[s]
+                stats_host[:E].copy_(f, non_blocking=True)
+                stats_host[E:2 * E].copy_(P, non_blocking=True)
+                stats_host[2 * E:].copy_(l_aux, non_blocking=True)
+            self.downloaded[s].record(self.d2h)
+        return y_host

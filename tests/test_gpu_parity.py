@@ -94,6 +94,8 @@ def _check_routing(g, L32, K, C, E, renorm=False, alpha=0.01, sel_bias=None, ord
     (4097, 33, 5, 2.0, True, False),
     (1, 1, 1, 1.0, False, False),
     (37, 5, 5, 0.5, True, False),
+    (300, 256, 32, 1.0, True, True),     # the largest supported top-K
+    (77, 32, 32, 0.7, True, False),      # K = E = 32
 ])
 def test_routing_bit_exact_random_logits(T, E, K, cf, ties, renorm):
     L32 = make_logits(T, E, seed=T + E, ties=ties).numpy()
@@ -454,3 +456,31 @@ def test_graph_replay_matches_eager(idx, overlap):
         assert torch.equal(layer.y, y_ref) and torch.equal(layer.l_aux, l_ref)
         assert marks[0].elapsed_time(marks[-1]) > 0
     layer.check_device_status()
+
+
+def test_host_stream_pipeline_matches_eager():
+    """Pipelined host-buffer forwards (two device slots, uploads/downloads on their own
+    streams) give, batch by batch, exactly the eager forward's output and statistics,
+    with different inputs alternating so a slot mix-up would show."""
+    from routing_dispatch_expert_04_b300.layer import HostStream
+    wl = SMALL[4]                                   # bf16, bias, shared expert
+    inp = make_inputs(wl, "cuda")
+    x2 = make_inputs(wl, "cuda", seed=1, weights=False)["x"]
+    layer = MoELayer.from_workload(wl, inp)
+    refs = []
+    for x in (inp["x"], x2):
+        layer.forward(x)
+        torch.cuda.synchronize()
+        refs.append((layer.y.clone().cpu(), torch.cat([layer.f, layer.P, layer.l_aux]).cpu()))
+    hs = HostStream(layer, inp["x"])
+    xs = [inp["x"].cpu().pin_memory(), x2.cpu().pin_memory()]
+    n = 6
+    ys = [torch.empty((wl.T, wl.d), dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    sts = [torch.empty(2 * wl.E + 1, dtype=torch.float32).pin_memory() for _ in range(n)]
+    for i in range(n):
+        hs.run(xs[i & 1], ys[i], sts[i])
+    torch.cuda.synchronize()
+    layer.check_device_status()
+    for i in range(n):
+        assert torch.equal(ys[i], refs[i & 1][0]), i
+        assert torch.equal(sts[i], refs[i & 1][1]), i
