@@ -287,7 +287,8 @@ def run_ours(args, wl):
     dom_flops = flops_up if dom == "expert_up" else flops_down
     achieved_tf = dom_flops / (avg[dom] * 1e-3) / 1e12
     kernel_srcs = ["routing_dispatch_expert_04_b300/csrc/" + f
-                   for f in ("gemm_tc.cu", "gemm_tc2.cu", "tc_common.cuh", "tc_ptx.cuh")]
+                   for f in ("gemm_tc.cu", "gemm_tc2.cu", "gemm_tc2t.cu", "tc_common.cuh",
+                             "tc_ptx.cuh")]
     traffic = recorded_traffic(f"{dom}:{wl.name}:{args.experts}:{args.gemm}",
                                source_digest(*kernel_srcs))
     if args.experts == "e4m3":

@@ -286,16 +286,21 @@ moe_status_t moe_sync_status(void* ws, void* stream);
  *   MOE_GEMM_PAIR   two CTAs per 256-row tile (tcgen05 cta_group::2: one MMA over two
  *                   SMs, each SM loading half of the operands), which pads each group
  *                   to a multiple of 256 rows;
- *   MOE_GEMM_SPLIT  pairs for each group's whole 256-row tiles, then one CTA per 128-row
- *                   tile for the remaining rows (two launches on the stream);
+ *   MOE_GEMM_SPLIT  pairs for each group's whole 256-row tiles and, at the same time on
+ *                   the other SMs, one CTA per 128-row tile for the remaining rows (the
+ *                   second kernel runs on a library-owned stream per device, forked from
+ *                   and joined back into the caller's stream with events, which also
+ *                   works under stream capture; calls on different streams that use this
+ *                   plan share that side stream);
  *   MOE_GEMM_PAIR_T two CTAs per tile computing the transpose: 256 weight rows (output
  *                   columns) on the MMA's M side and up to 256 of a group's rows on its
  *                   N side, sized to the group (rounded up to 32), so no group is padded
  *                   to 256 rows; row-gathered and E4M3 calls use the other kernels;
  *   MOE_GEMM_AUTO   (default) pairs when the 256-row padding is at most 5% of the rows
- *                   (judged from the capacity), transposed pairs when the groups have
- *                   no capacity bound, one CTA otherwise (pairs of either kind need the
- *                   output width to be a multiple of 256).
+ *                   (judged from the capacity), the split when the capacity reaches 256
+ *                   rows, transposed pairs when the groups have no capacity bound, one
+ *                   CTA otherwise (all pair plans need the output width to be a
+ *                   multiple of 256).
  * Every choice sums the same products in the same order, so results are identical.
  * Returns MOE_ERR_INVALID for any other value.  Calls already enqueued are unaffected. */
 typedef enum {

@@ -22,6 +22,8 @@
 // zeros).  Every mbarrier wait is bounded: after WAIT_LIMIT_NS the CTA records a timeout
 // in the status word, every role leaves its loop, in-flight copies and MMAs are awaited
 // (bounded), TMEM is freed and the CTA exits.
+#include <mutex>
+
 #include "tc_common.cuh"
 
 namespace moe {
@@ -347,12 +349,13 @@ cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const 
 // 96 B/clk of operands from shared memory and its TMA stages write as much again, more
 // than the SM's shared memory delivers, which caps the tensor pipe near two thirds; a
 // pair MMA reads and stages half of B per SM.  But pairs pad a group to a multiple of
-// 256 rows, and the split's second launch waits for the first one's tail.  Measured on
-// the layer shapes (B300), pairs win only where that padding is small, so MOE_GEMM_AUTO
-// takes pairs when the padding is at most 5% (judged from the per-group row bound, when
-// known, and with N filling 256-wide tiles) and one CTA otherwise; groups of unknown
-// size (no capacity) go to the transposed pairs, which size the token side of each tile
-// to the group (measured fastest on the DeepSeek-V3-shaped layer).
+// 256 rows.  The split runs pairs on each group's whole 256-row tiles and, at the same
+// time on the remaining SMs, one CTA per tile on the rest.  Measured on the layer shapes
+// (B300), MOE_GEMM_AUTO takes pairs when their padding is at most 5% (judged from the
+// per-group row bound, and with N filling 256-wide tiles), the split when groups are
+// known to reach 256 rows (Mixtral shape: 0.50 -> 0.47-0.48 ms per GEMM), one CTA
+// otherwise, and for groups of unknown size (no capacity) the transposed pairs, which
+// size the token side of each tile to the group (DeepSeek-V3 shape).
 enum { PLAN_SINGLE = 0, PLAN_PAIR = 1, PLAN_SPLIT = 2, PLAN_PAIR_T = 3 };
 
 cudaError_t launch_tc2t_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
@@ -374,7 +377,52 @@ static int gemm_plan(int mode, int64_t rows_cap, int G, int64_t cap_per_group, i
   const int64_t per = cap_per_group < rows_cap ? cap_per_group : rows_cap;
   const int64_t rows128 = (int64_t)G * ((per + 127) / 128) * 128;
   const int64_t rows256 = (int64_t)G * ((per + 255) / 256) * 256;
-  return rows256 * 100 <= rows128 * 105 ? PLAN_PAIR : PLAN_SINGLE;
+  if (rows256 * 100 <= rows128 * 105) return PLAN_PAIR;
+  return per >= 256 ? PLAN_SPLIT : PLAN_SINGLE;
+}
+
+// The split plan runs the CTA-pair kernel (whole 256-row tiles) and the one-CTA kernel
+// (the rest of each group) at the same time on disjoint SM shares: the second kernel
+// goes on a library-owned side stream, forked from and joined back into the caller's
+// stream with events (which also works inside stream capture).  One side stream and
+// one event pair per device, created on first use.
+struct SplitStreams {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static cudaError_t split_streams(SplitStreams** out) {
+  static std::mutex mu;
+  static SplitStreams per_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  SplitStreams& s = per_dev[dev];
+  if (s.side == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &s;
+  return cudaSuccess;
+}
+
+// SMs given to the pair kernel in the split plan: its share of the rows, weighted by
+// the one-CTA kernel taking ~1.1x as long per row (measured per-tile MMA rates), so that
+// both finish together; an even count (whole pairs), leaving the one-CTA kernel some.
+static int split_pair_sms(int64_t cap_per_group, int num_sms) {
+  double frac = 0.75;  // groups of unknown size
+  if (cap_per_group > 0) {
+    const double whole = (double)(cap_per_group / 256 * 256);
+    const double rest = (double)(cap_per_group - cap_per_group / 256 * 256);
+    frac = whole / (whole + 1.1 * rest);
+  }
+  int sp = ((int)(num_sms * frac)) & ~1;
+  if (sp > num_sms - 2) sp = (num_sms - 2) & ~1;
+  if (sp < 2) sp = 2;
+  return sp;
 }
 
 template <int EPI, int KIND, bool GATHER>
@@ -404,13 +452,24 @@ cudaError_t launch_tc_up(const void* a_in, const int32_t* gather_src, int gather
                                                                   num_sms, st)
                   : launch_tc_single<TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, cap_per_group,
                                                                    num_sms, st);
-  cudaError_t e = launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd,
-                                rows_cap, plan == PLAN_PAIR ? TC_ROWS_ALL : TC_ROWS_FULL256, hdr,
-                                num_sms, st);
-  if (e != cudaSuccess || plan == PLAN_PAIR) return e;
+  if (plan == PLAN_PAIR)
+    return launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd,
+                         rows_cap, TC_ROWS_ALL, hdr, num_sms, st);
+  SplitStreams* ss = nullptr;
+  cudaError_t e = split_streams(&ss);
+  if (e != cudaSuccess) return e;
+  const int sp = split_pair_sms(cap_per_group, num_sms);
+  if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(ss->side, ss->fork, 0)) != cudaSuccess) return e;
+  e = launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd, rows_cap,
+                    TC_ROWS_FULL256, hdr, sp, st);
+  if (e != cudaSuccess) return e;
   a.row_part = TC_ROWS_REST256;
-  return gather ? launch_tc_single<TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, 255, num_sms, st)
-                : launch_tc_single<TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, 255, num_sms, st);
+  e = gather ? launch_tc_single<TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, 255, num_sms - sp, ss->side)
+             : launch_tc_single<TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, 255, num_sms - sp, ss->side);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaEventRecord(ss->join, ss->side)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(st, ss->join, 0);
 }
 
 // Second expert Linear, fp16 in, fp32 out: y_perm[r] = h[r] . W2[g]^T.
@@ -424,11 +483,22 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
            TC_ROWS_ALL};
   if (plan == PLAN_SINGLE)
     return launch_tc_single<TC_EPI_F32, OP_F16, false>(h, w2h, a, cap_per_group, num_sms, st);
-  cudaError_t e = launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap,
-                                  plan == PLAN_PAIR ? TC_ROWS_ALL : TC_ROWS_FULL256, hdr, num_sms, st);
-  if (e != cudaSuccess || plan == PLAN_PAIR) return e;
+  if (plan == PLAN_PAIR)
+    return launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_ALL, hdr,
+                           num_sms, st);
+  SplitStreams* ss = nullptr;
+  cudaError_t e = split_streams(&ss);
+  if (e != cudaSuccess) return e;
+  const int sp = split_pair_sms(cap_per_group, num_sms);
+  if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(ss->side, ss->fork, 0)) != cudaSuccess) return e;
+  e = launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_FULL256, hdr, sp, st);
+  if (e != cudaSuccess) return e;
   a.row_part = TC_ROWS_REST256;
-  return launch_tc_single<TC_EPI_F32, OP_F16, false>(h, w2h, a, 255, num_sms, st);
+  e = launch_tc_single<TC_EPI_F32, OP_F16, false>(h, w2h, a, 255, num_sms - sp, ss->side);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaEventRecord(ss->join, ss->side)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(st, ss->join, 0);
 }
 
 // First expert Linear on E4M3 operands (codes + per-row scales), GELU fused, fp16 out:
