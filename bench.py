@@ -278,7 +278,8 @@ def run_ours(args, wl):
     bytes_dispatch = A * 12 + R * 4
     if args.dispatch == "copy":
         bytes_dispatch += t_active * wl.d * b + R * wl.d * b
-    bytes_combine = R * wl.d * 4 + wl.T * wl.d * b + A * 8 + (wl.T * wl.d * 4 if layer.shared else 0)
+    yb = 2 if wl.dtype == "bf16" else 4  # expert outputs: fp16 for bf16 layers
+    bytes_combine = R * wl.d * yb + wl.T * wl.d * b + A * 8 + (wl.T * wl.d * yb if layer.shared else 0)
     bytes_route = wl.T * wl.d * b + wl.E * wl.d * b + wl.T * wl.E * 4 * 2 + A * 8
     med = {n: statistics.median(v) for n, v in stage_ms.items()}
     avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}

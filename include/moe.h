@@ -27,8 +27,9 @@
  *   packed rows exceeding the buffer, an fp16 overflow) are recorded in a status word inside `ws`;
  *   moe_sync_status() synchronises the stream, returns and clears it.
  * - Activations and weights have the config's dtype (fp32 or bf16); logits, routing
- *   weights, biases, expert outputs (y_perm, y_shared) and statistics are fp32;
- *   indices are int32.
+ *   weights, biases and statistics are fp32; the intermediate activation h and the
+ *   expert outputs (y_perm, y_shared) are fp16 for bf16 layers and fp32 for fp32
+ *   layers; indices are int32.
  * - Weights use the Linear layout [out, in]: W_r [E, d], W1 [G, F, d], W2 [G, d, F].
  * - Flat assignment index a = t*K + k.  Routing ties: logits compare as fp32, higher
  *   first, equal values -> lower expert id.  Routing weights are the softmax
@@ -193,8 +194,9 @@ moe_status_t moe_expert_up_gather(const moe_config* cfg, const void* x, const in
  *   h [rows_cap, F] as written by moe_expert_up (fp32, or fp16 for MOE_BF16 layers);
  *   w2 [n_groups, d, F]: fp32 for MOE_F32 layers; FP16 for MOE_BF16 layers (convert the
  *   bf16 weights once with moe_bf16_to_f16);
- *   y_perm [rows_cap, d] FP32 out (expert outputs stay fp32 until the combine rounds
- *   the layer output once). */
+ *   y_perm [rows_cap, d] out: fp32 for MOE_F32 layers; FP16 for MOE_BF16 layers (11
+ *   significant bits, rounded once from the fp32 accumulator; the combine then sums in
+ *   fp32 and rounds the layer output once; |y| > 65504 is reported as MOE_ERR_DEVICE). */
 moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t* offsets,
                              int32_t n_groups, int64_t rows_cap, const void* w2, void* y_perm,
                              void* ws, void* stream);
@@ -222,7 +224,7 @@ moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t
  *   moe_expert_up_gather) or a = r when src is NULL (xq then holds the packed rows);
  *   h [rows_cap, F] fp16 out.
  * moe_expert_down_e4m3: y_perm[r] = h_scale[r] * w2_scale[g*d + n] * sum_k hq[r,k] w2q[g*d+n,k];
- *   y_perm [rows_cap, d] fp32 out.
+ *   y_perm [rows_cap, d] fp16 out (as moe_expert_down for bf16 layers).
  * Other arguments as moe_expert_up / moe_expert_down.  d and F must be multiples of 16
  * (else MOE_ERR_UNSUPPORTED); MOE_F32 layers return MOE_ERR_UNSUPPORTED. */
 moe_status_t moe_quantize_e4m3(const void* src, int32_t dtype, int64_t rows, int32_t cols,
@@ -245,8 +247,9 @@ moe_status_t moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const in
  * expert_output[token] * routing_weight[token]").  Gather-side, no atomics:
  *   Y[t] = sum_{k ascending, slot[t,k] >= 0} topk_w[t,k] * y_perm[slot[t,k]]
  *          (+ y_shared[t]), accumulated in fp32 and rounded once.
- *   y_perm [rows_cap, d] fp32, slot [T, K], topk_w [T, K], y_shared [T, d] fp32
- *   nullable, y [T, d] dtype out.  A dropped assignment contributes exactly 0. */
+ *   y_perm [rows_cap, d] and y_shared [T, d] (nullable): fp16 for MOE_BF16 layers, fp32
+ *   for MOE_F32 layers, as moe_expert_down writes them; slot [T, K], topk_w [T, K];
+ *   y [T, d] dtype out.  A dropped assignment contributes exactly 0. */
 moe_status_t moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot,
                          const float* topk_w, const void* y_shared, void* y, void* stream);
 

@@ -3,9 +3,10 @@
 // Combine -- "Expert Parallelism (MoE)", "MoE Layer Structure": Y = sum over the selected
 // experts of expert_output[token] * routing_weight[token]; "Expert Parallelism (EP)",
 // step 4 (all-to-all COMBINE sends outputs back to each token's home position).  On one
-// GPU this is a gather: one warp per token reads the token's kept packed rows (fp32
-// expert outputs) with 16-byte loads, accumulates w * y in fp32 in ascending k (then the shared expert's row),
-// and stores the token's row once.  Each output element is written by exactly one
+// GPU this is a gather: one warp per token reads the token's kept packed rows (expert
+// outputs: fp16 for bf16 layers, fp32 for fp32 layers) with 16-byte loads, accumulates
+// w * y in fp32 in ascending k (then the shared expert's row), and stores the token's
+// row once.  Each output element is written by exactly one
 // thread, so there are no atomics and the result is deterministic.  A dropped
 // assignment (slot -1) contributes exactly 0.
 //
@@ -14,32 +15,53 @@
 // dropping) and P_i the mean softmax probability of expert i.  P_i is a fixed-order
 // fp64 reduction of the per-block partial sums the routing kernel left in the workspace,
 // and the sum over experts is taken in expert order, so the result is deterministic.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace moe {
 
-// Expert outputs (yp, ys) are fp32.  Each lane handles two 4-column slots per pass (j and
-// j + 32) so that up to 2 x 4 row loads are in flight per lane; k is summed in order.
-template <typename T>
-__device__ __forceinline__ void store4(T* out, const float* acc);
+// Expert outputs (yp, ys) are fp16 for bf16 layers and fp32 for fp32 layers.  Each
+// lane handles two 16-byte slots per pass (j and j + 32: 8 fp16 or 4 fp32 columns each),
+// so that up to 2 x 4 row loads are in flight per lane; k is summed in order, in fp32.
+template <typename Tin> struct CombineIn;
+template <> struct CombineIn<float> {
+  static constexpr int P = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    Elem<float>::unpack(v, f);
+  }
+};
+template <> struct CombineIn<__half> {
+  static constexpr int P = 8;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = p.x;
+      f[2 * i + 1] = p.y;
+    }
+  }
+};
+
+// One 16-byte slot of P output columns, rounded once to the output type.
+template <typename Tout, int P>
+__device__ __forceinline__ void store_slot(Tout* out, const float* acc);
 template <>
-__device__ __forceinline__ void store4<float>(float* out, const float* acc) {
+__device__ __forceinline__ void store_slot<float, 4>(float* out, const float* acc) {
   st_v4(out, Elem<float>::pack(acc));
 }
 template <>
-__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* out, const float* acc) {
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
-  *reinterpret_cast<uint2*>(out) =
-      make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+__device__ __forceinline__ void store_slot<__nv_bfloat16, 8>(__nv_bfloat16* out, const float* acc) {
+  st_v4(out, Elem<__nv_bfloat16>::pack(acc));
 }
 
-template <typename T>
+template <typename Tout, typename Tin>
 __global__ void __launch_bounds__(256)
-combine_kernel(const float* __restrict__ yp, const int32_t* __restrict__ slot,
-               const float* __restrict__ w, const float* __restrict__ ys, T* __restrict__ y,
+combine_kernel(const Tin* __restrict__ yp, const int32_t* __restrict__ slot,
+               const float* __restrict__ w, const Tin* __restrict__ ys, Tout* __restrict__ y,
                int Tn, int d, int K) {
-  constexpr int P = 4, KC = 4;
+  constexpr int P = CombineIn<Tin>::P, KC = 4;
   __shared__ int s_slot[8][32];
   __shared__ float s_w[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -71,8 +93,8 @@ combine_kernel(const float* __restrict__ yp, const int32_t* __restrict__ slot,
           const int k = k0 + u;
           if (k < K && s_slot[warp][k] >= 0) {
             float f0[P], f1[P];
-            Elem<float>::unpack(v0[u], f0);
-            Elem<float>::unpack(v1[u], f1);
+            CombineIn<Tin>::unpack(v0[u], f0);
+            CombineIn<Tin>::unpack(v1[u], f1);
             const float wk = s_w[warp][k];
 #pragma unroll
             for (int i = 0; i < P; ++i) {
@@ -85,17 +107,17 @@ combine_kernel(const float* __restrict__ yp, const int32_t* __restrict__ slot,
       if (ys != nullptr) {
         const uint4* rs = reinterpret_cast<const uint4*>(ys + (size_t)t * d);
         float f0[P], f1[P];
-        Elem<float>::unpack(ld_nc_v4(rs + j0), f0);
-        Elem<float>::unpack(two ? ld_nc_v4(rs + j1) : make_uint4(0u, 0u, 0u, 0u), f1);
+        CombineIn<Tin>::unpack(ld_nc_v4(rs + j0), f0);
+        CombineIn<Tin>::unpack(two ? ld_nc_v4(rs + j1) : make_uint4(0u, 0u, 0u, 0u), f1);
 #pragma unroll
         for (int i = 0; i < P; ++i) {
           acc0[i] += f0[i];
           acc1[i] += f1[i];
         }
       }
-      T* out = y + (size_t)t * d;
-      store4<T>(out + (size_t)j0 * P, acc0);
-      if (two) store4<T>(out + (size_t)j1 * P, acc1);
+      Tout* out = y + (size_t)t * d;
+      store_slot<Tout, P>(out + (size_t)j0 * P, acc0);
+      if (two) store_slot<Tout, P>(out + (size_t)j1 * P, acc1);
     }
     __syncwarp();
   }
@@ -226,11 +248,11 @@ cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const
   const int want = (Tn + 7) / 8;
   const int grid = want < num_sms * 16 ? want : num_sms * 16;
   if (dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const float*)yp, slot, w,
-                                                        (const float*)ys, (__nv_bfloat16*)y, Tn, d, K);
+    combine_kernel<__nv_bfloat16, __half><<<grid, 256, 0, st>>>(
+        (const __half*)yp, slot, w, (const __half*)ys, (__nv_bfloat16*)y, Tn, d, K);
   else
-    combine_kernel<float><<<grid, 256, 0, st>>>((const float*)yp, slot, w, (const float*)ys,
-                                                (float*)y, Tn, d, K);
+    combine_kernel<float, float><<<grid, 256, 0, st>>>((const float*)yp, slot, w, (const float*)ys,
+                                                       (float*)y, Tn, d, K);
   count_launch();
   return cudaGetLastError();
 }

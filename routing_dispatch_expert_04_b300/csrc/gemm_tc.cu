@@ -472,7 +472,7 @@ cudaError_t launch_tc_up(const void* a_in, const int32_t* gather_src, int gather
   return cudaStreamWaitEvent(st, ss->join, 0);
 }
 
-// Second expert Linear, fp16 in, fp32 out: y_perm[r] = h[r] . W2[g]^T.
+// Second expert Linear, fp16 in, fp16 out: y_perm[r] = h[r] . W2[g]^T.
 cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
                            int G, int N, int Kd, int64_t rows_cap, int64_t cap_per_group,
                            int pair_mode, uint32_t* hdr, int num_sms, cudaStream_t st) {
@@ -482,7 +482,7 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            TC_ROWS_ALL};
   if (plan == PLAN_SINGLE)
-    return launch_tc_single<TC_EPI_F32, OP_F16, false>(h, w2h, a, cap_per_group, num_sms, st);
+    return launch_tc_single<TC_EPI_F16, OP_F16, false>(h, w2h, a, cap_per_group, num_sms, st);
   if (plan == PLAN_PAIR)
     return launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_ALL, hdr,
                            num_sms, st);
@@ -495,7 +495,7 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
   e = launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_FULL256, hdr, sp, st);
   if (e != cudaSuccess) return e;
   a.row_part = TC_ROWS_REST256;
-  e = launch_tc_single<TC_EPI_F32, OP_F16, false>(h, w2h, a, 255, num_sms - sp, ss->side);
+  e = launch_tc_single<TC_EPI_F16, OP_F16, false>(h, w2h, a, 255, num_sms - sp, ss->side);
   if (e != cudaSuccess) return e;
   if ((e = cudaEventRecord(ss->join, ss->side)) != cudaSuccess) return e;
   return cudaStreamWaitEvent(st, ss->join, 0);
@@ -517,7 +517,7 @@ cudaError_t launch_tc_up_e4m3(const void* xq, const float* sx, const int32_t* ga
   return launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, false>(xq, w1q, a, cap_per_group, num_sms, st);
 }
 
-// Second expert Linear on E4M3 operands, fp32 out:
+// Second expert Linear on E4M3 operands, fp16 out:
 // y_perm[r] = sh[r] * sw2[g*N + n] * sum_k hq[r, k] w2q[g*N + n, k].
 cudaError_t launch_tc_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
                                 void* y_perm, const int32_t* offsets, int G, int N, int Kd,
@@ -526,7 +526,7 @@ cudaError_t launch_tc_down_e4m3(const void* hq, const float* sh, const void* w2q
   constexpr int BKE = OpKind<OP_E4M3>::BK;
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + BKE - 1) / BKE, 0,
            TC_ROWS_ALL, nullptr, 1, 0, sh, sw2};
-  return launch_tc_single<TC_EPI_F32, OP_E4M3, false>(hq, w2q, a, cap_per_group, num_sms, st);
+  return launch_tc_single<TC_EPI_F16, OP_E4M3, false>(hq, w2q, a, cap_per_group, num_sms, st);
 }
 
 // Router Linear, bf16 in, fp32 logits: logits[t] = x[t] . W_r^T + b_r.  With nsplit > 1

@@ -281,13 +281,13 @@ cudaError_t launch_tc2_up(const void* a_in, const int32_t* gather_src, int gathe
   return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, num_sms, st);
 }
 
-// Second expert Linear on CTA pairs, fp16 in, fp32 out.
+// Second expert Linear on CTA pairs, fp16 in, fp16 out.
 cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
                             int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
                             int num_sms, cudaStream_t st) {
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            row_part};
-  return launch_tc2<256, 6, TC_EPI_F32, OP_F16, false>(h, w2h, a, num_sms, st);
+  return launch_tc2<256, 6, TC_EPI_F16, OP_F16, false>(h, w2h, a, num_sms, st);
 }
 
 }  // namespace moe

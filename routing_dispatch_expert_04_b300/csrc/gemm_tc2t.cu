@@ -122,8 +122,8 @@ __device__ __forceinline__ bool epilogue_chunk_t(const uint32_t (&r)[32], int co
     const int tok = tok_first + j;
     if (tok >= tok_end) break;
     const float v = __uint_as_float(r[j]);
-    if (EPI == TC_EPI_GELU_F16) {
-      const float a = gelu_exact(v);
+    if (EPI == TC_EPI_GELU_F16 || EPI == TC_EPI_F16) {
+      const float a = EPI == TC_EPI_GELU_F16 ? gelu_exact(v) : v;
       bad |= !(fabsf(a) <= 65504.f);
       ((__half*)args.out)[(size_t)tok * args.ldo + col] = __float2half_rn(a);
     } else {
@@ -353,12 +353,12 @@ cudaError_t launch_tc2t_up(const void* x_perm, const void* w1, void* h, const in
   return launch_tc2t<6, TC_EPI_GELU_F16, OP_BF16>(x_perm, w1, a, num_sms, st);
 }
 
-// Second expert Linear, tokens on the N side: y_perm = h . W2[g]^T, fp32 out.
+// Second expert Linear, tokens on the N side: y_perm = h . W2[g]^T, fp16 out.
 cudaError_t launch_tc2t_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
                              int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
                              cudaStream_t st) {
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, 0, 0, TC_ROWS_ALL};
-  return launch_tc2t<6, TC_EPI_F32, OP_F16>(h, w2h, a, num_sms, st);
+  return launch_tc2t<6, TC_EPI_F16, OP_F16>(h, w2h, a, num_sms, st);
 }
 
 }  // namespace moe

@@ -32,7 +32,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 constexpr int TC_MAX_GROUPS = 256;
 
-enum { TC_EPI_GELU_F16 = 0, TC_EPI_F32 = 1, TC_EPI_BIAS_F32 = 2 };
+enum { TC_EPI_GELU_F16 = 0, TC_EPI_F32 = 1, TC_EPI_BIAS_F32 = 2, TC_EPI_F16 = 3 };
 
 struct TcArgs {
   const int32_t* offsets;  // [G+1] device, or nullptr: one group of M rows
@@ -189,13 +189,29 @@ __device__ __forceinline__ void apply_scales(uint32_t (&r)[32], float sa, const 
 }
 
 // Epilogue for 32 accumulator columns [col0, col0+32) of one output row, held by this
-// thread in r[] (fp32 bit patterns).  Returns true if a GELU output left the fp16 range.
+// thread in r[] (fp32 bit patterns).  Returns true if an fp16 output left the fp16 range.
 template <int EPI>
 __device__ __forceinline__ bool epilogue_chunk(const uint32_t (&r)[32], int row, int col0,
                                                const TcArgs& args, int64_t slice,
                                                const float* bias) {
   bool bad = false;
-  if (EPI == TC_EPI_GELU_F16) {
+  if (EPI == TC_EPI_F16) {
+    __half* out = (__half*)args.out + (size_t)row * args.ldo + col0;
+#pragma unroll
+    for (int v8 = 0; v8 < 4; ++v8) {
+      if (col0 + v8 * 8 >= args.N) break;
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = __uint_as_float(r[v8 * 8 + 2 * i]);
+        const float b = __uint_as_float(r[v8 * 8 + 2 * i + 1]);
+        bad |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
+        __half2 h2 = __floats2half2_rn(a, b);
+        w[i] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      st_v4(out + v8 * 8, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+  } else if (EPI == TC_EPI_GELU_F16) {
     __half* out = (__half*)args.out + (size_t)row * args.ldo + col0;
 #pragma unroll
     for (int v8 = 0; v8 < 4; ++v8) {

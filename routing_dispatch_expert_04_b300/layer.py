@@ -67,7 +67,8 @@ class MoELayer:
         # the intermediate activation is fp16 for bf16 layers (see moe_expert_up)
         self.h_dtype = torch.float16 if dtype == "bf16" else torch.float32
         self.h = torch.empty((R, F), dtype=self.h_dtype, device=dev)
-        self.y_perm = torch.empty((R, d), dtype=f32, device=dev)
+        # expert outputs: fp16 for bf16 layers (see moe_expert_down), fp32 otherwise
+        self.y_perm = torch.empty((R, d), dtype=self.h_dtype, device=dev)
         self.y = torch.empty((T, d), dtype=dt, device=dev)
         self.f = torch.empty(E, dtype=f32, device=dev)
         self.P = torch.empty(E, dtype=f32, device=dev)
@@ -85,7 +86,7 @@ class MoELayer:
         if self.shared:
             self.shared_offsets = torch.tensor([0, T], dtype=i32, device=dev)
             self.h_s = torch.empty((max(T, 1), F), dtype=self.h_dtype, device=dev)
-            self.y_s = torch.empty((max(T, 1), d), dtype=f32, device=dev)
+            self.y_s = torch.empty((max(T, 1), d), dtype=self.h_dtype, device=dev)
         if experts == "bf16":
             self.w2 = self._down_weights(w2)
             self.w2s = self._down_weights(w2s) if self.shared else None

@@ -36,7 +36,8 @@ def stage_bytes(stage, wl, T, R, t_active, b):
     if stage == "dispatch":
         return t_active * wl.d * b + R * wl.d * b + A * 12 + R * 4
     if stage == "combine":
-        return R * wl.d * 4 + T * wl.d * b + A * 8
+        yb = 2 if wl.dtype == "bf16" else 4  # expert outputs: fp16 for bf16 layers
+        return R * wl.d * yb + T * wl.d * b + A * 8
     raise ValueError(stage)
 
 
@@ -89,6 +90,8 @@ def main():
         g = torch.Generator(device=dev)
         g.manual_seed(1)
         y_perm = torch.randn((rows_cap, d), generator=g, device=dev, dtype=f32)
+        if wl.dtype == "bf16":
+            y_perm = y_perm.half()  # expert outputs of bf16 layers are fp16
         y = torch.empty((T, d), dtype=x.dtype, device=dev)
 
         def run():
