@@ -45,12 +45,12 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
 cudaError_t launch_tc_up_e4m3(const void* xq, const float* sx, const int32_t* gather_src,
                               int gather_k, int64_t gather_rows, const void* w1q, const float* sw1,
                               void* h, const int32_t* offsets, int G, int N, int Kd,
-                              int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr, int num_sms,
-                              cudaStream_t st);
+                              int64_t rows_cap, int64_t cap_per_group, int pair_mode,
+                              uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_tc_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
                                 void* y_perm, const int32_t* offsets, int G, int N, int Kd,
-                                int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr,
-                                int num_sms, cudaStream_t st);
+                                int64_t rows_cap, int64_t cap_per_group, int pair_mode,
+                                uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_quantize_e4m3(int dtype, const void* src, int64_t rows, int cols,
                                  const int32_t* rows_dev, void* codes, float* scales, int num_sms,
                                  cudaStream_t st);
@@ -301,8 +301,9 @@ moe_status_t moe_expert_up_e4m3(const moe_config* cfg, const void* xq, const flo
   if (src != nullptr && c.T == 0) return MOE_OK;
   return cuda_status(launch_tc_up_e4m3(xq, x_scale, src, c.K, src != nullptr ? c.T : 0, w1q,
                                        w1_scale, h, offsets, n_groups, c.F, c.d, rows_cap,
-                                       group_row_bound(c, n_groups, rows_cap), (uint32_t*)ws,
-                                       num_sms(), (cudaStream_t)stream));
+                                       group_row_bound(c, n_groups, rows_cap),
+                                       g_gemm_pairing.load(), (uint32_t*)ws, num_sms(),
+                                       (cudaStream_t)stream));
 }
 
 moe_status_t moe_expert_down_e4m3(const moe_config* cfg, const void* hq, const float* h_scale,
@@ -316,7 +317,8 @@ moe_status_t moe_expert_down_e4m3(const moe_config* cfg, const void* hq, const f
   const moe_config& c = *cfg;
   return cuda_status(launch_tc_down_e4m3(hq, h_scale, w2q, w2_scale, y_perm, offsets, n_groups,
                                          c.d, c.F, rows_cap, group_row_bound(c, n_groups, rows_cap),
-                                         (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
+                                         g_gemm_pairing.load(), (uint32_t*)ws, num_sms(),
+                                         (cudaStream_t)stream));
 }
 
 moe_status_t moe_quantize_e4m3(const void* src, int32_t dtype, int64_t rows, int32_t cols,

@@ -425,6 +425,21 @@ static int split_pair_sms(int64_t cap_per_group, int num_sms) {
   return sp;
 }
 
+// Runs `pair(st)` on the caller's stream and, at the same time, `rest(side)` on the side
+// stream, forked from and joined back into `st`.
+template <class PairFn, class RestFn>
+static cudaError_t run_split(cudaStream_t st, PairFn pair, RestFn rest) {
+  SplitStreams* ss = nullptr;
+  cudaError_t e = split_streams(&ss);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(ss->side, ss->fork, 0)) != cudaSuccess) return e;
+  if ((e = pair(st)) != cudaSuccess) return e;
+  if ((e = rest(ss->side)) != cudaSuccess) return e;
+  if ((e = cudaEventRecord(ss->join, ss->side)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(st, ss->join, 0);
+}
+
 template <int EPI, int KIND, bool GATHER>
 static cudaError_t launch_tc_single(const void* A, const void* B, const TcArgs& a,
                                     int64_t cap_per_group, int num_sms, cudaStream_t st) {
@@ -455,21 +470,20 @@ cudaError_t launch_tc_up(const void* a_in, const int32_t* gather_src, int gather
   if (plan == PLAN_PAIR)
     return launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd,
                          rows_cap, TC_ROWS_ALL, hdr, num_sms, st);
-  SplitStreams* ss = nullptr;
-  cudaError_t e = split_streams(&ss);
-  if (e != cudaSuccess) return e;
   const int sp = split_pair_sms(cap_per_group, num_sms);
-  if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
-  if ((e = cudaStreamWaitEvent(ss->side, ss->fork, 0)) != cudaSuccess) return e;
-  e = launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd, rows_cap,
-                    TC_ROWS_FULL256, hdr, sp, st);
-  if (e != cudaSuccess) return e;
   a.row_part = TC_ROWS_REST256;
-  e = gather ? launch_tc_single<TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, 255, num_sms - sp, ss->side)
-             : launch_tc_single<TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, 255, num_sms - sp, ss->side);
-  if (e != cudaSuccess) return e;
-  if ((e = cudaEventRecord(ss->join, ss->side)) != cudaSuccess) return e;
-  return cudaStreamWaitEvent(st, ss->join, 0);
+  return run_split(
+      st,
+      [&](cudaStream_t s) {
+        return launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd,
+                             rows_cap, TC_ROWS_FULL256, hdr, sp, s);
+      },
+      [&](cudaStream_t s) {
+        return gather ? launch_tc_single<TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, 255,
+                                                                      num_sms - sp, s)
+                      : launch_tc_single<TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, 255,
+                                                                       num_sms - sp, s);
+      });
 }
 
 // Second expert Linear, fp16 in, fp16 out: y_perm[r] = h[r] . W2[g]^T.
@@ -486,19 +500,41 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
   if (plan == PLAN_PAIR)
     return launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_ALL, hdr,
                            num_sms, st);
-  SplitStreams* ss = nullptr;
-  cudaError_t e = split_streams(&ss);
-  if (e != cudaSuccess) return e;
   const int sp = split_pair_sms(cap_per_group, num_sms);
-  if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess) return e;
-  if ((e = cudaStreamWaitEvent(ss->side, ss->fork, 0)) != cudaSuccess) return e;
-  e = launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_FULL256, hdr, sp, st);
-  if (e != cudaSuccess) return e;
   a.row_part = TC_ROWS_REST256;
-  e = launch_tc_single<TC_EPI_F16, OP_F16, false>(h, w2h, a, 255, num_sms - sp, ss->side);
-  if (e != cudaSuccess) return e;
-  if ((e = cudaEventRecord(ss->join, ss->side)) != cudaSuccess) return e;
-  return cudaStreamWaitEvent(st, ss->join, 0);
+  return run_split(
+      st,
+      [&](cudaStream_t s) {
+        return launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_FULL256, hdr,
+                               sp, s);
+      },
+      [&](cudaStream_t s) {
+        return launch_tc_single<TC_EPI_F16, OP_F16, false>(h, w2h, a, 255, num_sms - sp, s);
+      });
+}
+
+cudaError_t launch_tc2_up_e4m3(const void* xq, const float* sx, const int32_t* gather_src,
+                               int gather_k, int64_t gather_rows, const void* w1q, const float* sw1,
+                               void* h, const int32_t* offsets, int G, int N, int Kd,
+                               int64_t rows_cap, int row_part, uint32_t* hdr, int num_sms,
+                               cudaStream_t st);
+cudaError_t launch_tc2_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
+                                 void* y_perm, const int32_t* offsets, int G, int N, int Kd,
+                                 int64_t rows_cap, int row_part, uint32_t* hdr, int num_sms,
+                                 cudaStream_t st);
+
+// Plan for the E4M3 GEMMs.  The transposed pairs take 16-bit operands only, so groups of
+// unknown size run on one CTA per tile (or on pairs when pairs were asked for).  E4M3
+// halves the weight bytes but doubles the tensor rate, so small groups stay HBM-bound
+// (2 x rows flops per weight byte against a ridge near 550): there the pair's halved
+// shared-memory traffic buys nothing and its longer tiles lose to the one-CTA kernel
+// (measured on B300: 192-row groups 0.111 vs 0.123 ms per GEMM; 8192-row groups pairs
+// 2.62 vs 2.68 ms).  AUTO takes pairs for E4M3 only from 512 rows per group on.
+static int gemm_plan_e4m3(int mode, int64_t rows_cap, int G, int64_t cap_per_group, int N) {
+  const int plan = gemm_plan(mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_PAIR && mode == MOE_GEMM_AUTO && cap_per_group < 512) return PLAN_SINGLE;
+  if (plan != PLAN_PAIR_T) return plan;
+  return mode == MOE_GEMM_PAIR_T ? PLAN_PAIR : PLAN_SINGLE;
 }
 
 // First expert Linear on E4M3 operands (codes + per-row scales), GELU fused, fp16 out:
@@ -507,26 +543,63 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
 cudaError_t launch_tc_up_e4m3(const void* xq, const float* sx, const int32_t* gather_src,
                               int gather_k, int64_t gather_rows, const void* w1q, const float* sw1,
                               void* h, const int32_t* offsets, int G, int N, int Kd,
-                              int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr, int num_sms,
-                              cudaStream_t st) {
+                              int64_t rows_cap, int64_t cap_per_group, int pair_mode,
+                              uint32_t* hdr, int num_sms, cudaStream_t st) {
+  const int plan = gemm_plan_e4m3(pair_mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_PAIR)
+    return launch_tc2_up_e4m3(xq, sx, gather_src, gather_k, gather_rows, w1q, sw1, h, offsets, G,
+                              N, Kd, rows_cap, TC_ROWS_ALL, hdr, num_sms, st);
   constexpr int BKE = OpKind<OP_E4M3>::BK;
+  const bool gather = gather_src != nullptr;
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + BKE - 1) / BKE, 0,
            TC_ROWS_ALL, gather_src, gather_k, gather_rows, sx, sw1};
-  if (gather_src != nullptr)
-    return launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, true>(xq, w1q, a, cap_per_group, num_sms, st);
-  return launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, false>(xq, w1q, a, cap_per_group, num_sms, st);
+  if (plan == PLAN_SINGLE)
+    return gather ? launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, true>(xq, w1q, a, cap_per_group,
+                                                                  num_sms, st)
+                  : launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, false>(xq, w1q, a, cap_per_group,
+                                                                   num_sms, st);
+  const int sp = split_pair_sms(cap_per_group, num_sms);
+  a.row_part = TC_ROWS_REST256;
+  return run_split(
+      st,
+      [&](cudaStream_t s) {
+        return launch_tc2_up_e4m3(xq, sx, gather_src, gather_k, gather_rows, w1q, sw1, h, offsets,
+                                  G, N, Kd, rows_cap, TC_ROWS_FULL256, hdr, sp, s);
+      },
+      [&](cudaStream_t s) {
+        return gather ? launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, true>(xq, w1q, a, 255,
+                                                                      num_sms - sp, s)
+                      : launch_tc_single<TC_EPI_GELU_F16, OP_E4M3, false>(xq, w1q, a, 255,
+                                                                       num_sms - sp, s);
+      });
 }
 
 // Second expert Linear on E4M3 operands, fp16 out:
 // y_perm[r] = sh[r] * sw2[g*N + n] * sum_k hq[r, k] w2q[g*N + n, k].
 cudaError_t launch_tc_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
                                 void* y_perm, const int32_t* offsets, int G, int N, int Kd,
-                                int64_t rows_cap, int64_t cap_per_group, uint32_t* hdr,
-                                int num_sms, cudaStream_t st) {
+                                int64_t rows_cap, int64_t cap_per_group, int pair_mode,
+                                uint32_t* hdr, int num_sms, cudaStream_t st) {
+  const int plan = gemm_plan_e4m3(pair_mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_PAIR)
+    return launch_tc2_down_e4m3(hq, sh, w2q, sw2, y_perm, offsets, G, N, Kd, rows_cap,
+                                TC_ROWS_ALL, hdr, num_sms, st);
   constexpr int BKE = OpKind<OP_E4M3>::BK;
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + BKE - 1) / BKE, 0,
            TC_ROWS_ALL, nullptr, 1, 0, sh, sw2};
-  return launch_tc_single<TC_EPI_F16, OP_E4M3, false>(hq, w2q, a, cap_per_group, num_sms, st);
+  if (plan == PLAN_SINGLE)
+    return launch_tc_single<TC_EPI_F16, OP_E4M3, false>(hq, w2q, a, cap_per_group, num_sms, st);
+  const int sp = split_pair_sms(cap_per_group, num_sms);
+  a.row_part = TC_ROWS_REST256;
+  return run_split(
+      st,
+      [&](cudaStream_t s) {
+        return launch_tc2_down_e4m3(hq, sh, w2q, sw2, y_perm, offsets, G, N, Kd, rows_cap,
+                                    TC_ROWS_FULL256, hdr, sp, s);
+      },
+      [&](cudaStream_t s) {
+        return launch_tc_single<TC_EPI_F16, OP_E4M3, false>(hq, w2q, a, 255, num_sms - sp, s);
+      });
 }
 
 // Router Linear, bf16 in, fp32 logits: logits[t] = x[t] . W_r^T + b_r.  With nsplit > 1

@@ -50,7 +50,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const TcArgs args) {
   using Lay = Tc2Layout<BN, STAGES>;
-  static_assert(KIND != OP_E4M3, "E4M3 operands run on the one-CTA kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + Lay::BAR_OFF);
@@ -184,8 +183,12 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
           const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
 #pragma unroll
           for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
-            mma_f16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32), IDESC,
-                         (kb != 0 || k != 0) ? 1u : 0u);
+            if (KIND == OP_E4M3)
+              mma_e4m3_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
+                            IDESC, (kb != 0 || k != 0) ? 1u : 0u);
+            else
+              mma_f16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
+                           IDESC, (kb != 0 || k != 0) ? 1u : 0u);
           }
           mma_commit_pair_mc(&empty[s], (uint16_t)3);
           if (++s == STAGES) {
@@ -214,6 +217,8 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
       tc_fence_after();
       const int row = ti.row0 + r_in_tile;
       const bool valid = row < ti.rowend;
+      float sa = 0.f;  // E4M3: this row's A scale (of its token row when gathered)
+      if (KIND == OP_E4M3 && valid) sa = args.a_scale[GATHER ? gather_row(args, row, ti.rowend) : row];
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         const int col0 = ti.n0 + c * 32;
@@ -222,6 +227,7 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
         tmem_ld_wait();
         if (!valid) continue;
+        if (KIND == OP_E4M3) apply_scales(r, sa, args.b_scale + (size_t)ti.g * args.N, col0, args.N);
         if (epilogue_chunk<EPI>(r, row, col0, args, 0, nullptr)) raise_error(args.hdr, DEV_ERR_RANGE);
       }
       tc_fence_before();
@@ -279,6 +285,31 @@ cudaError_t launch_tc2_up(const void* a_in, const int32_t* gather_src, int gathe
   if (gather_src != nullptr)
     return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, num_sms, st);
   return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, num_sms, st);
+}
+
+// Expert Linears on CTA pairs with E4M3 operands (codes + per-row scales applied in the
+// epilogue): the first with GELU (rows optionally gathered), the second with fp16 out.
+cudaError_t launch_tc2_up_e4m3(const void* xq, const float* sx, const int32_t* gather_src,
+                               int gather_k, int64_t gather_rows, const void* w1q, const float* sw1,
+                               void* h, const int32_t* offsets, int G, int N, int Kd,
+                               int64_t rows_cap, int row_part, uint32_t* hdr, int num_sms,
+                               cudaStream_t st) {
+  constexpr int BKE = OpKind<OP_E4M3>::BK;
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + BKE - 1) / BKE, 0,
+           row_part, gather_src, gather_k, gather_rows, sx, sw1};
+  if (gather_src != nullptr)
+    return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_E4M3, true>(xq, w1q, a, num_sms, st);
+  return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_E4M3, false>(xq, w1q, a, num_sms, st);
+}
+
+cudaError_t launch_tc2_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
+                                 void* y_perm, const int32_t* offsets, int G, int N, int Kd,
+                                 int64_t rows_cap, int row_part, uint32_t* hdr, int num_sms,
+                                 cudaStream_t st) {
+  constexpr int BKE = OpKind<OP_E4M3>::BK;
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + BKE - 1) / BKE, 0,
+           row_part, nullptr, 1, 0, sh, sw2};
+  return launch_tc2<256, 6, TC_EPI_F16, OP_E4M3, false>(hq, w2q, a, num_sms, st);
 }
 
 // Second expert Linear on CTA pairs, fp16 in, fp16 out.

@@ -5,7 +5,8 @@ accumulation; h stored in fp16 and quantised per row in turn).
 - moe_quantize_e4m3: codes and scales bit for bit (every step is one correctly rounded
   fp32 operation on both sides);
 - moe_expert_up_e4m3 / moe_expert_down_e4m3: against fp64 products of the oracle's own
-  codes of the same inputs (h and y_perm within one fp16 rounding);
+  codes of the same inputs (h and y_perm within one fp16 rounding), on every GEMM plan,
+  and the plans against each other bit for bit;
 - the whole layer in E4M3 mode against the oracle's E4M3 layer, with the bf16 layers'
   output bound.
 """
@@ -67,6 +68,16 @@ def test_quantize_rows_bounded_on_device():
     assert (codes[10:] == 0x55).all()
 
 
+@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_AUTO],
+                ids=["single", "pair", "split", "auto"])
+def pairing(request):
+    """Run the E4M3 GEMM on the one-CTA kernel, the CTA-pair kernel, the split of the two
+    and the default choice."""
+    N.set_gemm_pairing(request.param)
+    yield request.param
+    N.set_gemm_pairing(N.GEMM_AUTO)
+
+
 def _gen(shape, std, seed, dtype=torch.bfloat16):
     g = torch.Generator(device="cuda")
     g.manual_seed(seed)
@@ -74,9 +85,9 @@ def _gen(shape, std, seed, dtype=torch.bfloat16):
 
 
 @pytest.mark.parametrize("gather", [False, True])
-def test_expert_up_e4m3(gather):
+def test_expert_up_e4m3(gather, pairing):
     offs = [0, 300, 300, 812, 813, 1100]
-    G, rows, d, F, T, K = 5, 1100, 256, 384, 700, 2
+    G, rows, d, F, T, K = 5, 1100, 256, 640, 700, 2
     rows_cap = rows + 16
     cfg = N.make_config(T, d, G, K, F, "bf16", -1)
     ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
@@ -116,9 +127,9 @@ def test_expert_up_e4m3(gather):
     assert (hn[rows:] == 7.0).all()
 
 
-def test_expert_down_e4m3():
+def test_expert_down_e4m3(pairing):
     offs = [0, 129, 129, 700]
-    G, rows, F, d = 3, 700, 512, 256
+    G, rows, F, d = 3, 700, 512, 768
     rows_cap = rows + 8
     cfg = N.make_config(rows, d, G, 1, F, "bf16", -1)
     ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
@@ -145,6 +156,41 @@ def test_expert_down_e4m3():
             * swo[None, gi * d:(gi + 1) * d]
         assert_rounded_to(yn[lo:hi], ref, "f16")
     assert (yn[rows:] == 7.0).all()
+
+
+@pytest.mark.parametrize("fn", ["up", "down"])
+def test_e4m3_plans_agree_bitwise(fn):
+    """The one-CTA kernel, the CTA-pair kernel and their split multiply the same E4M3
+    codes and accumulate the 128-deep k-blocks in the same order: outputs bit for bit."""
+    offs = [0, 300, 812, 813, 1400]
+    G, rows, Kd, Nn = 4, 1400, 512, 768
+    rows_cap = rows + 16
+    cfg = N.make_config(rows, Kd if fn == "up" else Nn, G, 1, Nn if fn == "up" else Kd, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
+    a = _gen((rows_cap, Kd), 1.0, 21, torch.bfloat16 if fn == "up" else torch.float16)
+    w = _gen((G * Nn, Kd), Kd ** -0.5, 22)
+    aq = torch.empty((rows_cap, Kd), dtype=torch.uint8, device="cuda")
+    sa = torch.empty(rows_cap, dtype=torch.float32, device="cuda")
+    wq = torch.empty((G * Nn, Kd), dtype=torch.uint8, device="cuda")
+    sw = torch.empty(G * Nn, dtype=torch.float32, device="cuda")
+    N.quantize_e4m3(a, aq, sa)
+    N.quantize_e4m3(w, wq, sw)
+    outs = []
+    for mode in (N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT):
+        N.set_gemm_pairing(mode)
+        try:
+            out = torch.zeros((rows_cap, Nn), dtype=torch.float16, device="cuda")
+            if fn == "up":
+                N.expert_up_e4m3(cfg, aq, sa, None, off_t, G, rows_cap, wq, sw, out, ws)
+            else:
+                N.expert_down_e4m3(cfg, aq, sa, off_t, G, rows_cap, wq, sw, out, ws)
+        finally:
+            N.set_gemm_pairing(N.GEMM_AUTO)
+        assert N.sync_status(ws) == 0
+        outs.append(out.cpu())
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(outs[0], outs[2])
 
 
 FP8_LAYERS = [

@@ -484,3 +484,33 @@ def test_host_stream_pipeline_matches_eager():
     for i in range(n):
         assert torch.equal(ys[i], refs[i & 1][0]), i
         assert torch.equal(sts[i], refs[i & 1][1]), i
+
+
+def test_split_plan_captured_matches_eager_and_oracle():
+    """A layer whose experts hold whole 256-row tiles plus a remainder (C = 320 -> 256 +
+    64) takes the split plan: the pair kernel and the one-CTA kernel run concurrently,
+    the second on the library's side stream.  Captured in a CUDA graph, it reproduces the
+    eager forward bit for bit, and the eager forward matches the oracle."""
+    wl = Workload("split_case", 2048, 512, 8, 2, 1024, "bf16", 1.25)
+    assert N.capacity(wl.T, wl.E, wl.capacity_factor) == 320
+    inp = make_inputs(wl, "cuda")
+    layer = MoELayer.from_workload(wl, inp)
+    x_np = to_np(inp["x"])
+    _, L32 = O.router_logits(x_np, to_np(inp["w_r"]), None)
+    layer.forward(inp["x"], logits_in=torch.from_numpy(L32).cuda())
+    layer.check_device_status()
+    ref = O.moe_forward(x_np, to_np(inp["w_r"]), None, to_np(inp["w1"]), to_np(inp["w2"]),
+                        wl.K, 320, wl.alpha, logits32=L32)
+    assert np.array_equal(to_np(layer.offsets), ref["offsets"])
+    err, literal = layer_output_error(to_np(layer.y), ref["y"], "bf16")
+    assert err <= TOL["bf16"], (err, literal)
+    layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    y_eager = layer.y.clone()
+    layer.capture(inp["x"])
+    for _ in range(2):
+        layer.y.zero_()
+        layer.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(layer.y, y_eager)
+    layer.check_device_status()
