@@ -410,14 +410,18 @@ static cudaError_t split_streams(SplitStreams** out) {
 }
 
 // SMs given to the pair kernel in the split plan: its share of the rows, weighted by
-// the one-CTA kernel taking ~1.1x as long per row (measured per-tile MMA rates), so that
-// both finish together; an even count (whole pairs), leaving the one-CTA kernel some.
+// the one-CTA kernel taking ~1.25x as long per row, so that both finish together; an even
+// count (whole pairs), leaving the one-CTA kernel some.  Measured on the Mixtral shape
+// (640-row groups: 512 on pairs, 128 on one CTA), GEMM1 / GEMM2 ms by pair SMs: 106
+// 0.496 / 0.482, 110 0.471 / 0.492, 112 0.469 / 0.475, 114 0.466 / 0.491, 116 0.521 /
+// 0.498, 118 0.563 / 0.569; the weighting gives 112.  Past the optimum the one-CTA kernel's
+// share of the tiles finishes last, and the time rises steeply.
 static int split_pair_sms(int64_t cap_per_group, int num_sms) {
   double frac = 0.75;  // groups of unknown size
   if (cap_per_group > 0) {
     const double whole = (double)(cap_per_group / 256 * 256);
     const double rest = (double)(cap_per_group - cap_per_group / 256 * 256);
-    frac = whole / (whole + 1.1 * rest);
+    frac = whole / (whole + 1.25 * rest);
   }
   int sp = ((int)(num_sms * frac)) & ~1;
   if (sp > num_sms - 2) sp = (num_sms - 2) & ~1;

@@ -123,7 +123,7 @@ __device__ __forceinline__ bool epilogue_chunk_t(const uint32_t (&r)[32], int co
     if (tok >= tok_end) break;
     const float v = __uint_as_float(r[j]);
     if (EPI == TC_EPI_GELU_F16 || EPI == TC_EPI_F16) {
-      const float a = EPI == TC_EPI_GELU_F16 ? gelu_exact(v) : v;
+      const float a = EPI == TC_EPI_GELU_F16 ? gelu(v) : v;
       bad |= !(fabsf(a) <= 65504.f);
       ((__half*)args.out)[(size_t)tok * args.ldo + col] = __float2half_rn(a);
     } else {

@@ -113,6 +113,44 @@ def test_tensor_core_router(T, E, d, bias):
     assert np.max(np.abs(Lg - L64) / (1.0 + np.abs(L64))) <= 1e-5
 
 
+def _bf16_values(lo, hi):
+    """Every finite bf16 value in [lo, hi], as float32."""
+    bits = np.arange(1 << 16, dtype=np.uint32) << 16
+    v = bits.view(np.float32)
+    v = v[np.isfinite(v) & (v >= lo) & (v <= hi)]
+    return np.unique(v)
+
+
+def test_gelu_epilogue_accuracy_every_bf16_input(pairing):
+    """The GEMM1 epilogue's GELU on every bf16 value in [-16, 16], one value per row: A row r
+    is (v_r, 0, ..., 0) and every W1 row is (1, 0, ..., 0), so the accumulator is v_r
+    exactly and h[r, n] = fp16(GELU(v_r)).  Bound: half an fp16 ulp of the exact GELU (the
+    storage rounding) plus 4e-7 for the evaluation (the approximation of the normal tail
+    is within 7.5e-8 of Phi; in fp32 the epilogue's GELU is within 3.4e-7 of the exact)."""
+    from scipy.special import erf
+    v = _bf16_values(-16.0, 16.0)
+    rows, Kd, Nn = len(v), 64, 256
+    cfg = N.make_config(rows, Kd, 1, 1, Nn, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    a = torch.zeros((rows, Kd), dtype=torch.bfloat16, device="cuda")
+    a[:, 0] = torch.from_numpy(v).to(torch.bfloat16).cuda()
+    w = torch.zeros((1, Nn, Kd), dtype=torch.bfloat16, device="cuda")
+    w[:, :, 0] = 1.0
+    h = torch.zeros((rows, Nn), dtype=torch.float16, device="cuda")
+    off = torch.tensor([0, rows], dtype=torch.int32, device="cuda")
+    N.expert_up(cfg, a, off, 1, rows, w, h, ws)
+    assert N.sync_status(ws) == 0
+    hn = h.float().cpu().numpy().astype(np.float64)
+    assert (hn == hn[:, :1]).all()
+    vd = v.astype(np.float64)
+    exact = 0.5 * vd * (1.0 + erf(vd / np.sqrt(2.0)))
+    ulp = np.spacing(np.abs(exact).astype(np.float16)).astype(np.float64)
+    err = np.abs(hn[:, 0] - exact)
+    excess = err - (0.5 * ulp + 4e-7)
+    i = int(np.argmax(excess))
+    assert excess[i] <= 0, (v[i], hn[i, 0], exact[i])
+
+
 def test_f16_conversion_exact_and_range_error():
     src = _gen((4096,), 0.05, 8, torch.bfloat16)
     src[7] = 1e-6   # below 2^-17: rounds at 2^-25
