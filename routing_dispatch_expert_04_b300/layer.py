@@ -55,6 +55,10 @@ class MoELayer:
         dev, dt = self.device, self.dtype
         i32, f32 = torch.int32, torch.float32
         self.ws = torch.zeros(N.workspace_size(self.cfg), dtype=torch.uint8, device=dev)
+        # the shared expert runs beside routing and the routed experts on the side stream,
+        # and calls that can run concurrently need separate workspaces
+        self.ws_s = (torch.zeros(N.workspace_size(self.cfg), dtype=torch.uint8, device=dev)
+                     if w1s is not None else None)
         self.logits = torch.empty((T, E), dtype=f32, device=dev)
         self.ids = torch.empty((T, K), dtype=i32, device=dev)
         self.w = torch.empty((T, K), dtype=f32, device=dev)
@@ -197,14 +201,15 @@ class MoELayer:
         if self.experts == "e4m3":
             N.quantize_e4m3(x, self.xsq, self.xs_sc, None, stream)
             N.expert_up_e4m3(self.cfg, self.xsq, self.xs_sc, None, self.shared_offsets, 1, self.T,
-                             self.w1sq, self.w1s_sc, self.h_s, self.ws, stream)
+                             self.w1sq, self.w1s_sc, self.h_s, self.ws_s, stream)
             N.quantize_e4m3(self.h_s, self.hsq, self.hs_sc, None, stream)
             N.expert_down_e4m3(self.cfg, self.hsq, self.hs_sc, self.shared_offsets, 1, self.T,
-                               self.w2sq, self.w2s_sc, self.y_s, self.ws, stream)
+                               self.w2sq, self.w2s_sc, self.y_s, self.ws_s, stream)
             return
-        N.expert_up(self.cfg, x, self.shared_offsets, 1, self.T, self.w1s, self.h_s, self.ws, stream)
-        N.expert_down(self.cfg, self.h_s, self.shared_offsets, 1, self.T, self.w2s, self.y_s, self.ws,
-                      stream)
+        N.expert_up(self.cfg, x, self.shared_offsets, 1, self.T, self.w1s, self.h_s, self.ws_s,
+                    stream)
+        N.expert_down(self.cfg, self.h_s, self.shared_offsets, 1, self.T, self.w2s, self.y_s,
+                      self.ws_s, stream)
 
     def combine(self, stream=None, y=None):
         N.combine(self.cfg, self.y_perm, self.slot, self.w, self.y_s if self.shared else None,
@@ -321,9 +326,12 @@ class MoELayer:
         return y_host
 
     def check_device_status(self):
-        st = N.sync_status(self.ws)
-        if st != 0:
-            raise N.MoeError("moe_sync_status", st)
+        for ws in (self.ws, self.ws_s):
+            if ws is None:
+                continue
+            st = N.sync_status(ws)
+            if st != 0:
+                raise N.MoeError("moe_sync_status", st)
 
 
 class HostStream:

@@ -4,14 +4,20 @@
         [--tokens T] [--iters N] [--warmup W]
 
 Stages: ``route`` (router Linear + softmax/top-K), ``dispatch`` (histogram/scan/capacity
-+ row permutation), ``combine`` (weighted gather back to token order).  The routing that
-feeds dispatch and combine is computed by the library from the workload's seeded
-inputs; the expert outputs that combine reads are seeded N(0, 1) values (combine's cost
-does not depend on them).  No expert weights are allocated, so a stage of a large
-workload fits in a few GB of device memory -- the size a profiler capture should use.
++ row permutation), ``combine`` (weighted gather back to token order), ``expert_up`` and
+``expert_down`` (the two grouped expert GEMMs, ``--experts bf16|e4m3``).  The routing that
+feeds the later stages is computed by the library from the workload's seeded inputs; the
+rows the GEMMs and the combine read are seeded values of the layer's scale (their cost
+does not depend on them).  Only the stage's own weights are allocated (none for routing,
+dispatch and combine), so most stages fit in a few GB of device memory -- the size a
+profiler capture should use.
 
 L2 is flushed (a 512 MiB device write) before every timed launch.  Prints one JSON line
-with the median time, the stage's algorithmic bytes and the achieved GB/s.
+with the median time, the stage's algorithmic bytes and the achieved GB/s (and TFLOP/s
+for the GEMMs).  With ``--profile-range`` one more launch of the stage runs between
+cudaProfilerStart and cudaProfilerStop, for a profiler's range replay: the stage's kernels
+then run as in the layer (the split plan's two GEMM kernels concurrently), and the
+counters cover the whole stage.
 """
 
 from __future__ import annotations
@@ -28,9 +34,14 @@ from .workloads import WORKLOADS, make_inputs
 L2_FLUSH_BYTES = 512 << 20
 
 
-def stage_bytes(stage, wl, T, R, t_active, b):
+def stage_bytes(stage, wl, T, R, t_active, b, experts="bf16"):
     """Bytes the stage must move at least (inputs read once, outputs written once)."""
     A = T * wl.K
+    if stage in ("expert_up", "expert_down"):
+        wb = 1 if experts == "e4m3" else 2          # weight element bytes
+        ab = 1 if experts == "e4m3" else (b if stage == "expert_up" else 2)
+        n_in, n_out = (wl.d, wl.F) if stage == "expert_up" else (wl.F, wl.d)
+        return wl.E * wl.F * wl.d * wb + R * n_in * ab + R * n_out * 2
     if stage == "route":
         return T * wl.d * b + wl.E * wl.d * b + T * wl.E * 4 * 2 + A * 8
     if stage == "dispatch":
@@ -43,13 +54,22 @@ def stage_bytes(stage, wl, T, R, t_active, b):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--stage", required=True, choices=["route", "dispatch", "combine"])
+    ap.add_argument("--stage", required=True,
+                    choices=["route", "dispatch", "combine", "expert_up", "expert_down"])
+    ap.add_argument("--experts", choices=["bf16", "e4m3"], default="bf16",
+                    help="operand format of the expert GEMM stages")
+    ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t"], default="auto",
+                    help="expert-GEMM plan (moe_set_gemm_pairing) for the GEMM stages")
+    ap.add_argument("--profile-range", action="store_true",
+                    help="run one more launch between cudaProfilerStart/Stop")
     ap.add_argument("--workload", default="long", choices=sorted(WORKLOADS))
     ap.add_argument("--tokens", type=int, default=0, help="override the token count T")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args()
 
+    N.set_gemm_pairing({"auto": N.GEMM_AUTO, "single": N.GEMM_SINGLE, "pair": N.GEMM_PAIR,
+                        "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T}[args.gemm])
     wl = WORKLOADS[args.workload]
     if args.tokens > 0:
         wl = wl.scaled(args.tokens)
@@ -86,7 +106,7 @@ def main():
 
         def run():
             N.dispatch(cfg, x, ids, counts, offsets, slot, src, x_perm, ws)
-    else:
+    elif args.stage == "combine":
         g = torch.Generator(device=dev)
         g.manual_seed(1)
         y_perm = torch.randn((rows_cap, d), generator=g, device=dev, dtype=f32)
@@ -96,6 +116,9 @@ def main():
 
         def run():
             N.combine(cfg, y_perm, slot, w, None, y)
+    else:
+        run = _gemm_stage(args.stage, args.experts, wl, cfg, x, ids, counts, offsets, slot,
+                          src, ws, rows_cap, dev)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -113,16 +136,68 @@ def main():
         z.record(stream)
         z.synchronize()
         ms.append(a.elapsed_time(z))
+    if args.profile_range:
+        flush.zero_()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStart()
+        run()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
     st = N.sync_status(ws)
     if st != 0:
         raise N.MoeError(args.stage, st)
     b = 2 if wl.dtype == "bf16" else 4
-    nbytes = stage_bytes(args.stage, wl, T, R, t_active, b)
+    nbytes = stage_bytes(args.stage, wl, T, R, t_active, b, args.experts)
     med = statistics.median(ms)
-    print(json.dumps({"stage": args.stage, "workload": wl.name, "T": T, "rows_kept": R,
-                      "tokens_with_kept_rows": t_active, "ms_median": round(med, 5),
-                      "bytes": nbytes, "gbs": round(nbytes / (med * 1e-3) / 1e9, 1),
-                      "iters": args.iters}), flush=True)
+    line = {"stage": args.stage, "workload": wl.name, "T": T, "rows_kept": R,
+            "tokens_with_kept_rows": t_active, "ms_median": round(med, 5),
+            "bytes": nbytes, "gbs": round(nbytes / (med * 1e-3) / 1e9, 1), "iters": args.iters}
+    if args.stage in ("expert_up", "expert_down"):
+        flops = 2.0 * R * wl.d * wl.F
+        line.update({"experts": args.experts, "gemm": args.gemm, "flops": flops,
+                     "tflops": round(flops / (med * 1e-3) / 1e12, 1)})
+    print(json.dumps(line), flush=True)
+
+
+def _gemm_stage(stage, experts, wl, cfg, x, ids, counts, offsets, slot, src, ws, rows_cap, dev):
+    """Buffers and launch of one expert-GEMM stage over the workload's kept rows: A is the
+    dispatched token rows (expert_up) or seeded fp16 rows of the scale of h (expert_down);
+    the weights are seeded N(0, 1/fan_in) values (W2 in fp16, as the layer stores it for
+    bf16 layers).  E4M3 stages quantise A and the weights once, outside the timed launch."""
+    E, d, F = wl.E, wl.d, wl.F
+    g = torch.Generator(device=dev)
+    g.manual_seed(2)
+    if stage == "expert_up":
+        a = torch.empty((rows_cap, d), dtype=x.dtype, device=dev)
+        N.dispatch(cfg, x, ids, counts, offsets, slot, src, a, ws)
+        w = (torch.randn((E, F, d), generator=g, device=dev) * d ** -0.5).to(x.dtype)
+        out = torch.empty((rows_cap, F), dtype=torch.float16, device=dev)
+        n_in, n_out = d, F
+    else:
+        a = (torch.randn((rows_cap, F), generator=g, device=dev) * 0.5).half()
+        w = (torch.randn((E, d, F), generator=g, device=dev) * F ** -0.5).half()
+        out = torch.empty((rows_cap, d), dtype=torch.float16, device=dev)
+        n_in, n_out = F, d
+    if experts == "bf16":
+        fn = N.expert_up if stage == "expert_up" else N.expert_down
+
+        def run():
+            fn(cfg, a, offsets, E, rows_cap, w, out, ws)
+        return run
+    aq = torch.empty((rows_cap, n_in), dtype=torch.uint8, device=dev)
+    sa = torch.empty(rows_cap, dtype=torch.float32, device=dev)
+    wq = torch.empty((E * n_out, n_in), dtype=torch.uint8, device=dev)
+    sw = torch.empty(E * n_out, dtype=torch.float32, device=dev)
+    N.quantize_e4m3(a, aq, sa)
+    N.quantize_e4m3(w.reshape(E * n_out, n_in), wq, sw)
+    del w
+    if stage == "expert_up":
+        def run():
+            N.expert_up_e4m3(cfg, aq, sa, None, offsets, E, rows_cap, wq, sw, out, ws)
+    else:
+        def run():
+            N.expert_down_e4m3(cfg, aq, sa, offsets, E, rows_cap, wq, sw, out, ws)
+    return run
 
 
 if __name__ == "__main__":

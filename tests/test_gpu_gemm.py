@@ -48,6 +48,8 @@ CASES = [
     ("groups_empty_and_single_row", [0, 0, 130, 131, 400, 520], 136, 384),
     ("many_groups", list(np.cumsum([0] + [37 * (i % 5) for i in range(40)])), 256, 512),
     ("pair_tiles_ragged", [0, 600, 600, 856, 1111, 1367], 1024, 512),
+    # more tiles than SMs for every plan, ragged groups
+    ("many_tiles_ragged", list(np.cumsum([0, 700, 512, 0, 1000, 640, 383, 900, 250])), 512, 2048),
 ]
 
 
@@ -170,7 +172,7 @@ def test_f16_conversion_exact_and_range_error():
 
 @pytest.mark.parametrize("fn", ["up", "down"])
 def test_single_and_pair_kernels_agree_bitwise(fn):
-    """Both kernels multiply the same operands and accumulate the 64-deep k-blocks in the
+    """All kernels multiply the same operands and accumulate the 64-deep k-blocks in the
     same order; their outputs are compared bit for bit."""
     offs = [0, 300, 812, 813, 1400]
     G, rows, Kd, Nn = 4, 1400, 512, 768
