@@ -272,12 +272,34 @@ __device__ __forceinline__ bool f16x2_out_of_range(__half2 amax) {
 
 // E4M3 operands: the accumulator holds sum_k qa*qb; the real product is that times the
 // row's A scale and the column's B scale.
+// (r * sa) * sb for each column, rounded twice in that order; a whole aligned chunk loads
+// the column scales as four-float vectors and multiplies two columns per instruction.
 __device__ __forceinline__ void apply_scales(uint32_t (&r)[32], float sa, const float* sb_row,
                                              int col0, int N) {
+  const float* sb = sb_row + col0;
+  if (col0 + 32 <= N && ((uintptr_t)sb & 15u) == 0) {
+    const uint64_t sa2 = f32x2_splat(sa);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const float4 b = __ldg(reinterpret_cast<const float4*>(sb) + v);
+      float x0, x1, x2, x3;
+      f32x2_unpack(f32x2_mul(f32x2_mul(f32x2_pack(__uint_as_float(r[4 * v]),
+                                                  __uint_as_float(r[4 * v + 1])), sa2),
+                             f32x2_pack(b.x, b.y)), x0, x1);
+      f32x2_unpack(f32x2_mul(f32x2_mul(f32x2_pack(__uint_as_float(r[4 * v + 2]),
+                                                  __uint_as_float(r[4 * v + 3])), sa2),
+                             f32x2_pack(b.z, b.w)), x2, x3);
+      r[4 * v] = __float_as_uint(x0);
+      r[4 * v + 1] = __float_as_uint(x1);
+      r[4 * v + 2] = __float_as_uint(x2);
+      r[4 * v + 3] = __float_as_uint(x3);
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const float sb = (col0 + i < N) ? sb_row[col0 + i] : 0.f;
-    r[i] = __float_as_uint(__uint_as_float(r[i]) * sa * sb);
+    const float s = (col0 + i < N) ? sb[i] : 0.f;
+    r[i] = __float_as_uint(__fmul_rn(__fmul_rn(__uint_as_float(r[i]), sa), s));
   }
 }
 
