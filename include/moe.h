@@ -298,15 +298,14 @@ moe_status_t moe_sync_status(void* ws, void* stream);
  *   MOE_GEMM_PAIR_T two CTAs per tile computing the transpose: 256 weight rows (output
  *                   columns) on the MMA's M side and up to 256 of a group's rows on its
  *                   N side, sized to the group (rounded up to 32), so no group is padded
- *                   to 256 rows (16-bit operands only: row-gathered calls take
- *                   MOE_GEMM_PAIR instead, and so do E4M3 calls);
+ *                   to 256 rows (row-gathered calls take MOE_GEMM_PAIR instead);
  *   MOE_GEMM_AUTO   (default) pairs when the 256-row padding is at most 5% of the rows
  *                   (judged from the capacity), the split when the capacity reaches 256
- *                   rows, transposed pairs when the groups have no capacity bound (one
- *                   CTA for E4M3 calls), one CTA otherwise (all pair plans need the
- *                   output width to be a multiple of 256).  The E4M3 calls take the same
- *                   plans with E4M3 operands, except that AUTO keeps them on one CTA
- *                   where it would pick pairs for groups under 512 rows.
+ *                   rows, transposed pairs when the groups have no capacity bound, one
+ *                   CTA otherwise (all pair plans need the output width to be a
+ *                   multiple of 256).  The E4M3 calls take the same plans with E4M3
+ *                   operands, except that AUTO keeps them on one CTA where it would pick
+ *                   pairs for groups under 512 rows or transposed pairs.
  * Every choice sums the same products in the same order, so results are identical.
  * Returns MOE_ERR_INVALID for any other value.  Calls already enqueued are unaffected. */
 typedef enum {

@@ -527,18 +527,28 @@ cudaError_t launch_tc2_down_e4m3(const void* hq, const float* sh, const void* w2
                                  int64_t rows_cap, int row_part, uint32_t* hdr, int num_sms,
                                  cudaStream_t st);
 
-// Plan for the E4M3 GEMMs.  The transposed pairs take 16-bit operands only, so groups of
-// unknown size run on one CTA per tile (or on pairs when pairs were asked for).  E4M3
-// halves the weight bytes but doubles the tensor rate, so small groups stay HBM-bound
-// (2 x rows flops per weight byte against a ridge near 550): there the pair's halved
-// shared-memory traffic buys nothing and its longer tiles lose to the one-CTA kernel
-// (measured on B300: 192-row groups 0.111 vs 0.123 ms per GEMM; 8192-row groups pairs
-// 2.62 vs 2.68 ms).  AUTO takes pairs for E4M3 only from 512 rows per group on.
+cudaError_t launch_tc2t_up_e4m3(const void* xq, const float* sx, const void* w1q, const float* sw1,
+                                void* h, const int32_t* offsets, int G, int N, int Kd,
+                                int64_t rows_cap, uint32_t* hdr, int num_sms, cudaStream_t st);
+cudaError_t launch_tc2t_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
+                                  void* y_perm, const int32_t* offsets, int G, int N, int Kd,
+                                  int64_t rows_cap, uint32_t* hdr, int num_sms, cudaStream_t st);
+
+// Plan for the E4M3 GEMMs: as for 16-bit operands, except that E4M3 halves the weight
+// bytes but doubles the tensor rate, so small groups stay HBM-bound (2 x rows flops per
+// weight byte against a ridge near 550): there the pair's halved shared-memory traffic
+// buys nothing and its longer tiles lose to the one-CTA kernel (measured on B300:
+// 192-row groups 0.111 vs 0.123 ms per GEMM; 8192-row groups pairs 2.62 vs 2.68 ms).
+// AUTO takes pairs for E4M3 only from 512 rows per group on.  Nor does AUTO take the
+// transposed pairs for E4M3: with half as many k-blocks per tile their per-element
+// transposed stores dominate (DeepSeek-V3 shape, B300: GEMM2 2.22 vs 1.22 ms on one CTA
+// per tile, GEMM1 1.57 vs 1.45 ms).
 static int gemm_plan_e4m3(int mode, int64_t rows_cap, int G, int64_t cap_per_group, int N) {
   const int plan = gemm_plan(mode, rows_cap, G, cap_per_group, N);
-  if (plan == PLAN_PAIR && mode == MOE_GEMM_AUTO && cap_per_group < 512) return PLAN_SINGLE;
-  if (plan != PLAN_PAIR_T) return plan;
-  return mode == MOE_GEMM_PAIR_T ? PLAN_PAIR : PLAN_SINGLE;
+  if (mode != MOE_GEMM_AUTO) return plan;
+  if (plan == PLAN_PAIR && cap_per_group < 512) return PLAN_SINGLE;
+  if (plan == PLAN_PAIR_T) return PLAN_SINGLE;
+  return plan;
 }
 
 // First expert Linear on E4M3 operands (codes + per-row scales), GELU fused, fp16 out:
@@ -549,7 +559,10 @@ cudaError_t launch_tc_up_e4m3(const void* xq, const float* sx, const int32_t* ga
                               void* h, const int32_t* offsets, int G, int N, int Kd,
                               int64_t rows_cap, int64_t cap_per_group, int pair_mode,
                               uint32_t* hdr, int num_sms, cudaStream_t st) {
-  const int plan = gemm_plan_e4m3(pair_mode, rows_cap, G, cap_per_group, N);
+  int plan = gemm_plan_e4m3(pair_mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_PAIR_T && gather_src != nullptr) plan = PLAN_PAIR;  // gathers: rows on M
+  if (plan == PLAN_PAIR_T)
+    return launch_tc2t_up_e4m3(xq, sx, w1q, sw1, h, offsets, G, N, Kd, rows_cap, hdr, num_sms, st);
   if (plan == PLAN_PAIR)
     return launch_tc2_up_e4m3(xq, sx, gather_src, gather_k, gather_rows, w1q, sw1, h, offsets, G,
                               N, Kd, rows_cap, TC_ROWS_ALL, hdr, num_sms, st);
@@ -585,6 +598,9 @@ cudaError_t launch_tc_down_e4m3(const void* hq, const float* sh, const void* w2q
                                 int64_t rows_cap, int64_t cap_per_group, int pair_mode,
                                 uint32_t* hdr, int num_sms, cudaStream_t st) {
   const int plan = gemm_plan_e4m3(pair_mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_PAIR_T)
+    return launch_tc2t_down_e4m3(hq, sh, w2q, sw2, y_perm, offsets, G, N, Kd, rows_cap, hdr,
+                                 num_sms, st);
   if (plan == PLAN_PAIR)
     return launch_tc2_down_e4m3(hq, sh, w2q, sw2, y_perm, offsets, G, N, Kd, rows_cap,
                                 TC_ROWS_ALL, hdr, num_sms, st);

@@ -112,16 +112,19 @@ __device__ __forceinline__ TTile decode_ttile(int t, int G, const GroupTable* ta
   return ti;
 }
 
-// Epilogue of the transposed tile: r[j] = C[tok0 + c0 + j, col] for j < 32.
-template <int EPI>
+// Epilogue of the transposed tile: r[j] = C[tok0 + c0 + j, col] for j < 32.  E4M3
+// operands: the accumulator times the token row's scale, then the column's scale (the
+// order of the other kernels' epilogues, so every plan stores the same values).
+template <int EPI, int KIND>
 __device__ __forceinline__ bool epilogue_chunk_t(const uint32_t (&r)[32], int col, int tok_first,
-                                                 int tok_end, const TcArgs& args) {
+                                                 int tok_end, const TcArgs& args, float sb) {
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int tok = tok_first + j;
     if (tok >= tok_end) break;
-    const float v = __uint_as_float(r[j]);
+    float v = __uint_as_float(r[j]);
+    if (KIND == OP_E4M3) v = __fmul_rn(__fmul_rn(v, args.a_scale[tok]), sb);
     if (EPI == TC_EPI_GELU_F16 || EPI == TC_EPI_F16) {
       const float a = EPI == TC_EPI_GELU_F16 ? gelu(v) : v;
       bad |= !(fabsf(a) <= 65504.f);
@@ -140,7 +143,6 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
                          const __grid_constant__ CUtensorMap tmap_x32,
                          const __grid_constant__ CUtensorMap tmap_w, const TcArgs args) {
   using Lay = Tc2tLayout<STAGES>;
-  static_assert(KIND != OP_E4M3, "E4M3 operands run on the one-CTA kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + Lay::BAR_OFF);
@@ -262,8 +264,12 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
           const uint32_t x_addr = smem_u32(smem + Lay::X_OFF + s * Lay::X_BYTES);
 #pragma unroll
           for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
-            mma_f16_pair(d_tmem, sdesc_sw128(w_addr + k * 32), sdesc_sw128(x_addr + k * 32), idesc,
-                         (kb != 0 || k != 0) ? 1u : 0u);
+            if (KIND == OP_E4M3)
+              mma_e4m3_pair(d_tmem, sdesc_sw128(w_addr + k * 32), sdesc_sw128(x_addr + k * 32),
+                            idesc, (kb != 0 || k != 0) ? 1u : 0u);
+            else
+              mma_f16_pair(d_tmem, sdesc_sw128(w_addr + k * 32), sdesc_sw128(x_addr + k * 32),
+                           idesc, (kb != 0 || k != 0) ? 1u : 0u);
           }
           mma_commit_pair_mc(&empty[s], (uint16_t)3);
           if (++s == STAGES) {
@@ -292,13 +298,14 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
       const int col = ti.w0 + wl;
       const bool valid = col < args.N;
       const int tok_end = ti.tok0 + ti.ntok;
+      const float sb = (KIND == OP_E4M3 && valid) ? args.b_scale[(size_t)ti.g * args.N + col] : 0.f;
 #pragma unroll 1
       for (int c = 0; c < ti.ninst; c += 32) {  // warp-uniform
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * T2T_TILE + c, r);
         tmem_ld_wait();
         if (!valid) continue;
-        if (epilogue_chunk_t<EPI>(r, col, ti.tok0 + c, tok_end, args))
+        if (epilogue_chunk_t<EPI, KIND>(r, col, ti.tok0 + c, tok_end, args, sb))
           raise_error(args.hdr, DEV_ERR_RANGE);
       }
       tc_fence_before();
@@ -359,6 +366,24 @@ cudaError_t launch_tc2t_down(const void* h, const void* w2h, void* y_perm, const
                              cudaStream_t st) {
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, 0, 0, TC_ROWS_ALL};
   return launch_tc2t<6, TC_EPI_F16, OP_F16>(h, w2h, a, num_sms, st);
+}
+
+// The same two Linears on E4M3 operands (codes + per-row scales of the packed rows and of
+// the stacked weight rows, applied in the epilogue).
+cudaError_t launch_tc2t_up_e4m3(const void* xq, const float* sx, const void* w1q, const float* sw1,
+                                void* h, const int32_t* offsets, int G, int N, int Kd,
+                                int64_t rows_cap, uint32_t* hdr, int num_sms, cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, 0, 0, TC_ROWS_ALL,
+           nullptr, 1, 0, sx, sw1};
+  return launch_tc2t<6, TC_EPI_GELU_F16, OP_E4M3>(xq, w1q, a, num_sms, st);
+}
+
+cudaError_t launch_tc2t_down_e4m3(const void* hq, const float* sh, const void* w2q, const float* sw2,
+                                  void* y_perm, const int32_t* offsets, int G, int N, int Kd,
+                                  int64_t rows_cap, uint32_t* hdr, int num_sms, cudaStream_t st) {
+  TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, 0, 0, TC_ROWS_ALL,
+           nullptr, 1, 0, sh, sw2};
+  return launch_tc2t<6, TC_EPI_F16, OP_E4M3>(hq, w2q, a, num_sms, st);
 }
 
 }  // namespace moe

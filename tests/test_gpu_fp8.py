@@ -68,11 +68,11 @@ def test_quantize_rows_bounded_on_device():
     assert (codes[10:] == 0x55).all()
 
 
-@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_AUTO],
-                ids=["single", "pair", "split", "auto"])
+@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T, N.GEMM_AUTO],
+                ids=["single", "pair", "split", "pair_t", "auto"])
 def pairing(request):
-    """Run the E4M3 GEMM on the one-CTA kernel, the CTA-pair kernel, the split of the two
-    and the default choice."""
+    """Run the E4M3 GEMM on the one-CTA kernel, the CTA-pair kernel, the split of the two,
+    the transposed pair kernel and the default choice."""
     N.set_gemm_pairing(request.param)
     yield request.param
     N.set_gemm_pairing(N.GEMM_AUTO)
@@ -160,8 +160,9 @@ def test_expert_down_e4m3(pairing):
 
 @pytest.mark.parametrize("fn", ["up", "down"])
 def test_e4m3_plans_agree_bitwise(fn):
-    """The one-CTA kernel, the CTA-pair kernel and their split multiply the same E4M3
-    codes and accumulate the 128-deep k-blocks in the same order: outputs bit for bit."""
+    """The one-CTA kernel, the CTA-pair kernel, their split and the transposed pairs
+    multiply the same E4M3 codes and accumulate the 128-deep k-blocks in the same order:
+    outputs bit for bit."""
     offs = [0, 300, 812, 813, 1400]
     G, rows, Kd, Nn = 4, 1400, 512, 768
     rows_cap = rows + 16
@@ -177,7 +178,7 @@ def test_e4m3_plans_agree_bitwise(fn):
     N.quantize_e4m3(a, aq, sa)
     N.quantize_e4m3(w, wq, sw)
     outs = []
-    for mode in (N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT):
+    for mode in (N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T):
         N.set_gemm_pairing(mode)
         try:
             out = torch.zeros((rows_cap, Nn), dtype=torch.float16, device="cuda")
@@ -191,6 +192,7 @@ def test_e4m3_plans_agree_bitwise(fn):
         outs.append(out.cpu())
     assert torch.equal(outs[0], outs[1])
     assert torch.equal(outs[0], outs[2])
+    assert torch.equal(outs[0], outs[3])
 
 
 FP8_LAYERS = [
