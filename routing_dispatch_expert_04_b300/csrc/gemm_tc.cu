@@ -540,9 +540,9 @@ cudaError_t launch_tc2t_down_e4m3(const void* hq, const float* sh, const void* w
 // buys nothing and its longer tiles lose to the one-CTA kernel (measured on B300:
 // 192-row groups 0.111 vs 0.123 ms per GEMM; 8192-row groups pairs 2.62 vs 2.68 ms).
 // AUTO takes pairs for E4M3 only from 512 rows per group on.  Nor does AUTO take the
-// transposed pairs for E4M3: with half as many k-blocks per tile their per-element
-// transposed stores dominate (DeepSeek-V3 shape, B300: GEMM2 2.22 vs 1.22 ms on one CTA
-// per tile, GEMM1 1.57 vs 1.45 ms).
+// transposed pairs for E4M3: with half as many k-blocks per tile their transposed
+// epilogue weighs more (DeepSeek-V3 shape, B300: GEMM2 1.71 vs 1.26 ms on one CTA per
+// tile; GEMM1 1.44 vs 1.49 ms).
 static int gemm_plan_e4m3(int mode, int64_t rows_cap, int G, int64_t cap_per_group, int N) {
   const int plan = gemm_plan(mode, rows_cap, G, cap_per_group, N);
   if (mode != MOE_GEMM_AUTO) return plan;

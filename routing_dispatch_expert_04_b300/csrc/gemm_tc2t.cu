@@ -41,7 +41,9 @@ struct Tc2tLayout {
   static constexpr int NBAR = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], done
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int GRP_OFF = MISC_OFF + 16;
-  static constexpr int TOTAL = GRP_OFF + (int)sizeof(GroupTable);
+  static constexpr int EPI_OFF = (GRP_OFF + (int)sizeof(GroupTable) + 15) / 16 * 16;
+  static constexpr int EPI_BYTES = 32 * 32 * 2;  // per epilogue warp: 32 tokens x 32 columns, fp16
+  static constexpr int TOTAL = EPI_OFF + 4 * EPI_BYTES;
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * T2T_TILE;
 };
@@ -131,6 +133,46 @@ __device__ __forceinline__ bool epilogue_chunk_t(const uint32_t (&r)[32], int co
       ((__half*)args.out)[(size_t)tok * args.ldo + col] = __float2half_rn(a);
     } else {
       ((float*)args.out)[(size_t)tok * args.ldo + col] = v;
+    }
+  }
+  return bad;
+}
+
+// 16-bit outputs of the transposed tile: lane l holds column colbase + l of 32 tokens.
+// The warp's 32 x 32 block goes through its shared-memory buffer (token-major), so that
+// each lane then stores 16 contiguous bytes of one token row (four 16-byte stores per lane
+// instead of 32 two-byte ones).  Same values and range test as epilogue_chunk_t.
+template <int EPI, int KIND>
+__device__ __forceinline__ bool epilogue_chunk_t16(const uint32_t (&r)[32], int colbase, int lane,
+                                                   int tok_first, int tok_end, const TcArgs& args,
+                                                   float sb, __half* sbuf) {
+  const bool valid = colbase + lane < args.N;
+  float sa_l = 0.f;  // E4M3: the scale of token tok_first + lane
+  if (KIND == OP_E4M3 && tok_first + lane < tok_end) sa_l = args.a_scale[tok_first + lane];
+  bool bad = false;
+  __syncwarp();  // the previous chunk's reads of the buffer are done
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float a = __uint_as_float(r[j]), b = __uint_as_float(r[j + 1]);
+    if (KIND == OP_E4M3) {
+      a = __fmul_rn(__fmul_rn(a, __shfl_sync(0xffffffffu, sa_l, j)), sb);
+      b = __fmul_rn(__fmul_rn(b, __shfl_sync(0xffffffffu, sa_l, j + 1)), sb);
+    }
+    if (EPI == TC_EPI_GELU_F16) gelu2(a, b, a, b);
+    bad |= valid && ((tok_first + j < tok_end && !(fabsf(a) <= 65504.f)) ||
+                     (tok_first + j + 1 < tok_end && !(fabsf(b) <= 65504.f)));
+    sbuf[j * 32 + lane] = __float2half_rn(a);
+    sbuf[(j + 1) * 32 + lane] = __float2half_rn(b);
+  }
+  __syncwarp();
+  const int cg = (lane & 3) * 8;  // this lane's 8 columns of a token row
+  if (colbase + cg < args.N) {    // N is a multiple of 8: a group is all in or all out
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = (lane >> 2) + 8 * i;
+      if (tok_first + row < tok_end)
+        st_v4((__half*)args.out + (size_t)(tok_first + row) * args.ldo + colbase + cg,
+              *reinterpret_cast<const uint4*>(sbuf + row * 32 + cg));
     }
   }
   return bad;
@@ -290,6 +332,7 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int wl = (int)rank * T2T_CTA_ROWS + q * 32 + lane;  // weight row within the tile
+    __half* epi_buf = (__half*)(smem + Lay::EPI_OFF + (warp - 2) * Lay::EPI_BYTES);
     uint32_t acc = 0, aph = 0;
     for (int t = cluster; t < total; t += n_clusters) {
       const TTile ti = decode_ttile(t, G, tab);
@@ -304,6 +347,12 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * T2T_TILE + c, r);
         tmem_ld_wait();
+        if (EPI == TC_EPI_GELU_F16 || EPI == TC_EPI_F16) {  // whole warp, staged stores
+          if (epilogue_chunk_t16<EPI, KIND>(r, col - lane, lane, ti.tok0 + c, tok_end, args, sb,
+                                             epi_buf))
+            raise_error(args.hdr, DEV_ERR_RANGE);
+          continue;
+        }
         if (!valid) continue;
         if (epilogue_chunk_t<EPI, KIND>(r, col, ti.tok0 + c, tok_end, args, sb))
           raise_error(args.hdr, DEV_ERR_RANGE);
