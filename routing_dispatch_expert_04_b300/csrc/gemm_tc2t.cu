@@ -14,9 +14,9 @@
 //     each CTA loads its half of the tile with the smallest of three boxes (128, 64 or
 //     32 rows) that covers it, so the bytes staged follow the tile;
 //   - each CTA's TMEM holds its 128 weight rows x the tile's tokens, and the epilogue
-//     writes the transpose: lane l of a warp owns output column n and stores the 32
-//     tokens of a chunk one by one, so a warp store covers 32 consecutive columns of one
-//     output row (64 B of fp16, 128 B of fp32).
+//     writes the transpose: lane l of a warp owns output column n of a chunk of 32
+//     tokens; for fp16 outputs the warp's 32 x 32 block goes through a shared-memory
+//     buffer, token-major, and each lane then stores 16 contiguous bytes of a token row.
 // Pipeline, barriers, bounded waits and teardown as in gemm_tc2.cu: warp 0 TMA producer,
 // warp 1 TMEM owner + MMA issuer (even CTA), warps 2..5 epilogue; both CTAs' copies
 // signal the even CTA's "full" barrier, its commits arrive on both CTAs' "empty" and
