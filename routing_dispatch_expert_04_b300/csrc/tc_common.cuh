@@ -336,10 +336,25 @@ __device__ __forceinline__ bool epilogue_chunk(const uint32_t (&r)[32], int row,
     }
   } else {
     float* out = (float*)args.out + slice + (size_t)row * args.ldo;
+    const bool vec = col0 + 32 <= args.N && ((uintptr_t)(out + col0) & 15u) == 0 &&
+                     (bias == nullptr || ((uintptr_t)(bias + col0) & 15u) == 0);
+    if (vec) {  // 16-byte stores of the 32 columns (one fp32 addition each, as below)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int col = col0 + i;
-      if (col < args.N) out[col] = __uint_as_float(r[i]) + (bias != nullptr ? bias[col] : 0.f);
+      for (int v4 = 0; v4 < 8; ++v4) {
+        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (bias != nullptr) b = __ldg(reinterpret_cast<const float4*>(bias + col0) + v4);
+        st_v4(out + col0 + v4 * 4,
+              make_uint4(__float_as_uint(__uint_as_float(r[v4 * 4]) + b.x),
+                         __float_as_uint(__uint_as_float(r[v4 * 4 + 1]) + b.y),
+                         __float_as_uint(__uint_as_float(r[v4 * 4 + 2]) + b.z),
+                         __float_as_uint(__uint_as_float(r[v4 * 4 + 3]) + b.w)));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int col = col0 + i;
+        if (col < args.N) out[col] = __uint_as_float(r[i]) + (bias != nullptr ? bias[col] : 0.f);
+      }
     }
   }
   return bad;
