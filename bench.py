@@ -221,7 +221,7 @@ def run_ours(args, wl):
                         "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T}[args.gemm])
     inp = make_inputs(wl, dev, seed=0)
     layer = MoELayer.from_workload(wl, inp, device=dev, fused_dispatch=args.dispatch == "fused",
-                                   experts=args.experts)
+                                   experts=args.experts, shared_sms=args.shared_sms)
     x = inp["x"]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -372,6 +372,7 @@ def run_ours(args, wl):
                                f"{wl.dtype} capacity_factor={wl.capacity_factor}",
                    "capacity": layer.cfg.capacity, "parallelism": f"replicas x{world}",
                    "expert_gemm": args.gemm, "dispatch": args.dispatch, "experts": args.experts,
+                   "shared_expert_sms": args.shared_sms if layer.shared else None,
                    "l2": "flushed before each step (512 MiB device write, outside the events)"},
         "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches, "gpu_launches_per_step": kernels_per_step,
@@ -430,6 +431,8 @@ def main():
                          "256-row tile, pairs for whole 256-row tiles + one CTA for the "
                          "rest, pairs with the tokens on the MMA's N side, or the "
                          "library's choice")
+    ap.add_argument("--shared-sms", type=int, default=0,
+                    help="SMs for the shared expert beside the routed GEMMs (0: beside routing)")
     ap.add_argument("--dispatch", choices=["fused", "copy"], default="copy",
                     help="fused: the first expert GEMM gathers its rows from x while loading "
                          "them; copy: the dispatch step copies them into a packed buffer")

@@ -317,6 +317,15 @@ typedef enum {
 } moe_gemm_pairing_t;
 moe_status_t moe_set_gemm_pairing(int32_t mode);
 
+/* SM budget of the persistent tensor-core expert GEMMs (moe_expert_up, _gather, _down and
+ * their E4M3 forms), process-wide: n = 0 (default) all SMs; n >= 2 at most n SMs (capped
+ * at the device's count), so that a GEMM on another stream can run beside them on the
+ * rest -- e.g. a shared expert on a few SMs next to the routed experts, which are bound by
+ * their weight stream from HBM.  The setting is read when a call is made; calls already
+ * enqueued keep theirs.  Results do not depend on it.  Returns MOE_ERR_INVALID for n < 0
+ * or n = 1. */
+moe_status_t moe_set_gemm_sms(int32_t n);
+
 /* Human-readable name of a status code (static storage). */
 const char* moe_status_string(moe_status_t status);
 

@@ -65,6 +65,7 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 static std::atomic<int> g_skip_block{-1};
 static std::atomic<int> g_spin_limit{1 << 21};
 static std::atomic<int> g_gemm_pairing{MOE_GEMM_AUTO};
+static std::atomic<int> g_gemm_sms{0};  // SM budget of the expert GEMMs (0: all)
 
 static int num_sms() {
   static int cached[64] = {0};
@@ -76,6 +77,14 @@ static int num_sms() {
     cached[dev] = n > 0 ? n : 148;
   }
   return cached[dev];
+}
+
+// SMs the persistent expert GEMMs may occupy: the budget set by moe_set_gemm_sms, capped
+// at the device's count, or all of them.
+static int gemm_sms() {
+  const int all = num_sms();
+  const int n = g_gemm_sms.load();
+  return (n > 0 && n < all) ? n : all;
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -251,7 +260,7 @@ static moe_status_t expert_up_impl(const moe_config& c, const void* a_in, const 
   if (c.dtype == MOE_BF16)
     return cuda_status(launch_tc_up(a_in, gather_src, c.K, gather_rows, w1, h, offsets, n_groups,
                                     c.F, c.d, rows_cap, group_row_bound(c, n_groups, rows_cap),
-                                    g_gemm_pairing.load(), (uint32_t*)ws, num_sms(),
+                                    g_gemm_pairing.load(), (uint32_t*)ws, gemm_sms(),
                                     (cudaStream_t)stream));
   return cuda_status(launch_simt_grouped(c.dtype, a_in, gather_src, c.K, gather_rows, w1, h, offsets,
                                          n_groups, c.F, c.d, rows_cap, true, (uint32_t*)ws,
@@ -302,7 +311,7 @@ moe_status_t moe_expert_up_e4m3(const moe_config* cfg, const void* xq, const flo
   return cuda_status(launch_tc_up_e4m3(xq, x_scale, src, c.K, src != nullptr ? c.T : 0, w1q,
                                        w1_scale, h, offsets, n_groups, c.F, c.d, rows_cap,
                                        group_row_bound(c, n_groups, rows_cap),
-                                       g_gemm_pairing.load(), (uint32_t*)ws, num_sms(),
+                                       g_gemm_pairing.load(), (uint32_t*)ws, gemm_sms(),
                                        (cudaStream_t)stream));
 }
 
@@ -317,7 +326,7 @@ moe_status_t moe_expert_down_e4m3(const moe_config* cfg, const void* hq, const f
   const moe_config& c = *cfg;
   return cuda_status(launch_tc_down_e4m3(hq, h_scale, w2q, w2_scale, y_perm, offsets, n_groups,
                                          c.d, c.F, rows_cap, group_row_bound(c, n_groups, rows_cap),
-                                         g_gemm_pairing.load(), (uint32_t*)ws, num_sms(),
+                                         g_gemm_pairing.load(), (uint32_t*)ws, gemm_sms(),
                                          (cudaStream_t)stream));
 }
 
@@ -343,7 +352,7 @@ moe_status_t moe_expert_down(const moe_config* cfg, const void* h, const int32_t
   if (c.dtype == MOE_BF16)
     return cuda_status(launch_tc_down(h, w2, y_perm, offsets, n_groups, c.d, c.F, rows_cap,
                                       group_row_bound(c, n_groups, rows_cap), g_gemm_pairing.load(),
-                                      (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
+                                      (uint32_t*)ws, gemm_sms(), (cudaStream_t)stream));
   return cuda_status(launch_simt_grouped(c.dtype, h, nullptr, 1, 0, w2, y_perm, offsets, n_groups,
                                          c.d, c.F, rows_cap, false, (uint32_t*)ws,
                                          (cudaStream_t)stream));
@@ -436,6 +445,12 @@ const char* moe_status_string(moe_status_t st) {
 }
 
 uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+moe_status_t moe_set_gemm_sms(int32_t n) {
+  if (n < 0 || n == 1) return MOE_ERR_INVALID;
+  g_gemm_sms.store(n);
+  return MOE_OK;
+}
 
 moe_status_t moe_set_gemm_pairing(int32_t mode) {
   if (mode != MOE_GEMM_AUTO && mode != MOE_GEMM_SINGLE && mode != MOE_GEMM_PAIR &&

@@ -24,8 +24,11 @@ class MoELayer:
     def __init__(self, T, d, E, K, F, dtype, capacity_factor, alpha, w_r, b_r, w1, w2,
                  w1s=None, w2s=None, renormalize=False, device="cuda", overlap=True,
                  drop_order="token", capacity_mode="tokens", sel_bias=None,
-                 fused_dispatch=False, experts="bf16"):
-        """``fused_dispatch``: the first expert Linear gathers its rows from x while loading
+                 fused_dispatch=False, experts="bf16", shared_sms=0):
+        """``shared_sms``: with a shared expert and ``overlap``, 0 (default) runs the shared
+        expert beside routing and dispatch; n > 0 runs it on n SMs beside the routed expert
+        GEMMs, which then get the other SMs (moe_set_gemm_sms).
+        ``fused_dispatch``: the first expert Linear gathers its rows from x while loading
         them (moe_expert_up_gather), so the dispatch step writes only the routing plan;
         by default the dispatch copies the rows into x_perm first, which measures faster
         on B300 (TMA row gathers move 512 bytes per instruction).
@@ -81,6 +84,7 @@ class MoELayer:
         # beside routing and the routed experts, the aux statistics (need only the routing
         # results) beside the expert GEMMs
         self.overlap = overlap
+        self.shared_sms = int(shared_sms) if w1s is not None else 0
         self.side = torch.cuda.Stream(device=dev) if overlap else None
         self.graph = None
         if experts not in ("bf16", "e4m3") or (experts == "e4m3" and dtype != "bf16"):
@@ -133,12 +137,13 @@ class MoELayer:
     @classmethod
     def from_workload(cls, wl, inputs, device="cuda", renormalize=False, overlap=True,
                       drop_order="token", capacity_mode="tokens", sel_bias=None,
-                      fused_dispatch=False, experts="bf16"):
+                      fused_dispatch=False, experts="bf16", shared_sms=0):
         return cls(wl.T, wl.d, wl.E, wl.K, wl.F, wl.dtype, wl.capacity_factor, wl.alpha,
                    inputs["w_r"], inputs["b_r"], inputs["w1"], inputs["w2"],
                    inputs.get("w1s"), inputs.get("w2s"), renormalize=renormalize, device=device,
                    overlap=overlap, drop_order=drop_order, capacity_mode=capacity_mode,
-                   sel_bias=sel_bias, fused_dispatch=fused_dispatch, experts=experts)
+                   sel_bias=sel_bias, fused_dispatch=fused_dispatch, experts=experts,
+                   shared_sms=shared_sms)
 
     # ---------------------------------------------------------------- stages
     def route(self, x, stream=None, logits_in=None):
@@ -264,7 +269,8 @@ class MoELayer:
             return self.y if y is None else y
         main = torch.cuda.current_stream()
         side = self.side
-        if self.shared:
+        beside_gemms = self.shared and self.shared_sms > 0
+        if self.shared and not beside_gemms:
             fork = torch.cuda.Event()
             fork.record(main)
             side.wait_event(fork)
@@ -277,15 +283,23 @@ class MoELayer:
         routed = torch.cuda.Event()
         routed.record(main)
         side.wait_event(routed)
-        with torch.cuda.stream(side):
-            self.aux(None, stats)
-        joined = torch.cuda.Event()
-        joined.record(side)
-        mark(2)
-        self.experts_up(x)
-        mark(3)
-        self.experts_down()
-        mark(4)
+        try:
+            with torch.cuda.stream(side):
+                self.aux(None, stats)
+                if beside_gemms:  # on its own SMs, beside the routed expert GEMMs
+                    N.set_gemm_sms(self.shared_sms)
+                    self.shared_expert(x)
+            joined = torch.cuda.Event()
+            joined.record(side)
+            if beside_gemms:
+                N.set_gemm_sms(max(N.num_sms(self.device) - self.shared_sms, 2))
+            mark(2)
+            self.experts_up(x)
+            mark(3)
+            self.experts_down()
+            mark(4)
+        finally:
+            N.set_gemm_sms(0)
         main.wait_event(joined)
         self.combine(None, y)
         mark(5)

@@ -26,7 +26,7 @@ EXPORTS = ("moe_workspace_size", "moe_rows_capacity", "moe_route", "moe_route_se
            "moe_expert_up", "moe_expert_up_gather", "moe_expert_down", "moe_quantize_e4m3",
            "moe_expert_up_e4m3", "moe_expert_down_e4m3", "moe_grouped_ffn", "moe_combine",
            "moe_aux_stats", "moe_aux_loss_grad", "moe_bf16_to_f16", "moe_sync_status", "moe_status_string", "moe_launch_count",
-           "moe_test_arm_scan_timeout", "moe_set_gemm_pairing")
+           "moe_test_arm_scan_timeout", "moe_set_gemm_pairing", "moe_set_gemm_sms")
 
 
 class MoeError(RuntimeError):
@@ -74,6 +74,7 @@ _SIGS = {
     "moe_launch_count": (ctypes.c_uint64, []),
     "moe_test_arm_scan_timeout": (None, [ctypes.c_int32, ctypes.c_int32]),
     "moe_set_gemm_pairing": (ctypes.c_int, [ctypes.c_int32]),
+    "moe_set_gemm_sms": (ctypes.c_int, [ctypes.c_int32]),
 }
 
 
@@ -262,6 +263,17 @@ def set_gemm_pairing(mode: int):
     GEMM_SPLIT (pairs for whole 256-row tiles, one CTA for the rest) or GEMM_PAIR_T
     (pairs with the tokens on the MMA's N side)."""
     _check("moe_set_gemm_pairing", lib().moe_set_gemm_pairing(mode))
+
+
+def set_gemm_sms(n: int):
+    """SM budget of the expert GEMMs (0: all SMs), read when a GEMM call is made."""
+    _check("moe_set_gemm_sms", lib().moe_set_gemm_sms(n))
+
+
+def num_sms(device=None) -> int:
+    import torch
+    return torch.cuda.get_device_properties(device if device is not None else
+                                            torch.cuda.current_device()).multi_processor_count
 
 
 def arm_scan_timeout(skip_block: int, spin_limit: int):

@@ -79,6 +79,14 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.moe_sync_status(None, None) == 1
 
 
+def test_gemm_settings_validated_on_host(lib):
+    assert lib.moe_set_gemm_sms(-1) == 1
+    assert lib.moe_set_gemm_sms(1) == 1
+    assert lib.moe_set_gemm_sms(20) == 0 and lib.moe_set_gemm_sms(0) == 0
+    assert lib.moe_set_gemm_pairing(9) == 1
+    assert lib.moe_set_gemm_pairing(N.GEMM_AUTO) == 0
+
+
 def test_capacity_binding_matches_pages_values():
     assert [N.capacity(256, 8, 1.25), N.capacity(4096, 8, 1.25), N.capacity(8192, 256, None),
             N.capacity(16384, 128, 1.5), N.capacity(65536, 8, 1.0)] == [40, 640, -1, 192, 8192]

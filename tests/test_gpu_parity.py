@@ -458,6 +458,57 @@ def test_graph_replay_matches_eager(idx, overlap):
     layer.check_device_status()
 
 
+def test_shared_expert_beside_routed_gemms_matches():
+    """The shared expert on a few SMs beside the routed expert GEMMs (SM budgets set per
+    call with moe_set_gemm_sms) gives exactly the default schedule's output, eager and
+    replayed from a CUDA graph; the budget is back at 0 afterwards."""
+    wl = Workload("shared_beside", 2048, 256, 16, 4, 512, "bf16", None, bias="normal",
+                  shared=True)
+    inp = make_inputs(wl, "cuda")
+    base = MoELayer.from_workload(wl, inp)
+    base.forward(inp["x"])
+    torch.cuda.synchronize()
+    y_ref = base.y.clone()
+    layer = MoELayer.from_workload(wl, inp, shared_sms=16)
+    layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert torch.equal(layer.y, y_ref)
+    layer.capture(inp["x"])
+    layer.y.zero_()
+    layer.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(layer.y, y_ref)
+    layer.check_device_status()
+
+
+@pytest.mark.parametrize("mode", [N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T],
+                         ids=["single", "pair", "split", "pair_t"])
+def test_gemm_sm_budget_gives_same_result(mode):
+    """An expert GEMM limited to a few SMs computes the same values as on all of them."""
+    offs = [0, 300, 812, 813, 1400]
+    G, rows, Kd, Nn = 4, 1400, 512, 768
+    cfg = N.make_config(rows, Kd, G, 1, Nn, "bf16", -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    a = torch.randn((rows, Kd), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((G, Nn, Kd), generator=g, device="cuda") * Kd ** -0.5).to(torch.bfloat16)
+    off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
+    outs = []
+    N.set_gemm_pairing(mode)
+    try:
+        for budget in (0, 12):
+            N.set_gemm_sms(budget)
+            h = torch.zeros((rows, Nn), dtype=torch.float16, device="cuda")
+            N.expert_up(cfg, a, off_t, G, rows, w, h, ws)
+            outs.append(h)
+    finally:
+        N.set_gemm_sms(0)
+        N.set_gemm_pairing(N.GEMM_AUTO)
+    assert N.sync_status(ws) == 0
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_host_stream_pipeline_matches_eager():
     """Pipelined host-buffer forwards (two device slots, uploads/downloads on their own
     streams) give, batch by batch, exactly the eager forward's output and statistics,
