@@ -105,39 +105,90 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
     float sc[VPT];
 #pragma unroll
     for (int j = 0; j < VPT; ++j) sc[j] = (sel_bias != nullptr) ? __fadd_rn(v[j], sb[j]) : v[j];
-    uint32_t taken = 0;
     int my_id = 0;
     float my_w = 0.f, wsum = 0.f;
-    uint32_t key[VPT];  // order-preserving integer image of each score (0: no candidate)
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) key[j] = (lane + 32 * j < E) ? score_key(sc[j]) : 0u;
-    for (int k = 0; k < K; ++k) {
-      // each lane's best untaken score (equal scores: the lower j, i.e. the lower id),
-      // then the warp's largest key and, among the lanes holding it, the lowest id
-      uint32_t bk = 0;
-      int be = INT_MAX;
+    if constexpr (VPT <= 4) {
+      // this lane's candidates, sorted once by (score desc, id asc): key = order-preserving
+      // integer image of the score (0: no candidate), with the expert's probability and j;
+      // each round the warp picks the largest head key and, among the lanes holding it,
+      // the lowest id, and the pick's owner drops its head (measured faster than a fresh
+      // scan of the lane's candidates per round up to 4 candidates per lane)
+      uint32_t ck[VPT];
+      float cp[VPT];
+      int cj[VPT];
 #pragma unroll
       for (int j = 0; j < VPT; ++j) {
-        const uint32_t kj = ((taken >> j) & 1u) ? 0u : key[j];
-        if (kj > bk) {
-          bk = kj;
-          be = lane + 32 * j;
+        ck[j] = (lane + 32 * j < E) ? score_key(sc[j]) : 0u;
+        cp[j] = p[j];
+        cj[j] = j;
+      }
+#pragma unroll
+      for (int pass = 0; pass < VPT; ++pass) {  // odd-even transposition sort
+#pragma unroll
+        for (int a = pass & 1; a + 1 < VPT; a += 2) {
+          const bool sw = ck[a + 1] > ck[a] || (ck[a + 1] == ck[a] && cj[a + 1] < cj[a]);
+          if (sw) {
+            const uint32_t tk = ck[a]; ck[a] = ck[a + 1]; ck[a + 1] = tk;
+            const float tp = cp[a]; cp[a] = cp[a + 1]; cp[a + 1] = tp;
+            const int tj = cj[a]; cj[a] = cj[a + 1]; cj[a + 1] = tj;
+          }
         }
       }
-      const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
-      const int bi = (int)__reduce_min_sync(0xffffffffu, bk == top ? (uint32_t)be : 0xffffffffu);
-      const int owner = bi & 31, jw = bi >> 5;
-      float mine = 0.f;
+      for (int k = 0; k < K; ++k) {
+        const uint32_t top = __reduce_max_sync(0xffffffffu, ck[0]);
+        const int bi = (int)__reduce_min_sync(
+            0xffffffffu, ck[0] == top ? (uint32_t)(lane + 32 * cj[0]) : 0xffffffffu);
+        const int owner = bi & 31;
+        const float pw = __shfl_sync(0xffffffffu, cp[0], owner);
+        if (lane == owner) {
 #pragma unroll
-      for (int j = 0; j < VPT; ++j)
-        if (j == jw) mine = p[j];
-      if (lane == owner) taken |= 1u << jw;
-      const float pw = __shfl_sync(0xffffffffu, mine, owner);
-      if (lane == k) {
-        my_id = bi;
-        my_w = pw;
+          for (int j = 0; j + 1 < VPT; ++j) {
+            ck[j] = ck[j + 1];
+            cp[j] = cp[j + 1];
+            cj[j] = cj[j + 1];
+          }
+          ck[VPT - 1] = 0u;
+        }
+        if (lane == k) {
+          my_id = bi;
+          my_w = pw;
+        }
+        wsum += pw;
       }
-      wsum += pw;
+    } else {
+      // eight candidates per lane: each round every lane rescans its untaken candidates
+      // (equal scores: the lower j, i.e. the lower id), then the warp's largest key and,
+      // among the lanes holding it, the lowest id
+      uint32_t taken = 0;
+      uint32_t key[VPT];  // order-preserving integer image of each score (0: no candidate)
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) key[j] = (lane + 32 * j < E) ? score_key(sc[j]) : 0u;
+      for (int k = 0; k < K; ++k) {
+        uint32_t bk = 0;
+        int be = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+          const uint32_t kj = ((taken >> j) & 1u) ? 0u : key[j];
+          if (kj > bk) {
+            bk = kj;
+            be = lane + 32 * j;
+          }
+        }
+        const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
+        const int bi = (int)__reduce_min_sync(0xffffffffu, bk == top ? (uint32_t)be : 0xffffffffu);
+        const int owner = bi & 31, jw = bi >> 5;
+        float mine = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+          if (j == jw) mine = p[j];
+        if (lane == owner) taken |= 1u << jw;
+        const float pw = __shfl_sync(0xffffffffu, mine, owner);
+        if (lane == k) {
+          my_id = bi;
+          my_w = pw;
+        }
+        wsum += pw;
+      }
     }
     if (renorm) my_w = my_w / wsum;
     if (lane < K) {
