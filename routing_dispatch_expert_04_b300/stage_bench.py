@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import json
 import statistics
+import time
 
 import torch
 
@@ -60,6 +61,9 @@ def main():
                     help="operand format of the expert GEMM stages")
     ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t"], default="auto",
                     help="expert-GEMM plan (moe_set_gemm_pairing) for the GEMM stages")
+    ap.add_argument("--sustain", type=float, default=0.0,
+                    help="also loop the stage back to back for this many seconds and report "
+                         "its mean time and the memory controller's busy fraction (nvidia-smi)")
     ap.add_argument("--profile-range", action="store_true",
                     help="run one more launch between cudaProfilerStart/Stop")
     ap.add_argument("--workload", default="long", choices=sorted(WORKLOADS))
@@ -136,6 +140,7 @@ def main():
         z.record(stream)
         z.synchronize()
         ms.append(a.elapsed_time(z))
+    sustained = _sustain(run, args.sustain) if args.sustain > 0 else None
     if args.profile_range:
         flush.zero_()
         torch.cuda.synchronize()
@@ -152,11 +157,45 @@ def main():
     line = {"stage": args.stage, "workload": wl.name, "T": T, "rows_kept": R,
             "tokens_with_kept_rows": t_active, "ms_median": round(med, 5),
             "bytes": nbytes, "gbs": round(nbytes / (med * 1e-3) / 1e9, 1), "iters": args.iters}
+    if sustained is not None:
+        line.update(sustained)
     if args.stage in ("expert_up", "expert_down"):
         flops = 2.0 * R * wl.d * wl.F
         line.update({"experts": args.experts, "gemm": args.gemm, "flops": flops,
                      "tflops": round(flops / (med * 1e-3) / 1e12, 1)})
     print(json.dumps(line), flush=True)
+
+
+def _sustain(run, seconds):
+    """Loop the stage back to back (no L2 flush) for `seconds` while nvidia-smi samples the
+    memory controller's busy fraction every 100 ms: the fraction of time the device memory
+    was being read or written, which scales with the DRAM bytes per second even where a
+    profiler would serialise concurrent kernels."""
+    import subprocess
+    for _ in range(5):
+        run()
+    torch.cuda.synchronize()
+    smi = subprocess.Popen(["nvidia-smi", f"--id={torch.cuda.current_device()}",
+                            "--query-gpu=utilization.memory", "--format=csv,noheader,nounits",
+                            "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                           text=True)
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    t0, n = time.time(), 0
+    a.record()
+    while time.time() - t0 < seconds:
+        for _ in range(20):
+            run()
+        n += 20
+        torch.cuda.synchronize()
+    z.record()
+    z.synchronize()
+    smi.terminate()
+    out = smi.communicate()[0].split()
+    busy = sorted(int(v) for v in out[3:-2] if v.strip().isdigit())
+    return {"sustained_ms": round(a.elapsed_time(z) / n, 5), "sustained_launches": n,
+            "mem_busy_pct_median": busy[len(busy) // 2] if busy else None,
+            "mem_busy_samples": len(busy)}
 
 
 def _gemm_stage(stage, experts, wl, cfg, x, ids, counts, offsets, slot, src, ws, rows_cap, dev):
