@@ -8,13 +8,16 @@
 // (EP)", step 3: expert GEMMs compute locally).
 //
 // Design (one CTA per SM, persistent):
-//   warp 0      TMA producer: per k-block, one 128x64 A box and one BNx64 B box into a
+//   warp 0      TMA producer: per k-block, one A box of 128 rows and one B box of BN rows,
+//               128 bytes of K each (64 bf16/fp16 or 128 E4M3 values), into a
 //               STAGES-deep ring of 128-byte-swizzled shared-memory stages;
 //   warp 1      owns TMEM (2 x BN fp32 columns: double-buffered accumulators) and one
-//               elected thread issues tcgen05.mma (M=128, N=BN, K=16) and commits;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused GELU (exact erf) or
-//               plain/bias, conversion and masked stores.  Overlaps the next tile's
-//               main loop through the second accumulator.
+//               elected thread issues tcgen05.mma (M=128, N=BN; kind::f16 with K=16 or
+//               kind::f8f6f4 with K=32) and commits;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, E4M3 row/column scales,
+//               fused GELU (the normal-tail form in tc_common.cuh) or plain/bias,
+//               conversion and masked stores.  Overlaps the next tile's main loop through
+//               the second accumulator.
 // Tiles are (group, n-tile, m-tile) with m fastest, so CTAs running at the same time
 // share one weight box through L2.  The per-group row ranges are read from `offsets` on
 // the device (no host synchronisation); the last m-tile of a group may run past the
