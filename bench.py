@@ -9,14 +9,22 @@ F=16384, bf16, capacity factor 1.25) unless ``--workload`` picks another shape.
 
 Prints ONE JSON line on rank 0.  ``value`` is tokens/s of the whole job (all ranks; each
 rank runs an independent replica, no collective on the data path).  L2 is flushed (a
-512 MiB device write) before every timed step, outside the step's CUDA events.
-``--impl reference`` times the fp64 CPU oracle on this host instead, on a bounded sample
-of the same workload.
+512 MiB device write) before every timed step, outside the step's CUDA events.  After
+the headline workload the same measurement runs, one after the other with the device
+memory freed in between, on the other bf16 layer shapes (DeepSeek-V3, Qwen3-30B-A3B,
+64K tokens); their results go into the line's ``workloads`` record.
+
+``cpu_baseline`` is the fp64 CPU oracle timed on this host: the whole layer for the
+Mixtral- and Qwen3-shaped workloads, a labelled extrapolation from whole expert blocks
+for the two largest.  ``--impl reference`` times the same oracle as the reference arm:
+each step is half a layer (the routing and half of the experts, then the other half and
+the combine), so two steps are exactly one layer forward.
 """
 
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -35,6 +43,8 @@ from routing_dispatch_expert_04_b300.workloads import WORKLOADS, make_inputs  # 
 
 METRIC = "MoE-layer fwd tokens/s; grouped-GEMM % bf16 peak; dispatch/combine HBM GB/s"
 L2_FLUSH_BYTES = 512 << 20
+L2_NOTE = "flushed before each timed GPU step (512 MiB device write, outside the events)"
+EXTRA_WORKLOADS = ("dsv3", "qwen3", "long")
 
 
 # ---------------------------------------------------------------------------- helpers
@@ -71,6 +81,21 @@ def dist_env():
     return ws, rank, local
 
 
+def workload_config(wl, capacity: int, world: int) -> dict:
+    """The `config` record: the workload and how it is measured.  Both arms print exactly
+    this record (implementation settings go elsewhere)."""
+    return {"workload": f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} K={wl.K} F={wl.F} "
+                        f"{wl.dtype} capacity_factor={wl.capacity_factor}",
+            "capacity": capacity, "parallelism": f"replicas x{world}", "l2": L2_NOTE}
+
+
+def gpu_uuid(device) -> str:
+    """nvidia-smi's identifier of a CUDA device: its UUID, which (unlike the CUDA ordinal)
+    names the same physical GPU whatever CUDA_VISIBLE_DEVICES says."""
+    u = str(torch.cuda.get_device_properties(device).uuid)
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -78,8 +103,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, device):
+        self.gpu = gpu_uuid(device)
         self.proc = None
         self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
 
@@ -120,7 +145,7 @@ class ClockSampler:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "gpu": self.gpu}
 
 
 def source_digest(*rel):
@@ -129,6 +154,11 @@ def source_digest(*rel):
         with open(os.path.join(ROOT, r), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ["routing_dispatch_expert_04_b300/csrc/" + f
+                for f in ("gemm_tc.cu", "gemm_tc2.cu", "gemm_tc2t.cu", "tc_common.cuh",
+                          "tc_ptx.cuh")]
 
 
 def recorded_traffic(kernel_key: str, digest: str):
@@ -146,46 +176,6 @@ def recorded_traffic(kernel_key: str, digest: str):
 
 
 # ---------------------------------------------------------------------------- CPU oracle
-def oracle_sample(wl, host, budget_s: float, rows_budget: int):
-    """Time the fp64 oracle on a bounded sample: routing, dispatch plan, combine and aux
-    in full, the expert FFN on up to ``rows_budget`` kept rows, scaled linearly to all R
-    kept rows.  Returns (seconds for the whole layer, description)."""
-    from oracle import moe_oracle as O
-    t0 = time.perf_counter()
-    _, L32 = O.router_logits(host["x"], host["w_r"], host["b_r"])
-    p = O.softmax(L32)
-    ids = O.top_k(L32, wl.K)
-    w = O.routing_weights(p, ids)
-    C = O.capacity(wl.T, wl.E, wl.capacity_factor)
-    plan = O.dispatch_plan(ids, wl.E, C)
-    O.aux_stats(ids, p, wl.E, wl.alpha)
-    t_route = time.perf_counter() - t0
-    R = plan["R"]
-    offs = plan["offsets"]
-    done = 0
-    t_ffn = 0.0
-    for e in range(wl.E):
-        lo, hi = int(offs[e]), int(offs[e + 1])
-        n = min(hi - lo, rows_budget - done)
-        if n <= 0:
-            continue
-        rows = plan["src"][lo:lo + n] // wl.K
-        t1 = time.perf_counter()
-        O.expert_ffn(host["x"][rows], host["w1"](e), host["w2"](e))
-        t_ffn += time.perf_counter() - t1
-        done += n
-        if done >= rows_budget or t_ffn > budget_s:
-            break
-    t1 = time.perf_counter()
-    O.combine(np.zeros((R, wl.d)), plan["slot"], w, wl.T)
-    t_comb = time.perf_counter() - t1
-    scale = R / max(done, 1)
-    total = t_route + t_ffn * scale + t_comb
-    desc = (f"routing, dispatch plan, combine and aux over all {wl.T} tokens; expert FFN "
-            f"on {done} of {R} kept rows, its time scaled by {scale:.1f}")
-    return total, desc
-
-
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -202,23 +192,98 @@ def host_views(wl, inp):
     def f32(t):
         return None if t is None else t.float().cpu().numpy()
     return {"x": f32(inp["x"]), "w_r": f32(inp["w_r"]), "b_r": f32(inp["b_r"]),
-            "w1": lambda e: f32(inp["w1"][e]), "w2": lambda e: f32(inp["w2"][e])}
+            "w1": lambda e: f32(inp["w1"][e]), "w2": lambda e: f32(inp["w2"][e]),
+            "w1s": f32(inp["w1s"][0]) if wl.shared else None,
+            "w2s": f32(inp["w2s"][0]) if wl.shared else None}
+
+
+def oracle_full_layer(wl, inp):
+    """The whole fp64 oracle layer forward (moe_forward) on the workload, timed once after
+    a warm-up on one expert block (which touches buffers of the same sizes).  Returns
+    (seconds, description)."""
+    from oracle import moe_oracle as O
+    h = host_views(wl, inp)
+    w1 = inp["w1"].float().cpu().numpy()
+    w2 = inp["w2"].float().cpu().numpy()
+    C = O.capacity(wl.T, wl.E, wl.capacity_factor)
+    n0 = min(wl.T * wl.K // wl.E, wl.T)
+    O.expert_ffn(h["x"][:max(n0, 1)], w1[0], w2[0])
+    shared = (h["w1s"], h["w2s"]) if wl.shared else None
+    t0 = time.perf_counter()
+    O.moe_forward(h["x"], h["w_r"], h["b_r"], w1, w2, wl.K, C, wl.alpha, shared=shared)
+    secs = time.perf_counter() - t0
+    return secs, (f"the whole layer (moe_forward: routing, dispatch plan, every expert's "
+                  f"kept rows, combine, aux) over all {wl.T} tokens, timed once after a "
+                  f"warm-up on one expert block")
+
+
+def oracle_extrapolated(wl, inp, rows_budget: int, block_rows: int):
+    """Routing, dispatch plan, aux and combine in full; the expert FFN on whole blocks of
+    up to ``block_rows`` kept rows (the layer's own GEMM shapes), experts in order, until
+    ``rows_budget`` rows; the FFN time scaled linearly to all R kept rows (and the shared
+    expert, if any, timed on one block and scaled to T rows).  Returns (seconds, desc)."""
+    from oracle import moe_oracle as O
+    h = host_views(wl, inp)
+    O.expert_ffn(h["x"][:min(block_rows, wl.T)], h["w1"](0), h["w2"](0))  # warm-up
+    t0 = time.perf_counter()
+    _, L32 = O.router_logits(h["x"], h["w_r"], h["b_r"])
+    p = O.softmax(L32)
+    ids = O.top_k(L32, wl.K)
+    w = O.routing_weights(p, ids)
+    C = O.capacity(wl.T, wl.E, wl.capacity_factor)
+    plan = O.dispatch_plan(ids, wl.E, C)
+    O.aux_stats(ids, p, wl.E, wl.alpha)
+    t_route = time.perf_counter() - t0
+    R, offs = plan["R"], plan["offsets"]
+    done, t_ffn = 0, 0.0
+    for e in range(wl.E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        n = min(hi - lo, block_rows)
+        if n <= 0:
+            continue
+        rows = plan["src"][lo:lo + n] // wl.K
+        w1e, w2e = h["w1"](e), h["w2"](e)
+        t1 = time.perf_counter()
+        O.expert_ffn(h["x"][rows], w1e, w2e)
+        t_ffn += time.perf_counter() - t1
+        done += n
+        if done >= rows_budget:
+            break
+    t_shared, shared_note = 0.0, ""
+    if wl.shared:
+        n = min(block_rows, wl.T)
+        t1 = time.perf_counter()
+        O.dense_ffn(h["x"][:n], h["w1s"], h["w2s"])
+        t_shared = (time.perf_counter() - t1) * wl.T / n
+        shared_note = f"; shared expert on {n} of {wl.T} tokens, scaled by {wl.T / n:.1f}"
+    t1 = time.perf_counter()
+    O.combine(np.zeros((R, wl.d)), plan["slot"], w, wl.T)
+    t_comb = time.perf_counter() - t1
+    scale = R / max(done, 1)
+    total = t_route + t_ffn * scale + t_shared + t_comb
+    return total, (f"routing, dispatch plan, aux and combine over all {wl.T} tokens; expert FFN "
+                   f"on {done} of {R} kept rows (blocks of up to {block_rows} rows of one "
+                   f"expert), its time scaled by {scale:.1f}{shared_note}")
+
+
+def cpu_baseline(wl, inp, full: bool) -> dict:
+    if full:
+        secs, desc = oracle_full_layer(wl, inp)
+    else:
+        secs, desc = oracle_extrapolated(wl, inp, rows_budget=4096,
+                                         block_rows=1024 if wl.E <= 16 else 512)
+    return {"value": round(wl.T / secs, 3), "unit": "tokens/s", "cores": blas_threads(),
+            "kind": "oracle", "sample": desc, "extrapolated": not full,
+            "seconds_per_layer": round(secs, 3)}
 
 
 # ---------------------------------------------------------------------------- our arm
-def run_ours(args, wl):
-    from routing_dispatch_expert_04_b300 import native as N
-    from routing_dispatch_expert_04_b300.layer import MoELayer
+def measure(wl, args, dev, world, pk, with_traffic: bool):
+    """One workload on this GPU: the CUDA-graph step timed with per-stage events, and the
+    end-to-end rate through the host-buffer pipeline.  Returns a plain dict (no device
+    tensors survive the call)."""
+    from routing_dispatch_expert_04_b300.layer import HostStream, MoELayer
 
-    world, rank, local = dist_env()
-    if world > 1:
-        torch.distributed.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pk = peaks()
-
-    N.set_gemm_pairing({"auto": N.GEMM_AUTO, "single": N.GEMM_SINGLE, "pair": N.GEMM_PAIR,
-                        "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T}[args.gemm])
     inp = make_inputs(wl, dev, seed=0)
     layer = MoELayer.from_workload(wl, inp, device=dev, fused_dispatch=args.dispatch == "fused",
                                    experts=args.experts, shared_sms=args.shared_sms)
@@ -240,13 +305,13 @@ def run_ours(args, wl):
 
     stage_ms = {n: [] for n in stage_names}
     step_ms = []
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev)
     clocks.start()
     time.sleep(0.3)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    for k in range(args.steps):
+    for _ in range(args.steps):
         flush.zero_()
         layer.replay()
         torch.cuda.synchronize()   # the graph's events are re-recorded by the next replay
@@ -254,7 +319,6 @@ def run_ours(args, wl):
             stage_ms[n].append(marks[i].elapsed_time(marks[i + 1]))
         step_ms.append(marks[0].elapsed_time(marks[-1]))
     torch.cuda.synchronize()
-    launches = kernels_per_step * args.steps
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
@@ -264,11 +328,10 @@ def run_ours(args, wl):
     value = whole_job_tokens_per_s(wl.T, args.steps, world, local_s, dev)
     total_s = world * wl.T * args.steps / value
 
-    # ---- algorithmic work of this batch (see the per-stage byte/flop model)
+    # ---- algorithmic work of this batch (the per-stage byte/flop model)
     R = int(layer.offsets[-1].item())
     b = 2 if wl.dtype == "bf16" else 4
-    slot = layer.slot
-    t_active = int((slot >= 0).any(dim=1).sum().item())
+    t_active = int((layer.slot >= 0).any(dim=1).sum().item())
     A = wl.T * wl.K
     flops_up = 2.0 * R * wl.d * wl.F
     flops_down = 2.0 * R * wl.F * wl.d
@@ -281,34 +344,35 @@ def run_ours(args, wl):
     yb = 2 if wl.dtype == "bf16" else 4  # expert outputs: fp16 for bf16 layers
     bytes_combine = R * wl.d * yb + wl.T * wl.d * b + A * 8 + (wl.T * wl.d * yb if layer.shared else 0)
     bytes_route = wl.T * wl.d * b + wl.E * wl.d * b + wl.T * wl.E * 4 * 2 + A * 8
+    # expert GEMM bytes: the weights (W1 bf16, W2 fp16: 2 bytes each, or 1 for E4M3), the
+    # A rows read and the output rows written (h and y_perm fp16)
+    wbytes = wl.E * wl.F * wl.d * (1 if args.experts == "e4m3" else 2)
+    bytes_up = wbytes + R * wl.d * b + R * wl.F * 2
+    bytes_down = wbytes + R * wl.F * 2 + R * wl.d * 2
     med = {n: statistics.median(v) for n, v in stage_ms.items()}
     avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
-
-    dom = "expert_up" if avg["expert_up"] >= avg["expert_down"] else "expert_down"
-    dom_flops = flops_up if dom == "expert_up" else flops_down
-    achieved_tf = dom_flops / (avg[dom] * 1e-3) / 1e12
-    kernel_srcs = ["routing_dispatch_expert_04_b300/csrc/" + f
-                   for f in ("gemm_tc.cu", "gemm_tc2.cu", "gemm_tc2t.cu", "tc_common.cuh",
-                             "tc_ptx.cuh")]
-    traffic = recorded_traffic(f"{dom}:{wl.name}:{args.experts}:{args.gemm}",
-                               source_digest(*kernel_srcs))
+    hbm = pk["hbm_gbs"]
     if args.experts == "e4m3":
         # FP8 contraction: the measured bf16 peak times the nominal fp8/bf16 ratio (2)
         peak_tf, peak_src = 2.0 * pk["bf16_tflops"], f"{pk['source']} bf16 dense (burst) x 2 (nominal e4m3/bf16)"
     else:
         peak_tf, peak_src = pk["bf16_tflops"], f"{pk['source']} bf16 dense (burst)"
-    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved_tf, 2),
-                "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": round(achieved_tf / peak_tf, 4), "traffic": traffic,
-                "peak_source": peak_src,
-                "algorithmic_flops_per_launch": dom_flops}
-    hbm = pk["hbm_gbs"]
 
     def gbs(nbytes, ms):
         return nbytes / (ms * 1e-3) / 1e9
 
+    def gemm_rec(flops, nbytes, ms):
+        tf = flops / (ms * 1e-3) / 1e12
+        g = gbs(nbytes, ms)
+        ft, fh = tf / peak_tf, g / hbm
+        return {"ms": round(ms, 4), "tflops": round(tf, 2), "frac_of_tensor_peak": round(ft, 4),
+                "gbs": round(g, 1), "frac_of_hbm": round(fh, 4),
+                "binding": "tensor" if ft >= fh else "hbm"}
+
     stages = {
         "ms_median": {n: round(v, 4) for n, v in med.items()},
+        "expert_up": gemm_rec(flops_up, bytes_up, avg["expert_up"]),
+        "expert_down": gemm_rec(flops_down, bytes_down, avg["expert_down"]),
         "expert_up_tflops": round(flops_up / (avg["expert_up"] * 1e-3) / 1e12, 2),
         "expert_down_tflops": round(flops_down / (avg["expert_down"] * 1e-3) / 1e12, 2),
         "grouped_gemm_frac_of_peak": round(
@@ -320,14 +384,28 @@ def run_ours(args, wl):
         "combine_frac_of_hbm": round(gbs(bytes_combine, avg["combine"]) / hbm, 4),
         "route_gbs": round(gbs(bytes_route, avg["route"]), 1),
         "rows_kept": R, "tokens_with_kept_rows": t_active,
-        "bytes": {"dispatch": bytes_dispatch, "combine": bytes_combine, "route": bytes_route},
+        "bytes": {"dispatch": bytes_dispatch, "combine": bytes_combine, "route": bytes_route,
+                  "expert_up": bytes_up, "expert_down": bytes_down},
         "flops": {"expert_up": flops_up, "expert_down": flops_down},
+        "peak": {"tensor_tflops": peak_tf, "tensor_source": peak_src, "hbm_gbs": hbm,
+                 "hbm_source": f"{pk['source']} copy bandwidth"},
     }
+
+    dom = "expert_up" if avg["expert_up"] >= avg["expert_down"] else "expert_down"
+    dom_flops = flops_up if dom == "expert_up" else flops_down
+    achieved_tf = dom_flops / (avg[dom] * 1e-3) / 1e12
+    traffic = None
+    if with_traffic:
+        traffic = recorded_traffic(f"{dom}:{wl.name}:{args.experts}:{args.gemm}",
+                                   source_digest(*GEMM_SOURCES))
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved_tf, 2),
+                "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(achieved_tf / peak_tf, 4), "traffic": traffic,
+                "peak_source": peak_src, "algorithmic_flops_per_launch": dom_flops}
 
     # ---- end to end through the public API with host buffers: every step uploads its
     # input from pinned host memory and downloads its output and aux statistics; the
     # steps are pipelined (upload of step i+1 and download of step i-1 overlap step i)
-    from routing_dispatch_expert_04_b300.layer import HostStream
     hs = HostStream(layer, x)
     x_host = x.cpu().pin_memory()
     y_hosts = [torch.empty((wl.T, wl.d), dtype=layer.dtype).pin_memory() for _ in range(2)]
@@ -353,31 +431,70 @@ def run_ours(args, wl):
            "ms_per_step": round(e2e_s * 1e3 / args.steps, 4),
            "pipelining": "two device slots; upload i+1 and download i-1 overlap step i"}
     layer.check_device_status()
+    capacity = layer.cfg.capacity
+    shared = layer.shared
+    del hs, layer, flush, marks, x_host, y_hosts, st_hosts
+    gc.collect()
+    torch.cuda.synchronize()
+    return {"value": value, "ms_per_step": total_s * 1e3 / args.steps, "stages": stages,
+            "roofline": roofline, "e2e": e2e, "clocks": clk, "kernels_per_step": kernels_per_step,
+            "capacity": capacity, "shared": shared, "inputs": inp}
 
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        host = host_views(wl, inp)
-        secs, desc = oracle_sample(wl, host, budget_s=args.cpu_budget, rows_budget=args.cpu_rows)
-        cpu = {"value": round(wl.T / secs, 3), "unit": "tokens/s", "cores": blas_threads(),
-               "kind": "oracle", "sample": desc}
+
+def run_ours(args, wl):
+    from routing_dispatch_expert_04_b300 import native as N
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    N.set_gemm_pairing({"auto": N.GEMM_AUTO, "single": N.GEMM_SINGLE, "pair": N.GEMM_PAIR,
+                        "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T}[args.gemm])
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+
+    m = measure(wl, args, dev, world, pk, with_traffic=True)
+    cpu = cpu_baseline(wl, m["inputs"], full=True) if do_cpu else None
+    launches = m["kernels_per_step"] * args.steps
+    del m["inputs"]
+    torch.cuda.empty_cache()
+
+    extra = {}
+    names = [] if args.extra_workloads in ("", "none") else args.extra_workloads.split(",")
+    for name in names:
+        if name == wl.name:
+            continue
+        xw = WORKLOADS[name]
+        r = measure(xw, args, dev, world, pk, with_traffic=False)
+        rec = {"config": workload_config(xw, r["capacity"], world),
+               "tokens_per_s": round(r["value"], 1), "ms_per_step": round(r["ms_per_step"], 4),
+               "e2e_tokens_per_s": r["e2e"]["value"], "e2e": r["e2e"],
+               "stages": r["stages"], "clocks": r["clocks"],
+               "gpu_launches_per_step": r["kernels_per_step"]}
+        if do_cpu:
+            rec["cpu_baseline"] = cpu_baseline(xw, r["inputs"], full=(name == "qwen3"))
+        launches += r["kernels_per_step"] * args.steps
+        del r
+        gc.collect()
+        torch.cuda.empty_cache()
+        extra[name] = rec
 
     out = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": round(m["value"], 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(total_s * 1e3 / args.steps, 4), "higher_is_better": True,
+        "ms_per_step": round(m["ms_per_step"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype if args.experts == "bf16" else f"{wl.dtype} layer, e4m3 expert GEMMs",
         "data": "synthetic",
-        "config": {"workload": f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} K={wl.K} F={wl.F} "
-                               f"{wl.dtype} capacity_factor={wl.capacity_factor}",
-                   "capacity": layer.cfg.capacity, "parallelism": f"replicas x{world}",
-                   "expert_gemm": args.gemm, "dispatch": args.dispatch, "experts": args.experts,
-                   "shared_expert_sms": args.shared_sms if layer.shared else None,
-                   "l2": "flushed before each step (512 MiB device write, outside the events)"},
-        "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches, "gpu_launches_per_step": kernels_per_step,
+        "config": workload_config(wl, m["capacity"], world),
+        "settings": {"expert_gemm": args.gemm, "dispatch": args.dispatch, "experts": args.experts,
+                     "shared_expert_sms": args.shared_sms if m["shared"] else None},
+        "roofline": m["roofline"], "stages": m["stages"], "cpu_baseline": cpu, "e2e": m["e2e"],
+        "gpu_launches": launches, "gpu_launches_per_step": m["kernels_per_step"],
         "launch_mode": "one CUDA graph per step (library kernels + the scan's memset node)",
-        "clocks": clk,
+        "clocks": m["clocks"],
+        "workloads": extra,
         "device": torch.cuda.get_device_name(dev),
     }
     if rank == 0:
@@ -387,34 +504,89 @@ def run_ours(args, wl):
 
 
 # ---------------------------------------------------------------------------- reference
+class HalfLayerOracle:
+    """The fp64 oracle layer forward cut into two half-layer steps: an even step runs the
+    routing, the dispatch plan and the aux statistics over all T tokens and the expert FFN
+    of the first half of the experts; an odd step the FFN of the other half and the
+    combine.  Every expert block is whole (all its kept rows), so two consecutive steps
+    are exactly one moe_forward's work in the same library calls."""
+
+    def __init__(self, wl, inp):
+        from oracle import moe_oracle as O
+        self.O, self.wl = O, wl
+        h = host_views(wl, inp)
+        self.x, self.w_r, self.b_r = h["x"], h["w_r"], h["b_r"]
+        self.w1 = inp["w1"].float().cpu().numpy()
+        self.w2 = inp["w2"].float().cpu().numpy()
+        self.shared = (h["w1s"], h["w2s"]) if wl.shared else None
+        self.C = O.capacity(wl.T, wl.E, wl.capacity_factor)
+        self.half = (wl.E + 1) // 2
+        self.i = 0
+
+    def _experts(self, lo_e, hi_e):
+        O, wl, p = self.O, self.wl, self.plan
+        offs = p["offsets"]
+        for e in range(lo_e, hi_e):
+            lo, hi = int(offs[e]), int(offs[e + 1])
+            if hi > lo:
+                self.y_perm[lo:hi], _ = O.expert_ffn(self.x_perm[lo:hi], self.w1[e], self.w2[e])
+
+    def step(self):
+        O, wl = self.O, self.wl
+        if self.i % 2 == 0:
+            _, L32 = O.router_logits(self.x, self.w_r, self.b_r)
+            prob = O.softmax(L32)
+            ids = O.top_k(L32, wl.K)
+            self.w = O.routing_weights(prob, ids)
+            self.plan = O.dispatch_plan(ids, wl.E, self.C)
+            O.aux_stats(ids, prob, wl.E, wl.alpha)
+            src = self.plan["src"].astype(np.int64)
+            self.x_perm = O.widen(self.x)[src // wl.K]
+            self.y_perm = np.zeros((self.plan["R"], wl.d))
+            self._experts(0, self.half)
+        else:
+            self._experts(self.half, wl.E)
+            ys = O.expert_ffn(O.widen(self.x), *self.shared)[0] if self.shared else None
+            self.y = O.combine(self.y_perm, self.plan["slot"], self.w, wl.T, ys)
+        self.i += 1
+
+
 def run_reference(args, wl):
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    from oracle import moe_oracle as O
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(wl, dev, seed=0)
-    host = host_views(wl, inp)
+    C = O.capacity(wl.T, wl.E, wl.capacity_factor)
     cores = blas_threads()
+    orc = HalfLayerOracle(wl, inp)
+    del inp
     for _ in range(args.warmup):
-        oracle_sample(wl, host, budget_s=args.ref_budget, rows_budget=args.ref_rows)
-    secs, descs = [], None
+        orc.step()
+    secs = []
     for _ in range(args.steps):
-        s, descs = oracle_sample(wl, host, budget_s=args.ref_budget, rows_budget=args.ref_rows)
-        secs.append(s)
+        t0 = time.perf_counter()
+        orc.step()
+        secs.append(time.perf_counter() - t0)
     total = sum(secs)
-    value = wl.T * args.steps / total
+    # two half-layer steps are one layer forward of T tokens
+    value = wl.T * (args.steps / 2) / total
+    desc = (f"each step half a layer forward of the fp64 oracle (even steps: routing, dispatch "
+            f"plan and aux over all {wl.T} tokens, then the whole kept blocks of experts "
+            f"0..{orc.half - 1}; odd steps: experts {orc.half}..{wl.E - 1} and the combine), "
+            f"so two steps are one moe_forward; rank 0 only")
     out = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total * 1e3 / args.steps, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: T={wl.T} d={wl.d} E={wl.E} K={wl.K} F={wl.F} "
-                               f"{wl.dtype} capacity_factor={wl.capacity_factor}",
-                   "parallelism": "host cores"},
+        "config": workload_config(wl, C, world),
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
-                         "kind": "oracle", "sample": descs},
+                         "kind": "oracle", "sample": desc, "extrapolated": False},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "step_seconds": {"min": round(min(secs), 3), "max": round(max(secs), 3)},
     }
     print(json.dumps(out), flush=True)
 
@@ -426,6 +598,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral", choices=sorted(WORKLOADS))
+    ap.add_argument("--extra-workloads", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated workloads measured after the headline one and "
+                         "reported in the line's `workloads` record ('none' to skip)")
     ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t"], default="auto",
                     help="expert GEMM kernels: one CTA per 128-row tile, CTA pairs per "
                          "256-row tile, pairs for whole 256-row tiles + one CTA for the "
@@ -441,10 +616,6 @@ def main():
                          "(per-row E4M3 operands); an e4m3 line is a different precision "
                          "and says so in its dtype")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--cpu-rows", type=int, default=512)
-    ap.add_argument("--ref-budget", type=float, default=6.0)
-    ap.add_argument("--ref-rows", type=int, default=128)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

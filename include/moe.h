@@ -84,7 +84,12 @@ typedef enum { MOE_DROP_TOKEN_MAJOR = 0, MOE_DROP_SLOT_MAJOR = 1 } moe_drop_orde
 /* Bytes of device workspace `ws` the calls below need for this config.  The caller
  * allocates it and ZERO-FILLS it once before first use; the library keeps it
  * consistent afterwards.  One workspace must not be used by two calls that can run
- * concurrently. */
+ * concurrently, with one exception: moe_aux_stats reads only the probability sums that
+ * moe_route left and writes only its own region (per-expert f_i*P_i and its completion
+ * counter), so it may run concurrently with the expert-GEMM calls (moe_expert_up,
+ * _gather, _down, their E4M3 forms, moe_grouped_ffn) and moe_combine on the same
+ * workspace -- those touch only the status word, by atomic OR.  It must not overlap
+ * moe_route, moe_route_select_bias or moe_dispatch on that workspace. */
 size_t moe_workspace_size(const moe_config* cfg);
 
 /* Rows the packed buffers (src, x_perm, h, y_perm) must hold:
@@ -140,10 +145,11 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
 /* moe_dispatch without a workspace argument.  The pages have no counterpart: this
  * entry point exists for callers that cannot allocate device memory when they run the
  * layer (code inside a custom allocator or memory pool, plugins barred from cudaMalloc,
- * runtimes that reserve all memory up front).  Same arguments, outputs and results as
- * moe_dispatch minus `ws`: its scratch (scan descriptors, ticket, positions) lives in a
- * static 4 MiB device array inside the library, which every GPU that loads the library
- * holds until the process exits.  It allocates nothing and calls no allocating routine.
+ * runtimes that reserve all memory up front).  Same arguments, outputs, results and
+ * argument checks as moe_dispatch minus `ws`: its scratch (status word, scan
+ * descriptors, ticket, positions) lives in a static 4 MiB device array inside the
+ * library, which every GPU that loads the library holds until the process exits.  It
+ * allocates nothing and calls no allocating routine.
  * - Limit: the scratch must hold 256 + ceil(T*K/4096)*E*8 + T*K*4 bytes (each part
  *   rounded up to 256 bytes), i.e. T*K up to about 930,000 assignments at E = 256 and
  *   1,040,000 at E = 8; larger configs return MOE_ERR_UNSUPPORTED with a message on
@@ -152,11 +158,20 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
  *   current); make that first call before any stream capture.
  * - All calls share the array: calls that can overlap on the GPU (other streams, other
  *   host threads) race and must be serialised by the caller.
- * - Device-side errors are not reported: an out-of-range expert id gets slot -1 and is
- *   left out of counts, and a look-back wait that gives up leaves the results invalid. */
+ * - Device-side errors (an out-of-range expert id, which gets slot -1 and is left out of
+ *   counts; a look-back wait that gave up, which leaves that call's results invalid) are
+ *   recorded in the array's status word, which keeps them across calls until
+ *   moe_dispatch_noalloc_status reads it.
+ * - The test hook moe_test_arm_scan_timeout applies to this call as to moe_dispatch. */
 moe_status_t moe_dispatch_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_ids,
                                   int32_t* counts, int32_t* offsets, int32_t* slot, int32_t* src,
                                   void* x_perm, void* stream);
+
+/* Status of the moe_dispatch_noalloc calls on the current device: synchronises `stream`,
+ * then returns and clears the status word of the static scratch (MOE_OK, MOE_ERR_TIMEOUT
+ * or MOE_ERR_DEVICE), or MOE_ERR_CUDA if a CUDA call failed.  Like the dispatch itself it
+ * allocates nothing. */
+moe_status_t moe_dispatch_noalloc_status(void* stream);
 
 /* Step 3a -- grouped first expert Linear with GELU fused in its epilogue
  * ("Each expert applies: Linear(d -> 4d) -> GELU -> Linear(4d -> d)").

@@ -67,6 +67,14 @@ static std::atomic<int> g_spin_limit{1 << 21};
 static std::atomic<int> g_gemm_pairing{MOE_GEMM_AUTO};
 static std::atomic<int> g_gemm_sms{0};  // SM budget of the expert GEMMs (0: all)
 
+// The scan test hook (moe_test_arm_scan_timeout) for the next dispatch call, disarmed as
+// it is taken: the block that withholds its counts (-1: none) and the spin limit.
+void take_scan_test_hook(int* skip_block, int* spin_limit) {
+  const int skip = g_skip_block.exchange(-1);
+  *skip_block = skip;
+  *spin_limit = skip >= 0 ? g_spin_limit.load() : (1 << 21);
+}
+
 static int num_sms() {
   static int cached[64] = {0};
   int dev = 0;
@@ -89,7 +97,7 @@ static int gemm_sms() {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-static moe_status_t check_cfg(const moe_config* c) {
+moe_status_t check_cfg(const moe_config* c) {
   if (c == nullptr) return MOE_ERR_INVALID;
   if (c->T < 0 || c->d <= 0 || c->E <= 0 || c->K <= 0 || c->F <= 0) return MOE_ERR_INVALID;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID;
@@ -118,7 +126,7 @@ static int64_t group_row_bound(const moe_config& c, int n_groups, int64_t rows_c
   return 0;
 }
 
-static int64_t rows_capacity(const moe_config& c) {
+int64_t rows_capacity(const moe_config& c) {
   const int64_t A = (int64_t)c.T * c.K;
   if (c.capacity < 0) return A;
   const int64_t ec = (int64_t)c.E * c.capacity;
@@ -227,8 +235,8 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
   // reset the scan ticket and descriptors (the status word at offset 0 is kept)
   s = cuda_status(cudaMemsetAsync((char*)ws + 4, 0, L.desc + (size_t)L.nblk_scan * c.E * 8 - 4, st));
   if (s != MOE_OK) return s;
-  const int skip = g_skip_block.exchange(-1);
-  const int spin = skip >= 0 ? g_spin_limit.load() : (1 << 21);
+  int skip = -1, spin = 0;
+  take_scan_test_hook(&skip, &spin);
   int32_t* pos = (int32_t*)((char*)ws + L.pos);
   s = cuda_status(launch_scan(topk_ids, A, c.E, c.capacity, L.nblk_scan,
                               (unsigned long long*)((char*)ws + L.desc), pos, counts, offsets, hdr,

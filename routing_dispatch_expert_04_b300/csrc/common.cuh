@@ -91,6 +91,12 @@ inline WsLayout ws_layout(const moe_config& c) {
 // ------------------------------------------------------------------ launch bookkeeping
 void count_launch();
 
+// Argument checks and sizes shared by the entry points (api.cu): the config's validity
+// (MOE_OK or the error status), the rows of the packed buffers, and the scan test hook.
+moe_status_t check_cfg(const moe_config* c);
+int64_t rows_capacity(const moe_config& c);
+void take_scan_test_hook(int* skip_block, int* spin_limit);
+
 // ------------------------------------------------------------------ element helpers
 template <typename T> struct Elem;
 template <> struct Elem<float> {

@@ -11,7 +11,9 @@
 // The array is a fixed NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU which loads this
 // library holds until the process exits.  Its device address is looked up once per
 // device (cudaGetSymbolAddress, on the first call with that device current) -- in host
-// code the symbol names a host-side stand-in, never a device address.
+// code the symbol names a host-side stand-in, never a device address.  Its first word is
+// the status word the kernels record device-side errors in; it keeps them, across calls,
+// until moe_dispatch_noalloc_status reads and clears it.
 #include <mutex>
 #include <stdio.h>
 
@@ -68,13 +70,10 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config* cfg, const void* 
                                              const int32_t* topk_ids, int32_t* counts,
                                              int32_t* offsets, int32_t* slot, int32_t* src,
                                              void* x_perm, void* stream) {
-  if (cfg == nullptr) return MOE_ERR_INVALID;
+  // the same configurations are accepted and rejected as by moe_dispatch
+  const moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
-  if (c.T < 0 || c.d <= 0 || c.E <= 0 || c.K <= 0 || c.F <= 0 || c.K > c.E) return MOE_ERR_INVALID;
-  if (c.dtype != MOE_F32 && c.dtype != MOE_BF16) return MOE_ERR_INVALID;
-  if (c.E > 256 || c.K > 32) return MOE_ERR_UNSUPPORTED;
-  if ((int64_t)c.T * c.K >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
-  if (c.d % (c.dtype == MOE_BF16 ? 8 : 4) != 0) return MOE_ERR_UNSUPPORTED;
   if (!counts || !offsets || !aligned16_na(counts) || !aligned16_na(offsets)) return MOE_ERR_INVALID;
   const int A = c.T * c.K;
   if (A > 0) {
@@ -108,18 +107,36 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config* cfg, const void* 
     return MOE_ERR_CUDA;
   }
   char* base = (char*)scratch;
-  // status word, chunk ticket and descriptors must start at zero; the array keeps the
-  // previous call's contents
-  e = cudaMemsetAsync(base, 0, L.desc + (size_t)L.nblk_scan * c.E * 8, st);
+  // the chunk ticket and the descriptors must start at zero (the array keeps the previous
+  // call's contents); the status word at offset 0 is left alone, so that an error stays
+  // recorded until moe_dispatch_noalloc_status reads it
+  e = cudaMemsetAsync(base + 4, 0, L.desc + (size_t)L.nblk_scan * c.E * 8 - 4, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   uint32_t* hdr = (uint32_t*)base;
   int32_t* pos = (int32_t*)(base + L.pos);
+  int skip = -1, spin = 0;
+  take_scan_test_hook(&skip, &spin);
   e = launch_scan(topk_ids, A, c.E, c.capacity, L.nblk_scan, (unsigned long long*)(base + L.desc),
-                  pos, counts, offsets, hdr, -1, 1 << 21, c.drop_order, c.T, c.K, st);
+                  pos, counts, offsets, hdr, skip, spin, c.drop_order, c.T, c.K, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  int64_t rows_cap = A;
-  if (c.capacity >= 0 && (int64_t)c.E * c.capacity < rows_cap) rows_cap = (int64_t)c.E * c.capacity;
   e = launch_dispatch(c.dtype, x, topk_ids, pos, offsets, c.T, c.d, c.E, c.K, c.capacity, slot, src,
-                      x_perm, rows_cap, hdr, sms, st);
+                      x_perm, rows_capacity(c), hdr, sms, st);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status_t moe_dispatch_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  int sms = 0;
+  cudaError_t e = scratch_for_current_device(&scratch, &sms);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  uint32_t word = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != 0) e = cudaMemset(scratch, 0, sizeof(word));
+  if (e != cudaSuccess) {
+    fprintf(stderr, "moe_dispatch_noalloc_status: %s\n", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  if (word & DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (word & (DEV_ERR_BAD_ID | DEV_ERR_OVERFLOW | DEV_ERR_RANGE)) return MOE_ERR_DEVICE;
+  return MOE_OK;
 }

@@ -285,6 +285,9 @@ class MoELayer:
         side.wait_event(routed)
         try:
             with torch.cuda.stream(side):
+                # the aux statistics share the workspace with the expert GEMMs running on
+                # the main stream: moe_aux_stats may (it touches only its own region of
+                # the workspace, the GEMMs only the status word)
                 self.aux(None, stats)
                 if beside_gemms:  # on its own SMs, beside the routed expert GEMMs
                     N.set_gemm_sms(self.shared_sms)

@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_E
 
 EXPORTS = ("moe_workspace_size", "moe_rows_capacity", "moe_route", "moe_route_select_bias",
            "moe_adjust_select_bias", "moe_dispatch",
-           "moe_dispatch_noalloc",
+           "moe_dispatch_noalloc", "moe_dispatch_noalloc_status",
            "moe_expert_up", "moe_expert_up_gather", "moe_expert_down", "moe_quantize_e4m3",
            "moe_expert_up_e4m3", "moe_expert_down_e4m3", "moe_grouped_ffn", "moe_combine",
            "moe_aux_stats", "moe_aux_loss_grad", "moe_bf16_to_f16", "moe_sync_status", "moe_status_string", "moe_launch_count",
@@ -53,6 +53,7 @@ _SIGS = {
     "moe_adjust_select_bias": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, _P]),
     "moe_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_dispatch_noalloc_status": (ctypes.c_int, [_P]),
     "moe_expert_up": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P]),
     "moe_expert_up_gather": (ctypes.c_int, [_CFG, _P, _P, _P, ctypes.c_int32, ctypes.c_int64, _P, _P,
                                             _P, _P]),
@@ -175,6 +176,12 @@ def dispatch_noalloc(cfg, x, topk_ids, counts, offsets, slot, src, x_perm, strea
     _check("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(
         ctypes.byref(cfg), _ptr(x), _ptr(topk_ids), _ptr(counts), _ptr(offsets), _ptr(slot),
         _ptr(src), _ptr(x_perm), _stream(stream)))
+
+
+def dispatch_noalloc_status(stream=None) -> int:
+    """Synchronise and return (then clear) the status code of the moe_dispatch_noalloc
+    calls on the current device (0 = OK) without raising."""
+    return lib().moe_dispatch_noalloc_status(_stream(stream))
 
 
 def expert_up(cfg, x_perm, offsets, n_groups, rows_cap, w1, h, ws, stream=None):

@@ -175,10 +175,14 @@ def _sustain(run, seconds):
     for _ in range(5):
         run()
     torch.cuda.synchronize()
-    smi = subprocess.Popen(["nvidia-smi", f"--id={torch.cuda.current_device()}",
-                            "--query-gpu=utilization.memory", "--format=csv,noheader,nounits",
-                            "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                           text=True)
+    # nvidia-smi is given the device's UUID: its own indices need not follow the CUDA
+    # ordinals (CUDA_VISIBLE_DEVICES, a leased GPU of a shared machine)
+    uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    smi = subprocess.Popen(["nvidia-smi", f"--id={uuid}",
+                            "--query-gpu=utilization.memory,clocks.sm,clocks.mem",
+                            "--format=csv,noheader,nounits", "-lms", "100"],
+                           stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
     a = torch.cuda.Event(enable_timing=True)
     z = torch.cuda.Event(enable_timing=True)
     t0, n = time.time(), 0
@@ -191,11 +195,20 @@ def _sustain(run, seconds):
     z.record()
     z.synchronize()
     smi.terminate()
-    out = smi.communicate()[0].split()
-    busy = sorted(int(v) for v in out[3:-2] if v.strip().isdigit())
+    rows = []
+    for line in smi.communicate()[0].splitlines()[3:-2]:  # drop the ramp at both ends
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) == 3 and all(p.isdigit() for p in parts):
+            rows.append([int(p) for p in parts])
+
+    def median(col):
+        v = sorted(r[col] for r in rows)
+        return v[len(v) // 2] if v else None
+    # utilization.memory is the fraction of sample periods the memory controller was busy,
+    # in whole percent: an indirect, time-based figure, not a byte count
     return {"sustained_ms": round(a.elapsed_time(z) / n, 5), "sustained_launches": n,
-            "mem_busy_pct_median": busy[len(busy) // 2] if busy else None,
-            "mem_busy_samples": len(busy)}
+            "gpu": uuid, "mem_busy_pct_median": median(0), "sm_mhz_median": median(1),
+            "mem_mhz_median": median(2), "mem_busy_samples": len(rows)}
 
 
 def _gemm_stage(stage, experts, wl, cfg, x, ids, counts, offsets, slot, src, ws, rows_cap, dev):

@@ -43,3 +43,34 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(1.5, 1) == 1.5
     assert abs(bench.whole_job_tokens_per_s(100, 4, 1, 2.0) - 200.0) < 1e-12
+
+
+def test_reference_half_layer_steps_are_one_layer_forward():
+    """The reference arm's two half-layer steps compute exactly the oracle's layer forward
+    (same library calls on the same blocks), so its tokens/s counts two steps as one
+    layer of T tokens."""
+    import numpy as np
+
+    import bench
+    from oracle import moe_oracle as O
+    from routing_dispatch_expert_04_b300.workloads import WORKLOADS, make_inputs
+    for name in ("tiny",):
+        wl = WORKLOADS[name]
+        inp = make_inputs(wl, "cpu", seed=0)
+        orc = bench.HalfLayerOracle(wl, inp)
+        orc.step()
+        orc.step()
+        ref = O.moe_forward(inp["x"].numpy(), inp["w_r"].numpy(), None, inp["w1"].numpy(),
+                            inp["w2"].numpy(), wl.K, O.capacity(wl.T, wl.E, wl.capacity_factor),
+                            wl.alpha)
+        assert np.array_equal(orc.y, ref["y"])
+
+
+def test_both_arms_print_the_same_config():
+    import bench
+    from routing_dispatch_expert_04_b300.workloads import WORKLOADS
+    wl = WORKLOADS["mixtral"]
+    c = bench.workload_config(wl, 640, 1)
+    assert c == bench.workload_config(wl, 640, 1)
+    assert c["workload"].startswith("mixtral: T=4096 d=4096 E=8 K=2 F=16384")
+    assert set(c) == {"workload", "capacity", "parallelism", "l2"}

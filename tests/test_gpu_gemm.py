@@ -258,3 +258,52 @@ def test_expert_up_gather_bad_index_reported():
     h = torch.empty((100, Nn), dtype=torch.float16, device="cuda")
     N.expert_up_gather(cfg, x, src, off_t, G, 100, w1, h, ws)
     assert N.sync_status(ws) == 5  # MOE_ERR_DEVICE
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_grouped_ffn_through_the_abi(dtype):
+    """moe_grouped_ffn (both expert Linears, chained on the device through h) on a ragged
+    layout with an empty group, on the default plan, against the oracle's expert FFN:
+    h within its storage rounding, y_perm against the oracle applied to the h the GPU
+    stored (isolating the second Linear) and within the layer tolerance of the exact
+    expert output; rows past the groups untouched; bad arguments rejected before any
+    launch."""
+    offs = [0, 200, 200, 457, 1000, 1129]
+    G, rows, d, F = len(offs) - 1, offs[-1], 256, 512
+    rows_cap = rows + 32
+    cfg = N.make_config(rows, d, G, 1, F, dtype, -1)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    hdt = torch.float16 if dtype == "bf16" else torch.float32
+    x = _gen((rows_cap, d), 1.0, 11, tdt)
+    w1 = _gen((G, F, d), d ** -0.5, 12, tdt)
+    w2 = _gen((G, d, F), F ** -0.5, 13, tdt)
+    w2k = w2
+    if dtype == "bf16":  # the second Linear takes fp16 weights (converted once)
+        w2k = torch.empty(w2.shape, dtype=torch.float16, device="cuda")
+        N.bf16_to_f16(w2, w2k, ws)
+    h = torch.full((rows_cap, F), 7.0, dtype=hdt, device="cuda")
+    y = torch.full((rows_cap, d), 7.0, dtype=hdt, device="cuda")
+    off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
+    N.grouped_ffn(cfg, x, off_t, G, rows_cap, w1, w2k, h, y, ws)
+    assert N.sync_status(ws) == 0
+    xn, w1n, w2n = to_np(x), to_np(w1), to_np(w2)
+    hn, yn = h.float().cpu().numpy(), y.float().cpu().numpy()
+    sdt = "f16" if dtype == "bf16" else "f32"
+    for g in range(G):
+        lo, hi = offs[g], offs[g + 1]
+        if hi == lo:
+            continue
+        y_ref, h_ref = O.expert_ffn(xn[lo:hi], w1n[g], w2n[g])
+        assert_rounded_to(hn[lo:hi], h_ref, sdt)
+        assert_rounded_to(yn[lo:hi], O.linear(hn[lo:hi], w2n[g]), sdt)
+        assert rel_rms_err(yn[lo:hi], y_ref) <= (2e-2 if dtype == "bf16" else 1e-4)
+    assert (hn[rows:] == 7.0).all() and (yn[rows:] == 7.0).all()
+    with pytest.raises(N.MoeError):
+        N.grouped_ffn(cfg, x, off_t, 0, rows_cap, w1, w2k, h, y, ws)   # no groups
+    with pytest.raises(N.MoeError):
+        N.grouped_ffn(cfg, x, off_t, G, rows_cap, w1, None, h, y, ws)  # no W2
+    with pytest.raises(N.MoeError):
+        N.grouped_ffn(cfg, x.view(-1)[1:], off_t, G, rows_cap, w1, w2k, h, y, ws)  # misaligned x
+    N.grouped_ffn(cfg, x, off_t, G, 0, w1, w2k, h, y, ws)  # no rows: nothing to do
+    assert N.sync_status(ws) == 0

@@ -1,8 +1,8 @@
 """GPU parity: the CUDA library, called through its C ABI, against the fp64 oracle.
 
 Tolerances: routing ids, counts, offsets, slot, src and the drop mask are compared bit
-for bit when the routing kernels are fed the oracle's fp32 logits; routing weights and
-P_i within 1e-6 / 1e-5 relative (fp32 softmax against fp64); layer output
+for bit when the routing kernels are fed the oracle's fp32 logits; routing weights, P_i
+and L_aux within 1e-6 relative (fp32 softmax against fp64); layer output
 max|GPU - oracle| / RMS(oracle) <= 1e-4 for fp32 layers; for bf16 layers the same bound
 2e-2 applies to the error in excess of half an output ulp (bf16 rounding of the exact
 result alone reaches 0.02-0.04 of RMS on these shapes), and the literal value is
@@ -78,8 +78,8 @@ def _check_routing(g, L32, K, C, E, renorm=False, alpha=0.01, sel_bias=None, ord
     assert np.array_equal(g["src"][:R], plan["src"])
     f, P, l_aux = O.aux_stats(ids, p, E, alpha)
     assert np.array_equal(g["f"], f.astype(np.float32))
-    assert np.max(np.abs(g["P"] - P) / np.maximum(P, 1e-30)) <= 1e-5
-    assert abs(g["l_aux"] - l_aux) <= 1e-5 * l_aux
+    assert np.max(np.abs(g["P"] - P) / np.maximum(P, 1e-30)) <= 1e-6
+    assert abs(g["l_aux"] - l_aux) <= 1e-6 * l_aux
     return plan
 
 
@@ -263,12 +263,21 @@ SMALL = [
 @pytest.mark.parametrize("fused", [True, False], ids=["fused_dispatch", "copy_dispatch"])
 @pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
 def test_layer_end_to_end_small(wl, fused):
+    """The whole layer from x, the GPU computing its own router logits.  Outputs are
+    compared over the tokens no near tie can flip; at least 90% of them.  When a near
+    tie's capacity cascade leaves fewer, the case runs again with the GPU routing fed the
+    oracle's fp32 logits, where every token is comparable."""
     layer, ref, L32, C = _layer_case(wl, fused=fused)
     # router logits themselves
     Lg = to_np(layer.logits)
-    assert np.max(np.abs(Lg - L32) / (1 + np.abs(L32))) <= (1e-5 if wl.dtype == "bf16" else 1e-5)
+    assert np.max(np.abs(Lg - L32) / (1 + np.abs(L32))) <= 1e-5
     keep = comparable_tokens(L32, ref["ids"], wl.K, C)
-    assert keep.mean() > 0.3
+    if keep.mean() < 0.9:
+        print(f"{wl.name}: {keep.mean():.2%} comparable from the GPU's own logits; "
+              "rerun with the oracle's logits")
+        layer, ref, L32, C = _layer_case(wl, fused=fused, logits_from_oracle=True)
+        keep = np.ones(wl.T, dtype=bool)
+    assert keep.mean() >= 0.9
     y = to_np(layer.y)
     err, literal = layer_output_error(y[keep], ref["y"][keep], wl.dtype)
     print(f"{wl.name}: output error {err:.4g} (literal max|err|/rms {literal:.4g})")
@@ -296,8 +305,8 @@ def test_layer_stages_with_oracle_logits(wl, fused):
     assert rel_rms_err(to_np(layer.y_perm)[:R], ref["y_perm"]) <= tol
     err, literal = layer_output_error(to_np(layer.y), ref["y"], wl.dtype)
     assert err <= tol, (err, literal)
-    assert np.max(np.abs(to_np(layer.P) - ref["P"]) / ref["P"]) <= 1e-5
-    assert abs(layer.l_aux.item() - ref["l_aux"]) <= 1e-5 * ref["l_aux"]
+    assert np.max(np.abs(to_np(layer.P) - ref["P"]) / ref["P"]) <= 1e-6
+    assert abs(layer.l_aux.item() - ref["l_aux"]) <= 1e-6 * ref["l_aux"]
 
 
 @pytest.mark.parametrize("idx,order,cap", [(2, "slot", "assignments"), (3, "slot", "tokens"),
@@ -365,10 +374,52 @@ def test_determinism_two_runs():
 
 
 # ------------------------------------------------------------------ full-size workloads
-def _sampled_full_check(name, n_tokens=48, seed=0, max_rows=512):
-    """Full-size workload in the bench's launch configuration: routing in full against
-    the oracle's own logits (near ties excluded), the expert FFN on the first
-    ``max_rows`` packed rows of two experts and the layer output on a token sample."""
+class _ExpertWeights:
+    """Host fp32 copies of one expert's weights, fetched from the device once."""
+
+    def __init__(self, inp):
+        self.inp, self.cache = inp, {}
+
+    def __call__(self, e):
+        if e not in self.cache:
+            self.cache[e] = (to_np(self.inp["w1"][e]), to_np(self.inp["w2"][e]))
+        return self.cache[e]
+
+
+def _check_expert_rows(wl, layer, x_np, weights, e, chunk=1024):
+    """Every packed row of expert e as the GPU packed it: its x_perm rows are exactly the
+    token rows src // K name, and its h and y_perm rows match the oracle's FFN of those
+    token rows (h within its fp16 storage rounding, y_perm within the layer tolerance);
+    the oracle runs in chunks of rows.  Returns the number of rows compared."""
+    g_offs = to_np(layer.offsets)
+    lo, hi = int(g_offs[e]), int(g_offs[e + 1])
+    src = to_np(layer.src)[lo:hi].astype(np.int64)
+    assert ((src >= 0) & (src < wl.T * wl.K)).all()
+    toks = src // wl.K
+    w1, w2 = weights(e)
+    hdt = "f16" if wl.dtype == "bf16" else "f32"
+    for c0 in range(lo, hi, chunk):
+        c1 = min(hi, c0 + chunk)
+        rows = toks[c0 - lo:c1 - lo]
+        assert np.array_equal(to_np(layer.x_perm[c0:c1]), x_np[rows])
+        y_ref, h_ref = O.expert_ffn(x_np[rows], w1, w2)
+        assert_rounded_to(to_np(layer.h[c0:c1]), h_ref, hdt)
+        assert rel_rms_err(to_np(layer.y_perm[c0:c1]), y_ref) <= TOL[wl.dtype]
+    return hi - lo
+
+
+def _sampled_full_check(name, n_tokens=512, seed=0):
+    """Full-size workload in the bench's launch configuration (the default expert-GEMM
+    plan, copied dispatch):
+    - routing in full against the oracle's own logits (near ties and their capacity
+      cascade excluded; bit for bit everywhere when nothing is excluded);
+    - every packed row of two experts -- expert 0 and the most loaded other expert --
+      against the oracle's FFN of the rows the GPU packed (on the Mixtral shape this
+      includes each expert's rows 512-639, which the split plan's one-CTA kernel
+      computes; on the 64K shape the whole 8192-row top expert);
+    - the layer output on ``n_tokens`` sampled comparable tokens, each token's kept
+      experts evaluated by the oracle (Y = sum of routing weight x expert output, plus
+      the shared expert)."""
     wl = WORKLOADS[name]
     inp = make_inputs(wl, "cuda")
     layer = MoELayer.from_workload(wl, inp)
@@ -388,21 +439,13 @@ def _sampled_full_check(name, n_tokens=48, seed=0, max_rows=512):
         assert np.array_equal(to_np(layer.offsets), plan["offsets"])
         assert np.array_equal(to_np(layer.slot), plan["slot"].reshape(wl.T, wl.K))
     tol = TOL[wl.dtype]
-    # two experts' packed rows in full (GPU rows of those experts are the oracle's rows
-    # whenever routing agrees; compare via the oracle's own packing)
-    offs = plan["offsets"]
-    g_offs = to_np(layer.offsets)
-    for e in (0, wl.E - 1):
-        lo, hi = int(offs[e]), int(offs[e + 1])
-        if hi == lo or not np.array_equal(g_offs[e:e + 2], offs[e:e + 2]):
-            continue
-        hi = min(hi, lo + max_rows)
-        rows = plan["src"][lo:hi] // wl.K
-        y_ref, h_ref = O.expert_ffn(x_np[rows], to_np(inp["w1"][e]), to_np(inp["w2"][e]))
-        glo, ghi = int(g_offs[e]), int(g_offs[e]) + (hi - lo)
-        assert np.array_equal(to_np(layer.src)[glo:ghi] // wl.K, rows)
-        assert_rounded_to(to_np(layer.h[glo:ghi]), h_ref, "f16" if wl.dtype == "bf16" else "f32")
-        assert rel_rms_err(to_np(layer.y_perm[glo:ghi]), y_ref) <= tol
+    weights = _ExpertWeights(inp)
+    kept = np.diff(to_np(layer.offsets))
+    e_big = 1 + int(np.argmax(kept[1:])) if wl.E > 1 else 0
+    n_rows = 0
+    for e in sorted({0, e_big}):
+        n_rows += _check_expert_rows(wl, layer, x_np, weights, e)
+    print(f"{name}: {n_rows} packed rows of experts {sorted({0, e_big})} compared")
     # token sample: the oracle evaluates each sampled token's kept experts one by one
     rng = np.random.default_rng(seed)
     cand = np.nonzero(keep)[0]
@@ -416,13 +459,16 @@ def _sampled_full_check(name, n_tokens=48, seed=0, max_rows=512):
         sel = [(t_i, k) for t_i in range(len(toks)) for k in range(wl.K)
                if ids[toks[t_i], k] == e and keepmask[t_i, k]]
         rows = np.array([toks[t_i] for t_i, _ in sel])
-        ye, _ = O.expert_ffn(x_np[rows], to_np(inp["w1"][e]), to_np(inp["w2"][e]))
+        ye, _ = O.expert_ffn(x_np[rows], *weights(e))
         for j, (t_i, k) in enumerate(sel):
             Y[t_i] += w[t_i, k] * ye[j]
+        if e not in (0, e_big):
+            weights.cache.pop(e, None)
     if wl.shared:
         Y += O.dense_ffn(x_np[toks], to_np(inp["w1s"][0]), to_np(inp["w2s"][0]))
     err, literal = layer_output_error(to_np(layer.y)[toks], Y, wl.dtype)
-    print(f"{name}: sampled output error {err:.4g} (literal {literal:.4g})")
+    print(f"{name}: {len(toks)} sampled tokens, output error {err:.4g} (literal {literal:.4g})")
+    assert len(toks) >= min(n_tokens, wl.T // 2)
     assert err <= tol, (err, literal)
 
 
