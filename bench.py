@@ -157,8 +157,8 @@ def source_digest(*rel):
 
 
 GEMM_SOURCES = ["routing_dispatch_expert_04_b300/csrc/" + f
-                for f in ("gemm_tc.cu", "gemm_tc2.cu", "gemm_tc2t.cu", "tc_common.cuh",
-                          "tc_ptx.cuh")]
+                for f in ("gemm_tc.cu", "gemm_tc2.cu", "gemm_tc2t.cu", "gemm_tc2m.cu",
+                          "tc_common.cuh", "tc_ptx.cuh")]
 
 
 def recorded_traffic(kernel_key: str, digest: str):
@@ -451,7 +451,8 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local)
     pk = peaks()
     N.set_gemm_pairing({"auto": N.GEMM_AUTO, "single": N.GEMM_SINGLE, "pair": N.GEMM_PAIR,
-                        "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T}[args.gemm])
+                        "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T,
+                        "mixed": N.GEMM_MIXED}[args.gemm])
     do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
 
     m = measure(wl, args, dev, world, pk, with_traffic=True)
@@ -601,10 +602,12 @@ def main():
     ap.add_argument("--extra-workloads", default=",".join(EXTRA_WORKLOADS),
                     help="comma-separated workloads measured after the headline one and "
                          "reported in the line's `workloads` record ('none' to skip)")
-    ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t"], default="auto",
+    ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t", "mixed"],
+                    default="auto",
                     help="expert GEMM kernels: one CTA per 128-row tile, CTA pairs per "
                          "256-row tile, pairs for whole 256-row tiles + one CTA for the "
-                         "rest, pairs with the tokens on the MMA's N side, or the "
+                         "rest, pairs with the tokens on the MMA's N side, pairs for whole "
+                         "tiles + transposed pair tiles for the rest in one launch, or the "
                          "library's choice")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared expert beside the routed GEMMs (0: beside routing)")

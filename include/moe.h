@@ -314,6 +314,12 @@ moe_status_t moe_sync_status(void* ws, void* stream);
  *                   columns) on the MMA's M side and up to 256 of a group's rows on its
  *                   N side, sized to the group (rounded up to 32), so no group is padded
  *                   to 256 rows (row-gathered calls take MOE_GEMM_PAIR instead);
+ *   MOE_GEMM_MIXED  CTA pairs only, in one launch: each group's whole 256-row tiles as
+ *                   for MOE_GEMM_PAIR and its remaining rows (fewer than 256) as one
+ *                   transposed tile per 256-wide slab of output columns, as for
+ *                   MOE_GEMM_PAIR_T, so no group is padded to 256 rows and every weight
+ *                   slab is walked by one kernel (16-bit operands; E4M3 and row-gathered
+ *                   calls take MOE_GEMM_SPLIT instead);
  *   MOE_GEMM_AUTO   (default) pairs when the 256-row padding is at most 5% of the rows
  *                   (judged from the capacity), the split when the capacity reaches 256
  *                   rows, transposed pairs when the groups have no capacity bound, one
@@ -328,7 +334,8 @@ typedef enum {
   MOE_GEMM_SINGLE = 1,
   MOE_GEMM_PAIR = 2,
   MOE_GEMM_SPLIT = 3,
-  MOE_GEMM_PAIR_T = 4
+  MOE_GEMM_PAIR_T = 4,
+  MOE_GEMM_MIXED = 5
 } moe_gemm_pairing_t;
 moe_status_t moe_set_gemm_pairing(int32_t mode);
 

@@ -232,9 +232,6 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
   }
   const WsLayout L = ws_layout(c);
   uint32_t* hdr = (uint32_t*)ws;
-  // reset the scan ticket and descriptors (the status word at offset 0 is kept)
-  s = cuda_status(cudaMemsetAsync((char*)ws + 4, 0, L.desc + (size_t)L.nblk_scan * c.E * 8 - 4, st));
-  if (s != MOE_OK) return s;
   int skip = -1, spin = 0;
   take_scan_test_hook(&skip, &spin);
   int32_t* pos = (int32_t*)((char*)ws + L.pos);
@@ -462,7 +459,7 @@ moe_status_t moe_set_gemm_sms(int32_t n) {
 
 moe_status_t moe_set_gemm_pairing(int32_t mode) {
   if (mode != MOE_GEMM_AUTO && mode != MOE_GEMM_SINGLE && mode != MOE_GEMM_PAIR &&
-      mode != MOE_GEMM_SPLIT && mode != MOE_GEMM_PAIR_T)
+      mode != MOE_GEMM_SPLIT && mode != MOE_GEMM_PAIR_T && mode != MOE_GEMM_MIXED)
     return MOE_ERR_INVALID;
   g_gemm_pairing.store(mode);
   return MOE_OK;

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -21,7 +23,9 @@ __device__ __forceinline__ void raise_error(uint32_t* status, uint32_t bit) {
 }
 
 // ------------------------------------------------------------------ workspace layout
-// [0, 256)        header: u32 status, u32 scan ticket, u32 aux ticket
+// [0, 256)        header: u32 status, u32 scan ticket, u32 aux ticket, u32 scan blocks
+//                 finished, u32 scan epoch (the look-back descriptors of one dispatch call
+//                 carry its epoch, so no call has to clear those of the previous one)
 // desc            scan descriptors, nblk_scan * E * u64 (flag << 32 | value)
 // pos             A * i32, position of each assignment inside its expert (pre-drop)
 // ppart           E * nblk_route * f32, per-block sums of softmax probabilities
@@ -134,6 +138,31 @@ template <> struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
   __device__ __forceinline__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
 };
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while its predecessor on the stream is still running;
+// griddep_wait() blocks until that predecessor has completed and its memory operations
+// are visible (a no-op for a kernel launched the ordinary way), and griddep_launch() lets
+// the successor be scheduled once every block of this grid has issued it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// Launch with programmatic stream serialisation (see griddep_wait).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 v;

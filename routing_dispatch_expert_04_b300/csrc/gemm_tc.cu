@@ -359,7 +359,14 @@ cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const 
 // known to reach 256 rows (Mixtral shape: 0.50 -> 0.47-0.48 ms per GEMM), one CTA
 // otherwise, and for groups of unknown size (no capacity) the transposed pairs, which
 // size the token side of each tile to the group (DeepSeek-V3 shape).
-enum { PLAN_SINGLE = 0, PLAN_PAIR = 1, PLAN_SPLIT = 2, PLAN_PAIR_T = 3 };
+enum { PLAN_SINGLE = 0, PLAN_PAIR = 1, PLAN_SPLIT = 2, PLAN_PAIR_T = 3, PLAN_MIXED = 4 };
+
+cudaError_t launch_tc2m_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
+                           int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                           cudaStream_t st);
+cudaError_t launch_tc2m_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
+                             int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                             cudaStream_t st);
 
 cudaError_t launch_tc2t_up(const void* x_perm, const void* w1, void* h, const int32_t* offsets,
                            int G, int N, int Kd, int64_t rows_cap, uint32_t* hdr, int num_sms,
@@ -373,6 +380,7 @@ static int gemm_plan(int mode, int64_t rows_cap, int G, int64_t cap_per_group, i
   if (mode == MOE_GEMM_PAIR) return PLAN_PAIR;
   if (mode == MOE_GEMM_SPLIT) return PLAN_SPLIT;
   if (mode == MOE_GEMM_PAIR_T) return PLAN_PAIR_T;
+  if (mode == MOE_GEMM_MIXED) return PLAN_MIXED;
   if (N % 256 != 0) return PLAN_SINGLE;
   // groups of unknown size (no capacity): the transposed pairs size each token tile to
   // the group, so ragged groups pad to 32 rows, not 128 or 256
@@ -465,8 +473,11 @@ cudaError_t launch_tc_up(const void* a_in, const int32_t* gather_src, int gather
   int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
   const bool gather = gather_src != nullptr;
   if (plan == PLAN_PAIR_T && gather) plan = PLAN_PAIR;  // row gathers need rows on the M side
+  if (plan == PLAN_MIXED && gather) plan = PLAN_SPLIT;
   if (plan == PLAN_PAIR_T)
     return launch_tc2t_up(a_in, w1, h, offsets, G, N, Kd, rows_cap, hdr, num_sms, st);
+  if (plan == PLAN_MIXED)
+    return launch_tc2m_up(a_in, w1, h, offsets, G, N, Kd, rows_cap, hdr, num_sms, st);
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            TC_ROWS_ALL, gather_src, gather_k, gather_rows};
   if (plan == PLAN_SINGLE)
@@ -500,6 +511,8 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
   const int plan = gemm_plan(pair_mode, rows_cap, G, cap_per_group, N);
   if (plan == PLAN_PAIR_T)
     return launch_tc2t_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, hdr, num_sms, st);
+  if (plan == PLAN_MIXED)
+    return launch_tc2m_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, hdr, num_sms, st);
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            TC_ROWS_ALL};
   if (plan == PLAN_SINGLE)
@@ -547,7 +560,8 @@ cudaError_t launch_tc2t_down_e4m3(const void* hq, const float* sh, const void* w
 // epilogue weighs more (DeepSeek-V3 shape, B300: GEMM2 1.71 vs 1.26 ms on one CTA per
 // tile; GEMM1 1.44 vs 1.49 ms).
 static int gemm_plan_e4m3(int mode, int64_t rows_cap, int G, int64_t cap_per_group, int N) {
-  const int plan = gemm_plan(mode, rows_cap, G, cap_per_group, N);
+  int plan = gemm_plan(mode, rows_cap, G, cap_per_group, N);
+  if (plan == PLAN_MIXED) plan = PLAN_SPLIT;  // the mixed-tile kernel takes 16-bit operands
   if (mode != MOE_GEMM_AUTO) return plan;
   if (plan == PLAN_PAIR && cap_per_group < 512) return PLAN_SINGLE;
   if (plan == PLAN_PAIR_T) return PLAN_SINGLE;

@@ -107,11 +107,10 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config* cfg, const void* 
     return MOE_ERR_CUDA;
   }
   char* base = (char*)scratch;
-  // the chunk ticket and the descriptors must start at zero (the array keeps the previous
-  // call's contents); the status word at offset 0 is left alone, so that an error stays
-  // recorded until moe_dispatch_noalloc_status reads it
-  e = cudaMemsetAsync(base + 4, 0, L.desc + (size_t)L.nblk_scan * c.E * 8 - 4, st);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // the array keeps the previous call's contents: the scan's ticket is reset by the block
+  // that finishes a call last and its descriptors carry the call's epoch, so none of it
+  // needs clearing; the status word at offset 0 keeps an error until
+  // moe_dispatch_noalloc_status reads it
   uint32_t* hdr = (uint32_t*)base;
   int32_t* pos = (int32_t*)(base + L.pos);
   int skip = -1, spin = 0;

@@ -36,6 +36,9 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
                     const float* __restrict__ bias, const float* __restrict__ sel_bias) {
   __shared__ float s_p[ROUTE_WARPS][VPT * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the dispatch scan, launched as a programmatic dependent, may be scheduled as soon as
+  // every block of this grid has started; it waits for this grid's results
+  griddep_launch();
   float pacc[VPT];
   float sb[VPT];  // selection-only bias of this lane's experts (0 without one)
 #pragma unroll

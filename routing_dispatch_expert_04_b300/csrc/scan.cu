@@ -19,7 +19,11 @@
 // per expert with warp match/popc and a warp-private running count in shared memory;
 // one prefix over the warps turns those into chunk ranks.  The block publishes its
 // per-expert totals, and obtains the totals of all earlier chunks by a decoupled look-back with
-// one descriptor per (chunk, expert).  Every wait is bounded: past `spin_limit` polls
+// one descriptor per (chunk, expert), reading up to LOOKBACK_W of them per round.  The
+// descriptors carry the call's epoch and the last block to finish resets the ticket, so
+// consecutive calls need no clearing of the workspace in between.  Both kernels are
+// launched as programmatic dependents of their predecessor on the stream: they are
+// scheduled while it finishes and wait for its results (griddepcontrol) before reading them.  Every wait is bounded: past `spin_limit` polls
 // the block records a timeout in the status word and carries on, so the kernel always
 // terminates.  The last chunk knows the grand totals and writes counts and offsets.
 //
@@ -35,17 +39,49 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-constexpr unsigned long long FLAG_AGG = 1ull << 32;   // this chunk's own totals
-constexpr unsigned long long FLAG_INCL = 2ull << 32;  // totals of chunks 0..this one
+constexpr int LOOKBACK_W = 32;  // predecessor descriptors loaded per look-back round
+// Descriptor word: flag (2 bits) | epoch of the dispatch call (30 bits) | count (32 bits).
+// A descriptor counts as published only with the current call's epoch, so the previous
+// call's descriptors never need clearing.
+constexpr unsigned long long FLAG_AGG = 1ull << 62;   // this chunk's own totals
+constexpr unsigned long long FLAG_INCL = 2ull << 62;  // totals of chunks 0..this one
+constexpr unsigned long long FLAG_MASK = 3ull << 62;
+constexpr uint32_t EPOCH_MASK = 0x3FFFFFFFu;
+
+__device__ __forceinline__ unsigned long long epoch_tag(uint32_t epoch) {
+  return (unsigned long long)(epoch & EPOCH_MASK) << 32;
+}
 
 // Flat assignment index (t*K + k) of the i-th assignment in arrival order: token-major
 // (the identity) or slot-major (every token's k-th choice before any (k+1)-th).
 __device__ __forceinline__ int64_t arrival_to_flat(int64_t i, int slot_major, int Tn, int K) {
   return slot_major ? (i % Tn) * K + i / Tn : i;
+}
+
+// Lanes of the warp whose expert id equals this lane's: the ids compared bit plane by bit
+// plane with ballots (one per bit of E - 1, plus one separating invalid ids, -1), which
+// takes far fewer cycles than a match instruction when a warp holds many distinct ids.
+__device__ __forceinline__ uint32_t same_id_lanes(int e, int nbits) {
+  const uint32_t valid = __ballot_sync(0xffffffffu, e >= 0);
+  uint32_t m = e >= 0 ? valid : ~valid;
+#pragma unroll
+  for (int bit = 0; bit < 8; ++bit) {
+    if (bit < nbits) {
+      const bool on = (e >> bit) & 1;
+      const uint32_t plane = __ballot_sync(0xffffffffu, on);
+      m &= on ? plane : ~plane;
+    }
+  }
+  return m;
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS)
@@ -59,12 +95,19 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
   __shared__ int s_run[256];             // count of e in this chunk
   __shared__ int s_excl[256];            // count of e in all earlier chunks
   __shared__ int s_b;
+  __shared__ uint32_t s_epoch;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  if (tid == 0) s_b = (int)atomicAdd(&hdr[1], 1u);
+  griddep_wait();    // the ids come from the routing kernel
+  griddep_launch();  // the row copy may be scheduled once every chunk has started
+  if (tid == 0) {
+    s_b = (int)atomicAdd(&hdr[1], 1u);
+    s_epoch = *(volatile uint32_t*)&hdr[4];
+  }
   for (int i = tid; i < NW * 256; i += SCAN_THREADS) (&s_wrun[0][0])[i] = 0;
   __syncthreads();
   const int b = s_b;
+  const unsigned long long tag = epoch_tag(s_epoch);
   const int64_t base = (int64_t)b * SCAN_ITEMS;
   const int64_t wbase = base + (int64_t)warp * WITEMS;
   uint32_t lt;
@@ -86,10 +129,11 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
     }
   }
   // rank inside the warp's segment, 32 assignments at a time, in flat order
+  const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;
 #pragma unroll
   for (int r = 0; r < SCAN_IPT; ++r) {
     const int e = my_e[r];
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const uint32_t peers = same_id_lanes(e, nbits);
     const int run = (e >= 0) ? s_wrun[warp][e] : 0;
     my_r[r] = run + __popc(peers & lt);
     __syncwarp();
@@ -120,26 +164,45 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
     unsigned long long* mine = desc + (size_t)b * E + tid;
     int excl = 0;
     if (b == 0) {
-      if (publish) st_release_u64(mine, FLAG_INCL | (uint32_t)agg);
+      if (publish) st_release_u64(mine, FLAG_INCL | tag | (uint32_t)agg);
     } else {
-      if (publish) st_release_u64(mine, FLAG_AGG | (uint32_t)agg);
+      if (publish) st_release_u64(mine, FLAG_AGG | tag | (uint32_t)agg);
+      // the next LOOKBACK_W predecessors' descriptors are loaded together, then walked
+      // from the nearest: their values add up until an inclusive total ends the walk; an
+      // unpublished one is polled again.  Flag and value share one 64-bit word, so
+      // relaxed loads suffice and do not serialise as acquire loads would.
       int j = b - 1, spins = 0;
       while (j >= 0) {
-        const unsigned long long v = ld_acquire_u64(desc + (size_t)j * E + tid);
-        const unsigned long long flag = v & ~0xffffffffull;
-        if (flag == 0) {
+        unsigned long long v[LOOKBACK_W];
+#pragma unroll
+        for (int i = 0; i < LOOKBACK_W; ++i)
+          v[i] = (j - i >= 0) ? ld_relaxed_u64(desc + (size_t)(j - i) * E + tid) : (FLAG_INCL | tag);
+        int used = 0;
+        bool stop = false, blocked = false;
+#pragma unroll
+        for (int i = 0; i < LOOKBACK_W; ++i) {
+          if (!stop && !blocked) {
+            const unsigned long long flag = v[i] & FLAG_MASK;
+            if (flag == 0 || (v[i] & ~FLAG_MASK & ~0xffffffffull) != tag) {  // not yet published
+              blocked = true;
+            } else {
+              excl += (int)(uint32_t)v[i];
+              ++used;
+              stop = (flag == FLAG_INCL);
+            }
+          }
+        }
+        if (stop) break;
+        j -= used;
+        if (blocked) {
           if (++spins > spin_limit) {
             raise_error(hdr, DEV_ERR_TIMEOUT);
             break;
           }
           __nanosleep(64);
-          continue;
         }
-        excl += (int)(uint32_t)v;
-        if (flag == FLAG_INCL) break;
-        --j;
       }
-      if (publish) st_release_u64(mine, FLAG_INCL | (uint32_t)(excl + agg));
+      if (publish) st_release_u64(mine, FLAG_INCL | tag | (uint32_t)(excl + agg));
     }
     s_excl[tid] = excl;
   }
@@ -152,19 +215,38 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
   }
 
   if (b == nblk - 1) {  // block-uniform
+    // grand totals, kept counts, and their exclusive scan over the experts (a warp scan of
+    // each 32 experts, then the sums of the earlier warps)
+    int kept = 0;
     if (tid < E) {
       const int tot = s_excl[tid] + s_run[tid];
       counts[tid] = tot;
-      s_run[tid] = (C < 0) ? tot : min(tot, C);
+      kept = (C < 0) ? tot : min(tot, C);
     }
+    int incl = kept;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    __syncthreads();                      // every chunk count has been read
+    if (lane == 31) s_run[warp] = incl;  // warp totals
     __syncthreads();
-    if (tid == 0) {
-      int acc = 0;
-      offsets[0] = 0;
-      for (int e = 0; e < E; ++e) {
-        acc += s_run[e];
-        offsets[e + 1] = acc;
-      }
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += s_run[w];
+    if (tid < E) offsets[tid + 1] = before + incl;
+    if (tid == 0) offsets[0] = 0;
+  }
+  // the block that finishes last resets the ticket and starts a new epoch for the next
+  // call (every other block is done with the descriptors by then)
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&hdr[3], 1u) == (uint32_t)(nblk - 1)) {
+      hdr[1] = 0u;
+      hdr[3] = 0u;
+      hdr[4] = (s_epoch + 1u) & EPOCH_MASK;
+      __threadfence();
     }
   }
 }
@@ -178,6 +260,7 @@ dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids,
   __shared__ int s_slot[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = d / Elem<T>::PER16;
+  griddep_wait();  // positions and offsets come from the scan
   for (int t = blockIdx.x * 8 + warp; t < Tn; t += gridDim.x * 8) {
     if (lane < K) {
       const int64_t a = (int64_t)t * K + lane;
@@ -229,10 +312,11 @@ cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsig
                         int32_t* pos, int32_t* counts, int32_t* offsets, uint32_t* hdr,
                         int skip_block, int spin_limit, int slot_major, int Tn, int K,
                         cudaStream_t st) {
-  scan_kernel<<<nblk, SCAN_THREADS, 0, st>>>(ids, A, E, C, nblk, desc, pos, counts, offsets, hdr,
-                                              skip_block, spin_limit, slot_major, Tn, K);
+  const cudaError_t e = launch_dependent(scan_kernel, dim3(nblk), dim3(SCAN_THREADS), 0, st, ids, A,
+                                         E, C, nblk, desc, pos, counts, offsets, hdr, skip_block,
+                                         spin_limit, slot_major, Tn, K);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const int32_t* pos,
@@ -241,15 +325,16 @@ cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const 
                             int num_sms, cudaStream_t st) {
   const int want = (Tn + 7) / 8;
   const int grid = want < num_sms * 16 ? want : num_sms * 16;
+  cudaError_t e;
   if (dtype == MOE_BF16)
-    dispatch_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        (const __nv_bfloat16*)x, ids, pos, offsets, Tn, d, E, K, C, slot, src, (__nv_bfloat16*)xp,
-        rows_cap, hdr);
+    e = launch_dependent(dispatch_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
+                         (const __nv_bfloat16*)x, ids, pos, offsets, Tn, d, E, K, C, slot, src,
+                         (__nv_bfloat16*)xp, rows_cap, hdr);
   else
-    dispatch_kernel<float><<<grid, 256, 0, st>>>((const float*)x, ids, pos, offsets, Tn, d, E, K, C,
-                                                 slot, src, (float*)xp, rows_cap, hdr);
+    e = launch_dependent(dispatch_kernel<float>, dim3(grid), dim3(256), 0, st, (const float*)x, ids,
+                         pos, offsets, Tn, d, E, K, C, slot, src, (float*)xp, rows_cap, hdr);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

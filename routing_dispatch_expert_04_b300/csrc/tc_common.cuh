@@ -360,6 +360,72 @@ __device__ __forceinline__ bool epilogue_chunk(const uint32_t (&r)[32], int row,
   return bad;
 }
 
+// Epilogues of a transposed tile (output columns on the TMEM lanes, the tile's rows on
+// its columns), shared by the transposed-pair and the mixed-pair kernels.
+// Epilogue of the transposed tile: r[j] = C[tok0 + c0 + j, col] for j < 32.  E4M3
+// operands: the accumulator times the token row's scale, then the column's scale (the
+// order of the other kernels' epilogues, so every plan stores the same values).
+template <int EPI, int KIND>
+__device__ __forceinline__ bool epilogue_chunk_t(const uint32_t (&r)[32], int col, int tok_first,
+                                                 int tok_end, const TcArgs& args, float sb) {
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int tok = tok_first + j;
+    if (tok >= tok_end) break;
+    float v = __uint_as_float(r[j]);
+    if (KIND == OP_E4M3) v = __fmul_rn(__fmul_rn(v, args.a_scale[tok]), sb);
+    if (EPI == TC_EPI_GELU_F16 || EPI == TC_EPI_F16) {
+      const float a = EPI == TC_EPI_GELU_F16 ? gelu(v) : v;
+      bad |= !(fabsf(a) <= 65504.f);
+      ((__half*)args.out)[(size_t)tok * args.ldo + col] = __float2half_rn(a);
+    } else {
+      ((float*)args.out)[(size_t)tok * args.ldo + col] = v;
+    }
+  }
+  return bad;
+}
+
+// 16-bit outputs of the transposed tile: lane l holds column colbase + l of 32 tokens.
+// The warp's 32 x 32 block goes through its shared-memory buffer (token-major), so that
+// each lane then stores 16 contiguous bytes of one token row (four 16-byte stores per lane
+// instead of 32 two-byte ones).  Same values and range test as epilogue_chunk_t.
+template <int EPI, int KIND>
+__device__ __forceinline__ bool epilogue_chunk_t16(const uint32_t (&r)[32], int colbase, int lane,
+                                                   int tok_first, int tok_end, const TcArgs& args,
+                                                   float sb, __half* sbuf) {
+  const bool valid = colbase + lane < args.N;
+  float sa_l = 0.f;  // E4M3: the scale of token tok_first + lane
+  if (KIND == OP_E4M3 && tok_first + lane < tok_end) sa_l = args.a_scale[tok_first + lane];
+  bool bad = false;
+  __syncwarp();  // the previous chunk's reads of the buffer are done
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float a = __uint_as_float(r[j]), b = __uint_as_float(r[j + 1]);
+    if (KIND == OP_E4M3) {
+      a = __fmul_rn(__fmul_rn(a, __shfl_sync(0xffffffffu, sa_l, j)), sb);
+      b = __fmul_rn(__fmul_rn(b, __shfl_sync(0xffffffffu, sa_l, j + 1)), sb);
+    }
+    if (EPI == TC_EPI_GELU_F16) gelu2(a, b, a, b);
+    bad |= valid && ((tok_first + j < tok_end && !(fabsf(a) <= 65504.f)) ||
+                     (tok_first + j + 1 < tok_end && !(fabsf(b) <= 65504.f)));
+    sbuf[j * 32 + lane] = __float2half_rn(a);
+    sbuf[(j + 1) * 32 + lane] = __float2half_rn(b);
+  }
+  __syncwarp();
+  const int cg = (lane & 3) * 8;  // this lane's 8 columns of a token row
+  if (colbase + cg < args.N) {    // N is a multiple of 8: a group is all in or all out
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = (lane >> 2) + 8 * i;
+      if (tok_first + row < tok_end)
+        st_v4((__half*)args.out + (size_t)(tok_first + row) * args.ldo + colbase + cg,
+              *reinterpret_cast<const uint4*>(sbuf + row * 32 + cg));
+    }
+  }
+  return bad;
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn();
 

@@ -262,13 +262,14 @@ def launch_count() -> int:
     return lib().moe_launch_count()
 
 
-GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR, GEMM_SPLIT, GEMM_PAIR_T = 0, 1, 2, 3, 4
+GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR, GEMM_SPLIT, GEMM_PAIR_T, GEMM_MIXED = 0, 1, 2, 3, 4, 5
 
 
 def set_gemm_pairing(mode: int):
     """Kernel choice for the bf16 expert GEMMs: GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR,
-    GEMM_SPLIT (pairs for whole 256-row tiles, one CTA for the rest) or GEMM_PAIR_T
-    (pairs with the tokens on the MMA's N side)."""
+    GEMM_SPLIT (pairs for whole 256-row tiles, one CTA for the rest), GEMM_PAIR_T
+    (pairs with the tokens on the MMA's N side) or GEMM_MIXED (pairs for whole 256-row
+    tiles and transposed pair tiles for the rest, in one launch)."""
     _check("moe_set_gemm_pairing", lib().moe_set_gemm_pairing(mode))
 
 

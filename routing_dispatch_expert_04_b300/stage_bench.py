@@ -59,7 +59,8 @@ def main():
                     choices=["route", "dispatch", "combine", "expert_up", "expert_down"])
     ap.add_argument("--experts", choices=["bf16", "e4m3"], default="bf16",
                     help="operand format of the expert GEMM stages")
-    ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t"], default="auto",
+    ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t", "mixed"],
+                    default="auto",
                     help="expert-GEMM plan (moe_set_gemm_pairing) for the GEMM stages")
     ap.add_argument("--sustain", type=float, default=0.0,
                     help="also loop the stage back to back for this many seconds and report "
@@ -73,7 +74,8 @@ def main():
     args = ap.parse_args()
 
     N.set_gemm_pairing({"auto": N.GEMM_AUTO, "single": N.GEMM_SINGLE, "pair": N.GEMM_PAIR,
-                        "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T}[args.gemm])
+                        "split": N.GEMM_SPLIT, "pair_t": N.GEMM_PAIR_T,
+                        "mixed": N.GEMM_MIXED}[args.gemm])
     wl = WORKLOADS[args.workload]
     if args.tokens > 0:
         wl = wl.scaled(args.tokens)

@@ -68,11 +68,13 @@ def test_quantize_rows_bounded_on_device():
     assert (codes[10:] == 0x55).all()
 
 
-@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T, N.GEMM_AUTO],
-                ids=["single", "pair", "split", "pair_t", "auto"])
+@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T, N.GEMM_MIXED,
+                        N.GEMM_AUTO],
+                ids=["single", "pair", "split", "pair_t", "mixed", "auto"])
 def pairing(request):
     """Run the E4M3 GEMM on the one-CTA kernel, the CTA-pair kernel, the split of the two,
-    the transposed pair kernel and the default choice."""
+    the transposed pair kernel, the mixed-tile setting (which E4M3 runs as the split) and
+    the default choice."""
     N.set_gemm_pairing(request.param)
     yield request.param
     N.set_gemm_pairing(N.GEMM_AUTO)

@@ -30,11 +30,11 @@ def _gen(shape, std, seed, dtype):
     return (torch.randn(*shape, generator=g, device="cuda") * std).to(dtype)
 
 
-@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T],
-                ids=["single", "pair", "split", "pair_t"])
+@pytest.fixture(params=[N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T, N.GEMM_MIXED],
+                ids=["single", "pair", "split", "pair_t", "mixed"])
 def pairing(request):
-    """Run the case on the one-CTA kernel, the CTA-pair kernel, the split of the two and
-    the transposed pair kernel."""
+    """Run the case on the one-CTA kernel, the CTA-pair kernel, the split of the two, the
+    transposed pair kernel and the mixed-tile pair kernel."""
     N.set_gemm_pairing(request.param)
     yield request.param
     N.set_gemm_pairing(N.GEMM_AUTO)
@@ -181,7 +181,7 @@ def test_single_and_pair_kernels_agree_bitwise(fn):
     ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
     off_t = torch.tensor(offs, dtype=torch.int32, device="cuda")
     outs = []
-    for mode in (N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T):
+    for mode in (N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T, N.GEMM_MIXED):
         N.set_gemm_pairing(mode)
         try:
             if fn == "up":
@@ -198,9 +198,8 @@ def test_single_and_pair_kernels_agree_bitwise(fn):
             N.set_gemm_pairing(N.GEMM_AUTO)
         assert N.sync_status(ws) == 0
         outs.append(out.cpu())
-    assert torch.equal(outs[0], outs[1])
-    assert torch.equal(outs[0], outs[2])
-    assert torch.equal(outs[0], outs[3])
+    for i in range(1, len(outs)):
+        assert torch.equal(outs[0], outs[i]), i
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])

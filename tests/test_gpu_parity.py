@@ -527,8 +527,9 @@ def test_shared_expert_beside_routed_gemms_matches():
     layer.check_device_status()
 
 
-@pytest.mark.parametrize("mode", [N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T],
-                         ids=["single", "pair", "split", "pair_t"])
+@pytest.mark.parametrize("mode", [N.GEMM_SINGLE, N.GEMM_PAIR, N.GEMM_SPLIT, N.GEMM_PAIR_T,
+                                  N.GEMM_MIXED],
+                         ids=["single", "pair", "split", "pair_t", "mixed"])
 def test_gemm_sm_budget_gives_same_result(mode):
     """An expert GEMM limited to a few SMs computes the same values as on all of them."""
     offs = [0, 300, 812, 813, 1400]
@@ -611,3 +612,31 @@ def test_split_plan_captured_matches_eager_and_oracle():
         torch.cuda.synchronize()
         assert torch.equal(layer.y, y_eager)
     layer.check_device_status()
+
+
+def test_dispatch_reuses_its_workspace_across_calls_and_sizes():
+    """Consecutive dispatch calls on one workspace, with the scan spanning different
+    numbers of chunks (3, 1, 8, 3 chunks of 4096 assignments), each match the oracle's
+    plan: the scan's ticket is reset and its look-back descriptors carry each call's epoch,
+    so no stale descriptor of an earlier call is ever taken for a published one."""
+    E, K = 16, 2
+    cfg_big = N.make_config(16384, 8, E, K, 8, "bf16", 1500)
+    ws = torch.zeros(N.workspace_size(cfg_big), dtype=torch.uint8, device="cuda")
+    for i, T in enumerate((6000, 1000, 16384, 6000)):
+        cfg = N.make_config(T, 8, E, K, 8, "bf16", T * 3 // E // 2)
+        C = cfg.capacity
+        L32 = make_logits(T, E, seed=40 + i, ties=(i % 2 == 1)).numpy()
+        logits = torch.from_numpy(L32).cuda()
+        ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        slot = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        src = torch.empty(T * K, dtype=torch.int32, device="cuda")
+        N.route(cfg, None, None, None, logits, ids, w, ws)
+        N.dispatch(cfg, None, ids, counts, offsets, slot, src, None, ws)
+        assert N.sync_status(ws) == 0
+        plan = O.dispatch_plan(O.top_k(L32, K), E, C)
+        assert np.array_equal(to_np(counts), plan["counts"]), T
+        assert np.array_equal(to_np(offsets), plan["offsets"]), T
+        assert np.array_equal(to_np(slot).reshape(-1), plan["slot"]), T
