@@ -305,6 +305,11 @@ def measure(wl, args, dev, world, pk, with_traffic: bool):
 
     stage_ms = {n: [] for n in stage_names}
     step_ms = []
+    # the library's clock telemetry (SM cycles and nanoseconds summed over the tensor-core
+    # kernels' CTAs, at bytes 64..79 of each workspace) over the timed steps
+    workspaces = [w for w in (layer.ws, layer.ws_s) if w is not None]
+    for w in workspaces:
+        w[64:80].zero_()
     clocks = ClockSampler(dev)
     clocks.start()
     time.sleep(0.3)
@@ -323,6 +328,8 @@ def measure(wl, args, dev, world, pk, with_traffic: bool):
         torch.distributed.barrier()
     clk = clocks.stop()
     layer.check_device_status()
+    tele = sum(w[64:80].view(torch.int64) for w in workspaces).tolist()
+    clk["tensor_kernels_sm_mhz"] = round(tele[0] / tele[1] * 1e3, 1) if tele[1] > 0 else None
 
     local_s = sum(step_ms) / 1e3
     value = whole_job_tokens_per_s(wl.T, args.steps, world, local_s, dev)
@@ -402,6 +409,48 @@ def measure(wl, args, dev, world, pk, with_traffic: bool):
                 "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": round(achieved_tf / peak_tf, 4), "traffic": traffic,
                 "peak_source": peak_src, "algorithmic_flops_per_launch": dom_flops}
+    sus = pk.get("bf16_tflops_sustained")
+    if sus and args.experts == "bf16":
+        roofline["peak_sustained"] = sus
+        roofline["frac_of_sustained"] = round(achieved_tf / sus, 4)
+    mhz = clk.get("tensor_kernels_sm_mhz")
+    if mhz:
+        # dense bf16 rate of a B300 SM: 8192 flop per clock (M=128, N=256, K=16 per 128 clocks)
+        per_clock_peak = 148 * 8192 * mhz * 1e6 / 1e12 * (2 if args.experts == "e4m3" else 1)
+        roofline["sm_mhz_in_kernel"] = mhz
+        roofline["frac_of_peak_at_that_clock"] = round(achieved_tf / per_clock_peak, 4)
+
+    # ---- a layer with a shared expert overlaps it with routing and dispatch, so those
+    # stages share the GPU; the same step on one stream (shared expert after the routed
+    # experts) shows each stage on its own
+    serial = None
+    if layer.shared and layer.overlap:
+        layer.overlap = False
+        s_names = layer.stage_names()
+        s_marks = [torch.cuda.Event(enable_timing=True, external=True)
+                   for _ in range(len(s_names) + 1)]
+        layer.capture(x, marks=s_marks)
+        s_ms = {n: [] for n in s_names}
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            layer.replay()
+        for _ in range(args.steps):
+            flush.zero_()
+            layer.replay()
+            torch.cuda.synchronize()
+            for i, n in enumerate(s_names):
+                s_ms[n].append(s_marks[i].elapsed_time(s_marks[i + 1]))
+        layer.check_device_status()
+        s_avg = {n: sum(v) / len(v) for n, v in s_ms.items()}
+        serial = {"ms_median": {n: round(statistics.median(v), 4) for n, v in s_ms.items()},
+                  "ms_per_step": round(sum(s_avg.values()), 4),
+                  "dispatch_frac_of_hbm": round(gbs(bytes_dispatch, s_avg["dispatch"]) / hbm, 4),
+                  "combine_frac_of_hbm": round(gbs(bytes_combine, s_avg["combine"]) / hbm, 4),
+                  "note": "one stream: route, dispatch, routed experts, shared expert, combine, "
+                          "aux"}
+        layer.overlap = True
+        layer.capture(x)  # back to the overlapped graph for the end-to-end run
+    stages["serial_schedule"] = serial
 
     # ---- end to end through the public API with host buffers: every step uploads its
     # input from pinned host memory and downloads its output and aux statistics; the

@@ -92,6 +92,13 @@ typedef enum { MOE_DROP_TOKEN_MAJOR = 0, MOE_DROP_SLOT_MAJOR = 1 } moe_drop_orde
  * moe_route, moe_route_select_bias or moe_dispatch on that workspace. */
 size_t moe_workspace_size(const moe_config* cfg);
 
+/* Clock telemetry in the workspace: bytes [64, 80) of `ws` hold two uint64 counters to
+ * which every CTA of the tensor-core kernels (the router of bf16 layers and the expert
+ * GEMMs) adds the SM clock cycles and the nanoseconds it ran.  A caller may zero them,
+ * run calls, and read cycles / nanoseconds: the mean SM clock (GHz) those kernels ran at. */
+#define MOE_WS_CLOCK_CYCLES_OFFSET 64
+#define MOE_WS_CLOCK_NS_OFFSET 72
+
 /* Rows the packed buffers (src, x_perm, h, y_perm) must hold:
  * min(T*K, E*C) with dropping, T*K without. */
 int64_t moe_rows_capacity(const moe_config* cfg);
@@ -117,6 +124,30 @@ moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, co
 moe_status_t moe_route_select_bias(const moe_config* cfg, const void* x, const void* w_r,
                                    const float* b_r, const float* sel_bias, float* logits,
                                    int32_t* topk_ids, float* topk_w, void* ws, void* stream);
+
+/* Steps 1 and 2's plan in one pass, for token-major arrival order (cfg.drop_order =
+ * MOE_DROP_TOKEN_MAJOR, else MOE_ERR_UNSUPPORTED): moe_route -- or, with sel_bias given,
+ * moe_route_select_bias -- followed in the same kernel by the histogram, capacity and
+ * positions of moe_dispatch ("Top-K Routing and Capacity Factor"): each block of the
+ * routing kernel ranks its tokens' assignments per expert, and a decoupled look-back over
+ * the blocks gives every assignment its position in its expert.
+ *   x, w_r, b_r, sel_bias (nullable), logits, topk_ids, topk_w: as moe_route /
+ *     moe_route_select_bias;
+ *   counts [E], offsets [E+1]: as moe_dispatch;
+ *   ws: receives the positions, read by moe_dispatch_planned (and the probability sums
+ *     moe_aux_stats reduces).
+ * Results are those of moe_route (or moe_route_select_bias) followed by moe_dispatch. */
+moe_status_t moe_route_plan(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
+                            const float* sel_bias, float* logits, int32_t* topk_ids, float* topk_w,
+                            int32_t* counts, int32_t* offsets, void* ws, void* stream);
+
+/* Step 2's permutation after moe_route_plan on the same ws and topk_ids: slot, src and
+ * (x and x_perm given) the row copy x_perm[r] = x[src[r] / K], from the positions
+ * moe_route_plan left in ws.  Arguments and results as moe_dispatch; offsets is an input
+ * here (as moe_route_plan wrote it).  Token-major arrival order only. */
+moe_status_t moe_dispatch_planned(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                                  const int32_t* offsets, int32_t* slot, int32_t* src,
+                                  void* x_perm, void* ws, void* stream);
 
 /* Nudge the selection bias toward balance after a step (the bias-adjustment scheme of
  * the same section; the pages name it without a formula, and this rule is the reading
@@ -355,7 +386,8 @@ const char* moe_status_string(moe_status_t status);
 uint64_t moe_launch_count(void);
 
 /* Test hook for the bounded wait of the dispatch scan.  When skip_block >= 0, the next
- * moe_dispatch call makes scan block `skip_block` withhold its published counts, so its
+ * moe_dispatch, moe_dispatch_noalloc or moe_route_plan call makes block `skip_block` of
+ * its look-back withhold its published counts, so its
  * successor's wait runs out after `spin_limit` polls and records MOE_ERR_TIMEOUT in
  * the device status word; every block still terminates.  Results of that call are
  * invalid.  The hook disarms itself after one call; skip_block < 0 disarms it. */

@@ -9,8 +9,9 @@
 namespace moe {
 
 cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, int32_t* ids,
-                                float* w, float* ppart, int nblk, const float* lpart, int nsplit,
-                                const float* bias, const float* sel_bias, cudaStream_t st);
+                                float* w, float* ppart, const float* lpart, int nsplit,
+                                const float* bias, const float* sel_bias, const RoutePlan& plan,
+                                cudaStream_t st);
 cudaError_t launch_adjust_select_bias(const int32_t* counts, float* sel_bias, int E, int64_t A,
                                       float gamma, cudaStream_t st);
 cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsigned long long* desc,
@@ -24,7 +25,7 @@ cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const 
 cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const float* w,
                            const void* ys, void* y, int Tn, int d, int K, int num_sms,
                            cudaStream_t st);
-cudaError_t launch_aux(const int32_t* counts, const float* ppart, int nblk, int E, int Tn, int K,
+cudaError_t launch_aux(const int32_t* counts, const float* ppart, int E, int Tn, int K,
                        float alpha, float* f, float* P, float* l_aux, double* auxfp, uint32_t* hdr,
                        cudaStream_t st);
 cudaError_t launch_aux_grad(const float* logits, const float* f, int Tn, int E, float alpha,
@@ -151,11 +152,18 @@ int64_t moe_rows_capacity(const moe_config* cfg) {
 
 static moe_status_t route_impl(const moe_config* cfg, const void* x, const void* w_r,
                                const float* b_r, const float* sel_bias, float* logits,
-                               int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
+                               int32_t* topk_ids, float* topk_w, void* ws, void* stream,
+                               int32_t* counts = nullptr, int32_t* offsets = nullptr) {
   moe_status_t s = check_cfg(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
-  if (c.T == 0) return MOE_OK;  // nothing is read or written
+  const bool planned = counts != nullptr;
+  if (c.T == 0) {  // nothing is read; a plan is empty
+    if (!planned) return MOE_OK;
+    s = cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, (cudaStream_t)stream));
+    if (s != MOE_OK) return s;
+    return cuda_status(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1), (cudaStream_t)stream));
+  }
   if (!logits || !topk_ids || !topk_w || !ws) return MOE_ERR_INVALID;
   if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(ws))
     return MOE_ERR_INVALID;
@@ -180,9 +188,17 @@ static moe_status_t route_impl(const moe_config* cfg, const void* x, const void*
     }
     if (s != MOE_OK) return s;
   }
+  RoutePlan plan{};
+  plan.hdr = hdr;
+  if (planned) {
+    int skip = -1, spin = 0;
+    take_scan_test_hook(&skip, &spin);
+    plan = RoutePlan{(int32_t*)((char*)ws + L.pos), counts, offsets,
+                     (unsigned long long*)((char*)ws + L.rdesc), hdr, c.capacity, skip, spin};
+  }
   return cuda_status(launch_softmax_topk(logits, c.T, c.E, c.K, c.renormalize, topk_ids, topk_w,
-                                         (float*)((char*)ws + L.ppart), L.nblk_route, lpart,
-                                         L.router_splits, b_r, sel_bias, st));
+                                         (float*)((char*)ws + L.ppart), lpart, L.router_splits,
+                                         b_r, sel_bias, plan, st));
 }
 
 moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
@@ -195,6 +211,40 @@ moe_status_t moe_route_select_bias(const moe_config* cfg, const void* x, const v
                                    int32_t* topk_ids, float* topk_w, void* ws, void* stream) {
   if (sel_bias == nullptr) return MOE_ERR_INVALID;
   return route_impl(cfg, x, w_r, b_r, sel_bias, logits, topk_ids, topk_w, ws, stream);
+}
+
+moe_status_t moe_route_plan(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
+                            const float* sel_bias, float* logits, int32_t* topk_ids, float* topk_w,
+                            int32_t* counts, int32_t* offsets, void* ws, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->drop_order != MOE_DROP_TOKEN_MAJOR) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !aligned16(counts) || !aligned16(offsets)) return MOE_ERR_INVALID;
+  if (sel_bias != nullptr && ((uintptr_t)sel_bias & 3u)) return MOE_ERR_INVALID;
+  return route_impl(cfg, x, w_r, b_r, sel_bias, logits, topk_ids, topk_w, ws, stream, counts,
+                    offsets);
+}
+
+moe_status_t moe_dispatch_planned(const moe_config* cfg, const void* x, const int32_t* topk_ids,
+                                  const int32_t* offsets, int32_t* slot, int32_t* src,
+                                  void* x_perm, void* ws, void* stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (c.drop_order != MOE_DROP_TOKEN_MAJOR) return MOE_ERR_UNSUPPORTED;
+  const int A = c.T * c.K;
+  if (A == 0) return MOE_OK;  // nothing is read or written
+  if (!topk_ids || !offsets || !slot || !src || !ws) return MOE_ERR_INVALID;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID;
+  if (!aligned16(topk_ids) || !aligned16(offsets) || !aligned16(slot) || !aligned16(src) ||
+      !aligned16(ws))
+    return MOE_ERR_INVALID;
+  if (x != nullptr && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID;
+  const WsLayout L = ws_layout(c);
+  return cuda_status(launch_dispatch(c.dtype, x, topk_ids, (const int32_t*)((char*)ws + L.pos),
+                                     offsets, c.T, c.d, c.E, c.K, c.capacity, slot, src, x_perm,
+                                     rows_capacity(c), (uint32_t*)ws, num_sms(),
+                                     (cudaStream_t)stream));
 }
 
 moe_status_t moe_adjust_select_bias(const moe_config* cfg, const int32_t* counts, float* sel_bias,
@@ -395,7 +445,7 @@ moe_status_t moe_aux_stats(const moe_config* cfg, const int32_t* counts, const v
     return MOE_ERR_INVALID;
   const WsLayout L = ws_layout(c);
   char* w = (char*)const_cast<void*>(ws);
-  return cuda_status(launch_aux(counts, (const float*)(w + L.ppart), L.nblk_route, c.E, c.T, c.K,
+  return cuda_status(launch_aux(counts, (const float*)(w + L.ppart), c.E, c.T, c.K,
                                 c.alpha, f, P, l_aux, (double*)(w + L.auxfp), (uint32_t*)w,
                                 (cudaStream_t)stream));
 }

@@ -128,12 +128,14 @@ combine_kernel(const Tin* __restrict__ yp, const int32_t* __restrict__ slot,
 constexpr int AUX_THREADS = 128;
 
 __global__ void __launch_bounds__(AUX_THREADS)
-aux_kernel(const int32_t* __restrict__ counts, const float* __restrict__ ppart, int nblk, int E,
+aux_kernel(const int32_t* __restrict__ counts, const float* __restrict__ ppart, int E,
            int Tn, int K, float alpha, float* __restrict__ f, float* __restrict__ P,
            float* __restrict__ l_aux, double* auxfp, uint32_t* hdr) {
   __shared__ double s_red[AUX_THREADS];
   __shared__ bool s_last;
   const int e = blockIdx.x, tid = threadIdx.x;
+  // the partial sums' layout [E][nblk] follows the routing grid the routing call recorded
+  const int nblk = Tn > 0 ? (int)*(volatile uint32_t*)&hdr[HDR_ROUTE_NBLK] : 0;
   const float* row = ppart + (size_t)e * nblk;
   double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
   int b = tid;
@@ -257,11 +259,10 @@ cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const
   return cudaGetLastError();
 }
 
-cudaError_t launch_aux(const int32_t* counts, const float* ppart, int nblk, int E, int Tn, int K,
+cudaError_t launch_aux(const int32_t* counts, const float* ppart, int E, int Tn, int K,
                        float alpha, float* f, float* P, float* l_aux, double* auxfp, uint32_t* hdr,
                        cudaStream_t st) {
-  aux_kernel<<<E, AUX_THREADS, 0, st>>>(counts, ppart, nblk, E, Tn, K, alpha, f, P, l_aux, auxfp,
-                                        hdr);
+  aux_kernel<<<E, AUX_THREADS, 0, st>>>(counts, ppart, E, Tn, K, alpha, f, P, l_aux, auxfp, hdr);
   count_launch();
   return cudaGetLastError();
 }

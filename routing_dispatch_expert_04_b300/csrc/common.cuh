@@ -25,12 +25,16 @@ __device__ __forceinline__ void raise_error(uint32_t* status, uint32_t bit) {
 // ------------------------------------------------------------------ workspace layout
 // [0, 256)        header: u32 status, u32 scan ticket, u32 aux ticket, u32 scan blocks
 //                 finished, u32 scan epoch (the look-back descriptors of one dispatch call
-//                 carry its epoch, so no call has to clear those of the previous one)
+//                 carry its epoch, so no call has to clear those of the previous one), the
+//                 same three words of the routing kernel's plan, u32 routing blocks of the
+//                 last routing call; bytes 64..79 clock telemetry
 // desc            scan descriptors, nblk_scan * E * u64 (flag << 32 | value)
 // pos             A * i32, position of each assignment inside its expert (pre-drop)
-// ppart           E * nblk_route * f32, per-block sums of softmax probabilities
+// ppart           E * nblk * f32, per-block sums of softmax probabilities (nblk = the
+//                 routing grid of the last routing call, which it records in header word 8)
 // auxfp           E * f64, per-expert f_i * P_i for the final fixed-order sum
 // lpart           router_splits * T * E * f32, partial router logits (split-K router only)
+// rdesc           nblk_plan * E * u64, look-back descriptors of the routing kernel's plan
 constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_IPT = 16;
 constexpr int SCAN_ITEMS = SCAN_THREADS * SCAN_IPT;  // assignments per scan block
@@ -42,9 +46,29 @@ constexpr int ROUTE_WARPS = 8;
 // T=16384 E=128 0.045 vs 0.049 ms and T=8192 E=256 0.074 vs 0.115 ms with 1).
 inline int route_tpw(int T) { return T >= 32768 ? 4 : 1; }
 
+// Tokens per warp of the routing kernel when it also computes the dispatch plan: enough
+// that the grid stays near 256 blocks (at most 512), since the plan's look-back runs
+// across the blocks of a wave that finish together, at a cost that grows with their
+// number (measured on the Qwen3 and 64K shapes: 2048 blocks added 40-55 us to the routing
+// stage).  At most 4 tokens per warp above 128 experts (register budget of the per-lane
+// candidate lists).
+inline int route_plan_tpw(int T, int E) {
+  if (T <= ROUTE_WARPS * 256) return 1;
+  if (T <= ROUTE_WARPS * 4 * 512 || E > 128) return 4;
+  return E <= 64 ? 16 : 8;
+}
+inline int route_blocks(int T, int tpw) {
+  const int per = ROUTE_WARPS * tpw;
+  return (int)(((int64_t)T + per - 1) / per);
+}
+
+// Workspace header word holding the routing grid (blocks) of the last routing call: the
+// layout of the probability partial sums the aux statistics reduce.
+constexpr int HDR_ROUTE_NBLK = 8;
+
 struct WsLayout {
-  size_t desc, pos, ppart, auxfp, lpart, total;
-  int nblk_scan, nblk_route, router_splits;
+  size_t desc, pos, ppart, auxfp, lpart, rdesc, total;
+  int nblk_scan, nblk_route, nblk_plan, router_splits;
 };
 
 // CTAs of the tensor-core router that share one SM: its E <= 64 variants stage in at
@@ -74,23 +98,43 @@ inline WsLayout ws_layout(const moe_config& c) {
   WsLayout L;
   int64_t A = (int64_t)c.T * c.K;
   L.nblk_scan = (int)((A + SCAN_ITEMS - 1) / SCAN_ITEMS);
-  const int route_tokens = ROUTE_WARPS * route_tpw(c.T);  // tokens per route block
-  L.nblk_route = (int)(((int64_t)c.T + route_tokens - 1) / route_tokens);
+  // the routing kernel runs route_blocks(T, route_tpw(T)) blocks, or with the dispatch plan
+  // route_blocks(T, route_plan_tpw(T, E)); the per-block buffers hold the larger count
+  L.nblk_route = route_blocks(c.T, route_tpw(c.T));
+  L.nblk_plan = route_blocks(c.T, route_plan_tpw(c.T, c.E));
+  const int nblk_rmax = L.nblk_route > L.nblk_plan ? L.nblk_route : L.nblk_plan;
   size_t off = 256;
   L.desc = off;
   off = align_up(off + (size_t)L.nblk_scan * c.E * 8, 256);
   L.pos = off;
   off = align_up(off + (size_t)A * 4, 256);
   L.ppart = off;
-  off = align_up(off + (size_t)L.nblk_route * c.E * 4, 256);
+  off = align_up(off + (size_t)nblk_rmax * c.E * 4, 256);
   L.auxfp = off;
   off = align_up(off + (size_t)c.E * 8, 256);
   L.router_splits = router_splits(c);
   L.lpart = off;
   if (L.router_splits > 1) off = align_up(off + (size_t)L.router_splits * c.T * c.E * 4, 256);
+  L.rdesc = off;
+  off = align_up(off + (size_t)L.nblk_plan * c.E * 8, 256);
   L.total = off;
   return L;
 }
+
+// The dispatch plan computed in the routing kernel's tail (token-major arrival order,
+// moe_route_plan): each routing block takes its tokens by ticket, ranks its assignments
+// per expert in arrival order, and a decoupled look-back over the blocks (lookback.cuh)
+// turns the ranks into each assignment's position in its expert; the last block writes
+// counts and offsets.
+struct RoutePlan {
+  int32_t* pos;               // [T*K] position of each assignment in its expert
+  int32_t* counts;            // [E] assignments per expert before dropping
+  int32_t* offsets;           // [E+1] exclusive scan of the kept counts
+  unsigned long long* desc;   // [nblk_plan, E] look-back descriptors
+  uint32_t* hdr;              // workspace header (status, ticket, finished, epoch words)
+  int C;                      // capacity (< 0: no dropping)
+  int skip_block, spin_limit; // bounded-wait test hook
+};
 
 // ------------------------------------------------------------------ launch bookkeeping
 void count_launch();

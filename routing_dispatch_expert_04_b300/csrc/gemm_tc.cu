@@ -67,6 +67,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
   GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
 
+  const long long clk0 = clock64();
+  const uint64_t ns0 = globaltimer_ns();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
   const int n_tiles = (args.N + BN - 1) / BN;
@@ -239,6 +241,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
   }
 
+  if (threadIdx.x == 0) clock_telemetry_add(args.hdr, clk0, ns0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -62,6 +62,8 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
   GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
 
+  const long long clk0 = clock64();
+  const uint64_t ns0 = globaltimer_ns();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
@@ -239,6 +241,7 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   }
 
   __syncwarp();
+  if (threadIdx.x == 0) clock_telemetry_add(args.hdr, clk0, ns0);
   tc_fence_before();
   cluster_sync();
   tc_fence_after();

@@ -17,6 +17,7 @@
 #include <limits.h>
 
 #include "common.cuh"
+#include "lookback.cuh"
 
 namespace moe {
 
@@ -28,17 +29,43 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int VPT, int TPW>
+template <int VPT, int TPW, bool PLAN>
 __global__ void __launch_bounds__(ROUTE_WARPS * 32)
 softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
                     int32_t* __restrict__ ids, float* __restrict__ wout,
                     float* __restrict__ ppart, const float* __restrict__ lpart, int nsplit,
-                    const float* __restrict__ bias, const float* __restrict__ sel_bias) {
+                    const float* __restrict__ bias, const float* __restrict__ sel_bias,
+                    const RoutePlan plan) {
   __shared__ float s_p[ROUTE_WARPS][VPT * 32];
+  __shared__ int s_wcnt[PLAN ? ROUTE_WARPS : 1][PLAN ? 256 : 1];  // per-warp running counts
+  __shared__ int s_excl[PLAN ? 256 : 1];
+  __shared__ int s_blk;
+  __shared__ uint32_t s_epoch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the dispatch scan, launched as a programmatic dependent, may be scheduled as soon as
   // every block of this grid has started; it waits for this grid's results
   griddep_launch();
+  // the aux statistics read the layout of the partial sums (this grid's size) from here
+  if (blockIdx.x == 0 && threadIdx.x == 0) plan.hdr[HDR_ROUTE_NBLK] = gridDim.x;
+  int blk = blockIdx.x;
+  if (PLAN) {
+    // tokens go to blocks in ticket order, so every chunk the look-back waits for belongs
+    // to a block that has started
+    if (threadIdx.x == 0) {
+      s_blk = (int)atomicAdd(&plan.hdr[HDR_PLAN_TICKET], 1u);
+      s_epoch = *(volatile uint32_t*)&plan.hdr[HDR_PLAN_EPOCH];
+    }
+    for (int i = threadIdx.x; i < ROUTE_WARPS * 256; i += blockDim.x) (&s_wcnt[0][0])[i] = 0;
+    __syncthreads();
+    blk = s_blk;
+  }
+  int my_rank[TPW];  // PLAN: rank of this lane's assignment among the warp's earlier ones
+  int my_pick[TPW];  //   and its expert (-1: no assignment)
+#pragma unroll
+  for (int i = 0; i < TPW; ++i) {
+    my_rank[i] = 0;
+    my_pick[i] = -1;
+  }
   float pacc[VPT];
   float sb[VPT];  // selection-only bias of this lane's experts (0 without one)
 #pragma unroll
@@ -48,7 +75,7 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
     sb[j] = (sel_bias != nullptr && e < E) ? sel_bias[e] : 0.f;
   }
 
-  const int t0 = (blockIdx.x * ROUTE_WARPS + warp) * TPW;
+  const int t0 = (blk * ROUTE_WARPS + warp) * TPW;
   // the warp's token rows are loaded up front: one memory latency for all of them.  With
   // a split-K router the logits are the partial slices summed in slice order, plus the
   // bias; they are written back to `logits`.
@@ -198,6 +225,17 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
       ids[(size_t)t * K + lane] = my_id;
       wout[(size_t)t * K + lane] = my_w;
     }
+    if (PLAN) {
+      // a token's K experts are distinct, so lane k's expert is counted once per token;
+      // the warp's tokens are ranked in order
+      my_pick[i] = lane < K ? my_id : -1;
+      my_rank[i] = 0;
+      if (lane < K) {
+        my_rank[i] = s_wcnt[warp][my_id];
+        s_wcnt[warp][my_id] = my_rank[i] + 1;
+      }
+      __syncwarp();
+    }
   }
 #pragma unroll
   for (int j = 0; j < VPT; ++j) s_p[warp][lane + 32 * j] = pacc[j];
@@ -206,29 +244,73 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
     float acc = 0.f;
 #pragma unroll
     for (int w = 0; w < ROUTE_WARPS; ++w) acc += s_p[w][e];
-    ppart[(size_t)e * gridDim.x + blockIdx.x] = acc;
+    ppart[(size_t)e * gridDim.x + blk] = acc;
   }
+  if (!PLAN) return;
+
+  // ---- dispatch plan: exclusive prefix of the warps' counts per expert (the warps hold
+  // consecutive tokens), the block's count, then the look-back over the blocks
+  const int nblk = gridDim.x;
+  const unsigned long long tag = epoch_tag(s_epoch);
+  const int e = threadIdx.x;  // E <= 256 = blockDim
+  int agg = 0;
+  if (e < E) {
+#pragma unroll
+    for (int w = 0; w < ROUTE_WARPS; ++w) {
+      const int c = s_wcnt[w][e];
+      s_wcnt[w][e] = agg;
+      agg += c;
+    }
+    s_excl[e] = lookback_exclusive<16>(plan.desc + e, E, blk, agg, tag, blk != plan.skip_block,
+                                   plan.spin_limit, plan.hdr);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < TPW; ++i) {
+    const int t = t0 + i;
+    if (t < T && my_pick[i] >= 0)
+      plan.pos[(size_t)t * K + lane] = s_excl[my_pick[i]] + s_wcnt[warp][my_pick[i]] + my_rank[i];
+  }
+  if (blk == nblk - 1) {  // block-uniform
+    __syncthreads();
+    write_counts_offsets(e < E ? s_excl[e] + agg : 0, E, plan.C, plan.counts, plan.offsets,
+                         &s_wcnt[0][0]);
+  }
+  finish_lookback_call(plan.hdr, HDR_PLAN_TICKET, HDR_PLAN_DONE, HDR_PLAN_EPOCH, s_epoch, nblk);
 }
 
 // lpart == nullptr: `logits` is the input.  Otherwise the logits are the sum of nsplit
-// partial slices of lpart (+ bias), and are also written to `logits`.
+// partial slices of lpart (+ bias), and are also written to `logits`.  `plan` carries the
+// workspace header (always) and, for the dispatch plan, its buffers (plan->pos != null).
 cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, int32_t* ids,
-                                float* w, float* ppart, int nblk, const float* lpart, int nsplit,
-                                const float* bias, const float* sel_bias, cudaStream_t st) {
-  const dim3 grid(nblk), block(ROUTE_WARPS * 32);
-#define MOE_SOFTMAX_TOPK(V, P)                                                                  \
-  softmax_topk_kernel<V, P><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart, lpart, \
-                                                    nsplit, bias, sel_bias)
-  const bool four = route_tpw(T) == 4;
-  if (E <= 32) {
-    if (four) MOE_SOFTMAX_TOPK(1, 4); else MOE_SOFTMAX_TOPK(1, 1);
-  } else if (E <= 64) {
-    if (four) MOE_SOFTMAX_TOPK(2, 4); else MOE_SOFTMAX_TOPK(2, 1);
-  } else if (E <= 128) {
-    if (four) MOE_SOFTMAX_TOPK(4, 4); else MOE_SOFTMAX_TOPK(4, 1);
-  } else {
-    if (four) MOE_SOFTMAX_TOPK(8, 4); else MOE_SOFTMAX_TOPK(8, 1);
-  }
+                                float* w, float* ppart, const float* lpart, int nsplit,
+                                const float* bias, const float* sel_bias, const RoutePlan& plan,
+                                cudaStream_t st) {
+  const bool planned = plan.pos != nullptr;
+  const int tpw = planned ? route_plan_tpw(T, E) : route_tpw(T);
+  const dim3 grid(route_blocks(T, tpw)), block(ROUTE_WARPS * 32);
+#define MOE_SOFTMAX_TOPK(V, P, PL)                                                                \
+  softmax_topk_kernel<V, P, PL><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart,    \
+                                                         lpart, nsplit, bias, sel_bias, plan)
+#define MOE_SOFTMAX_TOPK_TPW(V)                                                                  \
+  do {                                                                                           \
+    if (!planned) {                                                                              \
+      if (tpw == 4) MOE_SOFTMAX_TOPK(V, 4, false); else MOE_SOFTMAX_TOPK(V, 1, false);           \
+    } else if (tpw == 16) {                                                                      \
+      if constexpr (V <= 2) MOE_SOFTMAX_TOPK(V, 16, true);                                       \
+    } else if (tpw == 8) {                                                                       \
+      if constexpr (V <= 4) MOE_SOFTMAX_TOPK(V, 8, true);                                        \
+    } else if (tpw == 4) {                                                                       \
+      MOE_SOFTMAX_TOPK(V, 4, true);                                                              \
+    } else {                                                                                     \
+      MOE_SOFTMAX_TOPK(V, 1, true);                                                              \
+    }                                                                                            \
+  } while (0)
+  if (E <= 32) MOE_SOFTMAX_TOPK_TPW(1);
+  else if (E <= 64) MOE_SOFTMAX_TOPK_TPW(2);
+  else if (E <= 128) MOE_SOFTMAX_TOPK_TPW(4);
+  else MOE_SOFTMAX_TOPK_TPW(8);
+#undef MOE_SOFTMAX_TOPK_TPW
 #undef MOE_SOFTMAX_TOPK
   count_launch();
   return cudaGetLastError();

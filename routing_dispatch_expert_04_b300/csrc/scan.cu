@@ -19,7 +19,7 @@
 // per expert with warp match/popc and a warp-private running count in shared memory;
 // one prefix over the warps turns those into chunk ranks.  The block publishes its
 // per-expert totals, and obtains the totals of all earlier chunks by a decoupled look-back with
-// one descriptor per (chunk, expert), reading up to LOOKBACK_W of them per round.  The
+// one descriptor per (chunk, expert), reading up to 32 of them per round.  The
 // descriptors carry the call's epoch and the last block to finish resets the ticket, so
 // consecutive calls need no clearing of the workspace in between.  Both kernels are
 // launched as programmatic dependents of their predecessor on the stream: they are
@@ -31,35 +31,9 @@
 // and copies the token's row once from HBM into each of its kept packed rows with
 // 16-byte loads and stores (a token with no kept row is not read).
 #include "common.cuh"
+#include "lookback.cuh"
 
 namespace moe {
-
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-constexpr int LOOKBACK_W = 32;  // predecessor descriptors loaded per look-back round
-// Descriptor word: flag (2 bits) | epoch of the dispatch call (30 bits) | count (32 bits).
-// A descriptor counts as published only with the current call's epoch, so the previous
-// call's descriptors never need clearing.
-constexpr unsigned long long FLAG_AGG = 1ull << 62;   // this chunk's own totals
-constexpr unsigned long long FLAG_INCL = 2ull << 62;  // totals of chunks 0..this one
-constexpr unsigned long long FLAG_MASK = 3ull << 62;
-constexpr uint32_t EPOCH_MASK = 0x3FFFFFFFu;
-
-__device__ __forceinline__ unsigned long long epoch_tag(uint32_t epoch) {
-  return (unsigned long long)(epoch & EPOCH_MASK) << 32;
-}
 
 // Flat assignment index (t*K + k) of the i-th assignment in arrival order: token-major
 // (the identity) or slot-major (every token's k-th choice before any (k+1)-th).
@@ -101,8 +75,8 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
   griddep_wait();    // the ids come from the routing kernel
   griddep_launch();  // the row copy may be scheduled once every chunk has started
   if (tid == 0) {
-    s_b = (int)atomicAdd(&hdr[1], 1u);
-    s_epoch = *(volatile uint32_t*)&hdr[4];
+    s_b = (int)atomicAdd(&hdr[HDR_SCAN_TICKET], 1u);
+    s_epoch = *(volatile uint32_t*)&hdr[HDR_SCAN_EPOCH];
   }
   for (int i = tid; i < NW * 256; i += SCAN_THREADS) (&s_wrun[0][0])[i] = 0;
   __syncthreads();
@@ -158,54 +132,9 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
     if (my_e[r] >= 0) my_r[r] += s_wrun[warp][my_e[r]];
 
   // decoupled look-back, one thread per expert
-  const bool publish = (b != skip_block);
-  if (tid < E) {
-    const int agg = s_run[tid];
-    unsigned long long* mine = desc + (size_t)b * E + tid;
-    int excl = 0;
-    if (b == 0) {
-      if (publish) st_release_u64(mine, FLAG_INCL | tag | (uint32_t)agg);
-    } else {
-      if (publish) st_release_u64(mine, FLAG_AGG | tag | (uint32_t)agg);
-      // the next LOOKBACK_W predecessors' descriptors are loaded together, then walked
-      // from the nearest: their values add up until an inclusive total ends the walk; an
-      // unpublished one is polled again.  Flag and value share one 64-bit word, so
-      // relaxed loads suffice and do not serialise as acquire loads would.
-      int j = b - 1, spins = 0;
-      while (j >= 0) {
-        unsigned long long v[LOOKBACK_W];
-#pragma unroll
-        for (int i = 0; i < LOOKBACK_W; ++i)
-          v[i] = (j - i >= 0) ? ld_relaxed_u64(desc + (size_t)(j - i) * E + tid) : (FLAG_INCL | tag);
-        int used = 0;
-        bool stop = false, blocked = false;
-#pragma unroll
-        for (int i = 0; i < LOOKBACK_W; ++i) {
-          if (!stop && !blocked) {
-            const unsigned long long flag = v[i] & FLAG_MASK;
-            if (flag == 0 || (v[i] & ~FLAG_MASK & ~0xffffffffull) != tag) {  // not yet published
-              blocked = true;
-            } else {
-              excl += (int)(uint32_t)v[i];
-              ++used;
-              stop = (flag == FLAG_INCL);
-            }
-          }
-        }
-        if (stop) break;
-        j -= used;
-        if (blocked) {
-          if (++spins > spin_limit) {
-            raise_error(hdr, DEV_ERR_TIMEOUT);
-            break;
-          }
-          __nanosleep(64);
-        }
-      }
-      if (publish) st_release_u64(mine, FLAG_INCL | tag | (uint32_t)(excl + agg));
-    }
-    s_excl[tid] = excl;
-  }
+  if (tid < E)
+    s_excl[tid] = lookback_exclusive<32>(desc + tid, E, b, s_run[tid], tag, b != skip_block, spin_limit,
+                                     hdr);
   __syncthreads();
 
 #pragma unroll
@@ -215,40 +144,10 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
   }
 
   if (b == nblk - 1) {  // block-uniform
-    // grand totals, kept counts, and their exclusive scan over the experts (a warp scan of
-    // each 32 experts, then the sums of the earlier warps)
-    int kept = 0;
-    if (tid < E) {
-      const int tot = s_excl[tid] + s_run[tid];
-      counts[tid] = tot;
-      kept = (C < 0) ? tot : min(tot, C);
-    }
-    int incl = kept;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += u;
-    }
-    __syncthreads();                      // every chunk count has been read
-    if (lane == 31) s_run[warp] = incl;  // warp totals
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; ++w) before += s_run[w];
-    if (tid < E) offsets[tid + 1] = before + incl;
-    if (tid == 0) offsets[0] = 0;
+    __syncthreads();  // every thread has read its chunk counts from s_run
+    write_counts_offsets(tid < E ? s_excl[tid] + s_run[tid] : 0, E, C, counts, offsets, s_run);
   }
-  // the block that finishes last resets the ticket and starts a new epoch for the next
-  // call (every other block is done with the descriptors by then)
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&hdr[3], 1u) == (uint32_t)(nblk - 1)) {
-      hdr[1] = 0u;
-      hdr[3] = 0u;
-      hdr[4] = (s_epoch + 1u) & EPOCH_MASK;
-      __threadfence();
-    }
-  }
+  finish_lookback_call(hdr, HDR_SCAN_TICKET, HDR_SCAN_DONE, HDR_SCAN_EPOCH, s_epoch, nblk);
 }
 
 template <typename T>

@@ -100,6 +100,16 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Clock telemetry: thread 0 of every CTA of the tensor-core kernels adds the SM cycles and
+// the nanoseconds it ran to two 64-bit counters at byte offset 64 of the workspace header,
+// so a caller can read the mean SM clock these kernels ran at (a power-limited GPU lowers
+// it under load, which no sampling from the host resolves at kernel time scales).
+__device__ __forceinline__ void clock_telemetry_add(uint32_t* hdr, long long c0, uint64_t t0) {
+  unsigned long long* acc = reinterpret_cast<unsigned long long*>(hdr + 16);
+  atomicAdd(&acc[0], (unsigned long long)(clock64() - c0));
+  atomicAdd(&acc[1], (unsigned long long)(tc::globaltimer_ns() - t0));
+}
+
 // One warp fills the group table: rows clamped to the buffer, m-tiles of BM rows, and
 // the exclusive prefix of tiles (mt * n_tiles) over the groups.
 template <int BM>

@@ -9,6 +9,10 @@ works": route, dispatch, expert GEMMs, combine), followed by the aux statistics:
       [-> shared expert: moe_expert_up / moe_expert_down over all tokens]
       -> moe_combine -> moe_aux_stats
 
+With token-major drop order the first two calls are moe_route_plan (the routing kernel
+computes the dispatch plan in its tail) and moe_dispatch_planned (slot/src and the row
+copy).
+
 Buffers are torch tensors (device memory only); every step runs in the library's
 kernels.
 """
@@ -24,8 +28,13 @@ class MoELayer:
     def __init__(self, T, d, E, K, F, dtype, capacity_factor, alpha, w_r, b_r, w1, w2,
                  w1s=None, w2s=None, renormalize=False, device="cuda", overlap=True,
                  drop_order="token", capacity_mode="tokens", sel_bias=None,
-                 fused_dispatch=False, experts="bf16", shared_sms=0):
-        """``shared_sms``: with a shared expert and ``overlap``, 0 (default) runs the shared
+                 fused_dispatch=False, experts="bf16", shared_sms=0, plan_in_route=True):
+        """``plan_in_route``: with token-major drop order (the default), the routing kernel
+        also computes the dispatch plan -- counts, offsets and every assignment's position
+        (moe_route_plan) -- and the dispatch step only builds slot/src and copies the rows
+        (moe_dispatch_planned); False runs the plan in the dispatch step (moe_route, then
+        moe_dispatch's own scan), as slot-major order always does.
+        ``shared_sms``: with a shared expert and ``overlap``, 0 (default) runs the shared
         expert beside routing and dispatch; n > 0 runs it on n SMs beside the routed expert
         GEMMs, which then get the other SMs (moe_set_gemm_sms).
         ``fused_dispatch``: the first expert Linear gathers its rows from x while loading
@@ -47,6 +56,7 @@ class MoELayer:
         else:
             raise ValueError(capacity_mode)
         self.cfg = N.make_config(T, d, E, K, F, dtype, C, renormalize, alpha, drop_order)
+        self.planned = bool(plan_in_route) and drop_order == "token"
         self.sel_bias = sel_bias
         self.T, self.d, self.E, self.K, self.F = T, d, E, K, F
         self.dtype = torch.float32 if dtype == "f32" else torch.bfloat16
@@ -137,24 +147,28 @@ class MoELayer:
     @classmethod
     def from_workload(cls, wl, inputs, device="cuda", renormalize=False, overlap=True,
                       drop_order="token", capacity_mode="tokens", sel_bias=None,
-                      fused_dispatch=False, experts="bf16", shared_sms=0):
+                      fused_dispatch=False, experts="bf16", shared_sms=0, plan_in_route=True):
         return cls(wl.T, wl.d, wl.E, wl.K, wl.F, wl.dtype, wl.capacity_factor, wl.alpha,
                    inputs["w_r"], inputs["b_r"], inputs["w1"], inputs["w2"],
                    inputs.get("w1s"), inputs.get("w2s"), renormalize=renormalize, device=device,
                    overlap=overlap, drop_order=drop_order, capacity_mode=capacity_mode,
                    sel_bias=sel_bias, fused_dispatch=fused_dispatch, experts=experts,
-                   shared_sms=shared_sms)
+                   shared_sms=shared_sms, plan_in_route=plan_in_route)
 
     # ---------------------------------------------------------------- stages
     def route(self, x, stream=None, logits_in=None):
-        """Router + softmax + top-K.  With ``logits_in`` (fp32 [T,E]) the router Linear is
-        skipped and those logits drive the routing."""
+        """Router + softmax + top-K (and, with ``planned``, the dispatch plan).  With
+        ``logits_in`` (fp32 [T,E]) the router Linear is skipped and those logits drive the
+        routing."""
         if logits_in is not None:
             self.logits.copy_(logits_in)
             x, w_r, b_r = None, None, None
         else:
             w_r, b_r = self.w_r, self.b_r
-        if self.sel_bias is None:
+        if self.planned:
+            N.route_plan(self.cfg, x, w_r, b_r, self.sel_bias, self.logits, self.ids, self.w,
+                         self.counts, self.offsets, self.ws, stream)
+        elif self.sel_bias is None:
             N.route(self.cfg, x, w_r, b_r, self.logits, self.ids, self.w, self.ws, stream)
         else:
             N.route_select_bias(self.cfg, x, w_r, b_r, self.sel_bias, self.logits, self.ids,
@@ -171,6 +185,10 @@ class MoELayer:
         """Routing plan (counts, offsets, slot, src); with the unfused dispatch also the
         row copy into x_perm."""
         copy = x is not None and not self.fused_dispatch
+        if self.planned:
+            N.dispatch_planned(self.cfg, x if copy else None, self.ids, self.offsets, self.slot,
+                               self.src, self.x_perm if copy else None, self.ws, stream)
+            return
         N.dispatch(self.cfg, x if copy else None, self.ids, self.counts, self.offsets, self.slot,
                    self.src, self.x_perm if copy else None, self.ws, stream)
 

@@ -21,7 +21,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_E
           4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_DEVICE"}
 
 EXPORTS = ("moe_workspace_size", "moe_rows_capacity", "moe_route", "moe_route_select_bias",
-           "moe_adjust_select_bias", "moe_dispatch",
+           "moe_route_plan", "moe_dispatch_planned", "moe_adjust_select_bias", "moe_dispatch",
            "moe_dispatch_noalloc", "moe_dispatch_noalloc_status",
            "moe_expert_up", "moe_expert_up_gather", "moe_expert_down", "moe_quantize_e4m3",
            "moe_expert_up_e4m3", "moe_expert_down_e4m3", "moe_grouped_ffn", "moe_combine",
@@ -50,6 +50,8 @@ _SIGS = {
     "moe_rows_capacity": (ctypes.c_int64, [_CFG]),
     "moe_route": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_route_select_bias": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route_plan": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_dispatch_planned": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_adjust_select_bias": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, _P]),
     "moe_dispatch": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -158,6 +160,21 @@ def route_select_bias(cfg, x, w_r, b_r, sel_bias, logits, topk_ids, topk_w, ws, 
     _check("moe_route_select_bias", lib().moe_route_select_bias(
         ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(b_r), _ptr(sel_bias), _ptr(logits),
         _ptr(topk_ids), _ptr(topk_w), _ptr(ws), _stream(stream)))
+
+
+def route_plan(cfg, x, w_r, b_r, sel_bias, logits, topk_ids, topk_w, counts, offsets, ws,
+               stream=None):
+    """Routing plus the dispatch plan (counts, offsets, positions in ws) in one kernel."""
+    _check("moe_route_plan", lib().moe_route_plan(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(b_r), _ptr(sel_bias), _ptr(logits),
+        _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(ws), _stream(stream)))
+
+
+def dispatch_planned(cfg, x, topk_ids, offsets, slot, src, x_perm, ws, stream=None):
+    """The dispatch permutation (slot, src, row copy) after moe_route_plan on the same ws."""
+    _check("moe_dispatch_planned", lib().moe_dispatch_planned(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_ids), _ptr(offsets), _ptr(slot), _ptr(src),
+        _ptr(x_perm), _ptr(ws), _stream(stream)))
 
 
 def adjust_select_bias(cfg, counts, sel_bias, gamma: float, stream=None):

@@ -3,8 +3,10 @@
     python -m routing_dispatch_expert_04_b300.stage_bench --stage dispatch --workload long \
         [--tokens T] [--iters N] [--warmup W]
 
-Stages: ``route`` (router Linear + softmax/top-K), ``dispatch`` (histogram/scan/capacity
-+ row permutation), ``combine`` (weighted gather back to token order), ``expert_up`` and
+Stages: ``route`` (router Linear + softmax/top-K), ``route_plan`` (the same with the
+dispatch plan in the routing kernel's tail), ``dispatch`` (histogram/scan/capacity + row
+permutation), ``dispatch_planned`` (slot/src and the row copy after ``route_plan``),
+``combine`` (weighted gather back to token order), ``expert_up`` and
 ``expert_down`` (the two grouped expert GEMMs, ``--experts bf16|e4m3``).  The routing that
 feeds the later stages is computed by the library from the workload's seeded inputs; the
 rows the GEMMs and the combine read are seeded values of the layer's scale (their cost
@@ -45,6 +47,10 @@ def stage_bytes(stage, wl, T, R, t_active, b, experts="bf16"):
         return wl.E * wl.F * wl.d * wb + R * n_in * ab + R * n_out * 2
     if stage == "route":
         return T * wl.d * b + wl.E * wl.d * b + T * wl.E * 4 * 2 + A * 8
+    if stage == "route_plan":  # + the positions written
+        return T * wl.d * b + wl.E * wl.d * b + T * wl.E * 4 * 2 + A * 12
+    if stage == "dispatch_planned":  # ids and positions read, slot written, rows copied
+        return t_active * wl.d * b + R * wl.d * b + A * 12 + R * 4
     if stage == "dispatch":
         return t_active * wl.d * b + R * wl.d * b + A * 12 + R * 4
     if stage == "combine":
@@ -56,7 +62,8 @@ def stage_bytes(stage, wl, T, R, t_active, b, experts="bf16"):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--stage", required=True,
-                    choices=["route", "dispatch", "combine", "expert_up", "expert_down"])
+                    choices=["route", "route_plan", "dispatch", "dispatch_planned", "combine",
+                             "expert_up", "expert_down"])
     ap.add_argument("--experts", choices=["bf16", "e4m3"], default="bf16",
                     help="operand format of the expert GEMM stages")
     ap.add_argument("--gemm", choices=["auto", "single", "pair", "split", "pair_t", "mixed"],
@@ -107,6 +114,15 @@ def main():
     if args.stage == "route":
         def run():
             N.route(cfg, x, inp["w_r"], inp["b_r"], logits, ids, w, ws)
+    elif args.stage == "route_plan":
+        def run():
+            N.route_plan(cfg, x, inp["w_r"], inp["b_r"], None, logits, ids, w, counts, offsets, ws)
+    elif args.stage == "dispatch_planned":
+        x_perm = torch.empty((rows_cap, d), dtype=x.dtype, device=dev)
+        N.route_plan(cfg, x, inp["w_r"], inp["b_r"], None, logits, ids, w, counts, offsets, ws)
+
+        def run():
+            N.dispatch_planned(cfg, x, ids, offsets, slot, src, x_perm, ws)
     elif args.stage == "dispatch":
         x_perm = torch.empty((rows_cap, d), dtype=x.dtype, device=dev)
 

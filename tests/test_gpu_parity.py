@@ -60,8 +60,30 @@ def _routing_only(T, E, K, C, L32, renorm=False, sel_bias=None, order="token"):
     N.dispatch(cfg, None, ids, counts, offsets, slot, src, None, ws)
     N.aux_stats(cfg, counts, ws, f, P, l)
     assert N.sync_status(ws) == 0
-    return dict(ids=to_np(ids), w=to_np(w), counts=to_np(counts), offsets=to_np(offsets),
-                slot=to_np(slot), src=to_np(src), f=to_np(f), P=to_np(P), l_aux=float(l.item()))
+    out = dict(ids=to_np(ids), w=to_np(w), counts=to_np(counts), offsets=to_np(offsets),
+               slot=to_np(slot), src=to_np(src), f=to_np(f), P=to_np(P), l_aux=float(l.item()))
+    if order == "token":
+        # the same routing with the dispatch plan computed in the routing kernel's tail
+        # (moe_route_plan + moe_dispatch_planned) on a fresh workspace: identical results
+        ws2 = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device=dev)
+        sel = None if sel_bias is None else torch.from_numpy(sel_bias).to(dev)
+        ids2, w2, counts2, offsets2, slot2 = (torch.empty_like(t) for t in (ids, w, counts, offsets, slot))
+        src2 = torch.full((R,), -7, dtype=torch.int32, device=dev)
+        f2, P2, l2 = torch.empty_like(f), torch.empty_like(P), torch.empty_like(l)
+        N.route_plan(cfg, None, None, None, sel, logits, ids2, w2, counts2, offsets2, ws2)
+        N.dispatch_planned(cfg, None, ids2, offsets2, slot2, src2, None, ws2)
+        N.aux_stats(cfg, counts2, ws2, f2, P2, l2)
+        assert N.sync_status(ws2) == 0
+        for a, b in ((ids, ids2), (w, w2), (counts, counts2), (offsets, offsets2), (slot, slot2),
+                     (f, f2)):
+            assert torch.equal(a, b)
+        Rk = int(offsets[-1].item())
+        assert torch.equal(src[:Rk], src2[:Rk])
+        # P's per-block partial sums follow the routing grid, which differs between the two
+        # paths above 2048 tokens: the planned path's P and L_aux are checked against the
+        # oracle like the others
+        out["planned"] = dict(P=to_np(P2), l_aux=float(l2.item()))
+    return out
 
 
 def _check_routing(g, L32, K, C, E, renorm=False, alpha=0.01, sel_bias=None, order="token"):
@@ -78,8 +100,11 @@ def _check_routing(g, L32, K, C, E, renorm=False, alpha=0.01, sel_bias=None, ord
     assert np.array_equal(g["src"][:R], plan["src"])
     f, P, l_aux = O.aux_stats(ids, p, E, alpha)
     assert np.array_equal(g["f"], f.astype(np.float32))
-    assert np.max(np.abs(g["P"] - P) / np.maximum(P, 1e-30)) <= 1e-6
-    assert abs(g["l_aux"] - l_aux) <= 1e-6 * l_aux
+    for res in (g, g.get("planned")):
+        if res is None:
+            continue
+        assert np.max(np.abs(res["P"] - P) / np.maximum(P, 1e-30)) <= 1e-6
+        assert abs(res["l_aux"] - l_aux) <= 1e-6 * l_aux
     return plan
 
 
@@ -212,6 +237,50 @@ def test_scan_timeout_is_reported_and_recovers():
     assert N.sync_status(ws) == 0  # cleared
     g = _routing_only(T, E, K, -1, L32)
     _check_routing(g, L32, K, -1, E)
+
+
+def test_route_plan_timeout_is_reported_and_recovers():
+    """The routing kernel's plan look-back under the same hook: one block withholds its
+    counts, its successor's bounded wait runs out, the kernel terminates and the status
+    word says so; the next call on the same workspace matches the oracle."""
+    T, E, K = 4000, 8, 2            # 500 routing blocks of 8 tokens
+    L32 = make_logits(T, E, seed=5).numpy()
+    cfg = N.make_config(T, 8, E, K, 8, "bf16", 600)
+    ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    logits = torch.from_numpy(L32).cuda()
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    slot = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    src = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    N.arm_scan_timeout(3, 2000)
+    N.route_plan(cfg, None, None, None, None, logits, ids, w, counts, offsets, ws)
+    assert N.sync_status(ws) == 4  # MOE_ERR_TIMEOUT
+    assert N.sync_status(ws) == 0
+    N.route_plan(cfg, None, None, None, None, logits, ids, w, counts, offsets, ws)
+    N.dispatch_planned(cfg, None, ids, offsets, slot, src, None, ws)
+    assert N.sync_status(ws) == 0
+    plan = O.dispatch_plan(O.top_k(L32, K), E, 600)
+    assert np.array_equal(to_np(offsets), plan["offsets"])
+    assert np.array_equal(to_np(slot).reshape(-1), plan["slot"])
+
+
+@pytest.mark.parametrize("idx", [2, 4, 5])
+def test_layer_plan_in_route_matches_separate_scan(idx):
+    """The layer with the dispatch plan in the routing kernel (default) and with the plan
+    in the dispatch step's own scan give identical outputs and statistics."""
+    wl = SMALL[idx]
+    inp = make_inputs(wl, "cuda")
+    a = MoELayer.from_workload(wl, inp, plan_in_route=True)
+    b = MoELayer.from_workload(wl, inp, plan_in_route=False)
+    assert a.planned and not b.planned
+    for layer in (a, b):
+        layer.forward(inp["x"])
+        layer.check_device_status()
+    torch.cuda.synchronize()
+    for name in ("ids", "counts", "offsets", "slot", "y", "f", "P", "l_aux"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
 
 
 def test_out_of_range_expert_id_reported():
