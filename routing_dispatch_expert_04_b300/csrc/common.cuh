@@ -46,16 +46,14 @@ constexpr int ROUTE_WARPS = 8;
 // T=16384 E=128 0.045 vs 0.049 ms and T=8192 E=256 0.074 vs 0.115 ms with 1).
 inline int route_tpw(int T) { return T >= 32768 ? 4 : 1; }
 
-// Tokens per warp of the routing kernel when it also computes the dispatch plan: enough
-// that the grid stays near 256 blocks (at most 512), since the plan's look-back runs
-// across the blocks of a wave that finish together, at a cost that grows with their
-// number (measured on the Qwen3 and 64K shapes: 2048 blocks added 40-55 us to the routing
-// stage).  At most 4 tokens per warp above 128 experts (register budget of the per-lane
-// candidate lists).
+// Tokens per warp of the routing kernel when it also computes the dispatch plan: the same
+// as without (so both paths sum the probabilities over the same token groups).  Larger
+// blocks for the plan's look-back measured no better: on the Qwen3 shape 512 blocks of 32
+// tokens took 70 us against 82 us for 2048 blocks of 8, both above the 39 + 8 us of the
+// unplanned routing plus the dispatch scan.
 inline int route_plan_tpw(int T, int E) {
-  if (T <= ROUTE_WARPS * 256) return 1;
-  if (T <= ROUTE_WARPS * 4 * 512 || E > 128) return 4;
-  return E <= 64 ? 16 : 8;
+  (void)E;
+  return route_tpw(T);
 }
 inline int route_blocks(int T, int tpw) {
   const int per = ROUTE_WARPS * tpw;
