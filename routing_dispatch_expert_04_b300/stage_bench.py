@@ -17,9 +17,9 @@ profiler capture should use.
 L2 is flushed (a 512 MiB device write) before every timed launch.  Prints one JSON line
 with the median time, the stage's algorithmic bytes and the achieved GB/s (and TFLOP/s
 for the GEMMs).  With ``--profile-range`` one more launch of the stage runs between
-cudaProfilerStart and cudaProfilerStop, for a profiler's range replay: the stage's kernels
-then run as in the layer (the split plan's two GEMM kernels concurrently), and the
-counters cover the whole stage.
+cudaProfilerStart and cudaProfilerStop, for a profiler's range replay: the counters then
+cover the whole stage, for the split plan both of its GEMM kernels (launched concurrently
+as in the layer; whether a profiler lets them overlap is the profiler's choice).
 """
 
 from __future__ import annotations
