@@ -34,8 +34,10 @@ __device__ __forceinline__ void raise_error(uint32_t* status, uint32_t bit) {
 //                 routing grid of the last routing call, which it records in header word 8)
 // auxfp           E * f64, per-expert f_i * P_i for the final fixed-order sum
 // lpart           router_splits * T * E * f32, partial router logits (split-K router only)
-// rdesc           nblk_plan * E * u64, look-back descriptors of the routing kernel's plan
+// rdesc           (nblk_plan + ceil(nblk_plan / PLAN_GROUP)) * E * u64, look-back descriptors of
+//                 the routing kernel's plan: one row per routing block, then one per group
 constexpr int SCAN_THREADS = 256;
+constexpr int PLAN_GROUP = 16;  // routing blocks per group of the plan's two-level look-back
 constexpr int SCAN_IPT = 16;
 constexpr int SCAN_ITEMS = SCAN_THREADS * SCAN_IPT;  // assignments per scan block
 constexpr int ROUTE_WARPS = 8;
@@ -114,7 +116,8 @@ inline WsLayout ws_layout(const moe_config& c) {
   L.lpart = off;
   if (L.router_splits > 1) off = align_up(off + (size_t)L.router_splits * c.T * c.E * 4, 256);
   L.rdesc = off;
-  off = align_up(off + (size_t)L.nblk_plan * c.E * 8, 256);
+  const int ngroup_plan = (L.nblk_plan + PLAN_GROUP - 1) / PLAN_GROUP;
+  off = align_up(off + (size_t)(L.nblk_plan + ngroup_plan) * c.E * 8, 256);
   L.total = off;
   return L;
 }
@@ -128,7 +131,7 @@ struct RoutePlan {
   int32_t* pos;               // [T*K] position of each assignment in its expert
   int32_t* counts;            // [E] assignments per expert before dropping
   int32_t* offsets;           // [E+1] exclusive scan of the kept counts
-  unsigned long long* desc;   // [nblk_plan, E] look-back descriptors
+  unsigned long long* desc;   // [nblk_plan + groups, E] look-back descriptors (blocks, then groups)
   uint32_t* hdr;              // workspace header (status, ticket, finished, epoch words)
   int C;                      // capacity (< 0: no dropping)
   int skip_block, spin_limit; // bounded-wait test hook

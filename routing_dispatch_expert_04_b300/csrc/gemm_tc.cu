@@ -313,24 +313,26 @@ static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int 
 }
 
 // N tile of an expert GEMM: 256, or 192 when 256-wide tiles would leave the last wave
-// of the persistent grid much emptier or waste columns.  The m-tile count is estimated
-// on the host from the row capacity (each group holds at most `cap_per_group` rows
-// when that is known).
-static int pick_bn(int64_t rows_cap, int G, int64_t cap_per_group, int N, int num_sms) {
+// of the persistent grid much emptier or waste columns.  The m-tile count (tiles of `bm`
+// rows) is estimated on the host from the row capacity (each group holds at most
+// `cap_per_group` rows when that is known); `slots` = tiles that run at once (CTAs, or
+// CTA pairs).  Qwen3 shape on pairs (B300): GEMM1 (F = 768: 384 tiles of 256 on 74 pairs,
+// 5.2 waves) 0.115 -> 0.109 ms with 192-wide tiles (512 tiles, 6.9 waves).
+static int pick_bn(int64_t rows_cap, int G, int64_t cap_per_group, int N, int slots, int bm) {
   int64_t m_tiles;
   if (cap_per_group > 0) {
     const int64_t per = cap_per_group < rows_cap ? cap_per_group : rows_cap;
-    m_tiles = (int64_t)G * ((per + TC_BM - 1) / TC_BM);
-    const int64_t bound = (rows_cap + TC_BM - 1) / TC_BM + G;
+    m_tiles = (int64_t)G * ((per + bm - 1) / bm);
+    const int64_t bound = (rows_cap + bm - 1) / bm + G;
     if (m_tiles > bound) m_tiles = bound;
   } else {
-    m_tiles = (rows_cap + TC_BM - 1) / TC_BM + G / 2;
+    m_tiles = (rows_cap + bm - 1) / bm + G / 2;
   }
   double best = -1.0;
   int best_bn = 256;
   for (int bn : {256, 192}) {
     const int64_t nt = (N + bn - 1) / bn;
-    const double waves = (double)(m_tiles * nt) / num_sms;
+    const double waves = (double)(m_tiles * nt) / slots;
     const double full_waves = (double)(int64_t)(waves + 0.999999);
     const double eff = waves / full_waves * ((double)N / (double)(nt * bn));
     if (eff > best + 0.02) {
@@ -343,11 +345,11 @@ static int pick_bn(int64_t rows_cap, int G, int64_t cap_per_group, int N, int nu
 
 cudaError_t launch_tc2_up(const void* a_in, const int32_t* gather_src, int gather_k,
                           int64_t gather_rows, const void* w1, void* h, const int32_t* offsets,
-                          int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
-                          int num_sms, cudaStream_t st);
+                          int G, int N, int Kd, int64_t rows_cap, int row_part, int bn,
+                          uint32_t* hdr, int num_sms, cudaStream_t st);
 cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
-                            int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
-                            int num_sms, cudaStream_t st);
+                            int G, int N, int Kd, int64_t rows_cap, int row_part, int bn,
+                            uint32_t* hdr, int num_sms, cudaStream_t st);
 
 // How the expert GEMM's rows are split between the kernels: one CTA per 128-row tile
 // for all rows, CTA pairs per 256-row tile for all rows, or pairs for each group's whole
@@ -461,7 +463,7 @@ static cudaError_t run_split(cudaStream_t st, PairFn pair, RestFn rest) {
 template <int EPI, int KIND, bool GATHER>
 static cudaError_t launch_tc_single(const void* A, const void* B, const TcArgs& a,
                                     int64_t cap_per_group, int num_sms, cudaStream_t st) {
-  if (pick_bn(a.rows_cap, a.G, cap_per_group, a.N, num_sms) == 192)
+  if (pick_bn(a.rows_cap, a.G, cap_per_group, a.N, num_sms, TC_BM) == 192)
     return launch_tc<192, 5, EPI, KIND, GATHER>(A, B, a, num_sms, st);
   return launch_tc<256, 4, EPI, KIND, GATHER>(A, B, a, num_sms, st);
 }
@@ -490,14 +492,16 @@ cudaError_t launch_tc_up(const void* a_in, const int32_t* gather_src, int gather
                                                                    num_sms, st);
   if (plan == PLAN_PAIR)
     return launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd,
-                         rows_cap, TC_ROWS_ALL, hdr, num_sms, st);
+                         rows_cap, TC_ROWS_ALL,
+                         pick_bn(rows_cap, G, cap_per_group, N, num_sms / 2, 256), hdr, num_sms,
+                         st);
   const int sp = split_pair_sms(cap_per_group, num_sms);
   a.row_part = TC_ROWS_REST256;
   return run_split(
       st,
       [&](cudaStream_t s) {
         return launch_tc2_up(a_in, gather_src, gather_k, gather_rows, w1, h, offsets, G, N, Kd,
-                             rows_cap, TC_ROWS_FULL256, hdr, sp, s);
+                             rows_cap, TC_ROWS_FULL256, 256, hdr, sp, s);
       },
       [&](cudaStream_t s) {
         return gather ? launch_tc_single<TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, 255,
@@ -521,15 +525,16 @@ cudaError_t launch_tc_down(const void* h, const void* w2h, void* y_perm, const i
   if (plan == PLAN_SINGLE)
     return launch_tc_single<TC_EPI_F16, OP_F16, false>(h, w2h, a, cap_per_group, num_sms, st);
   if (plan == PLAN_PAIR)
-    return launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_ALL, hdr,
+    return launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_ALL,
+                           pick_bn(rows_cap, G, cap_per_group, N, num_sms / 2, 256), hdr,
                            num_sms, st);
   const int sp = split_pair_sms(cap_per_group, num_sms);
   a.row_part = TC_ROWS_REST256;
   return run_split(
       st,
       [&](cudaStream_t s) {
-        return launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_FULL256, hdr,
-                               sp, s);
+        return launch_tc2_down(h, w2h, y_perm, offsets, G, N, Kd, rows_cap, TC_ROWS_FULL256, 256,
+                               hdr, sp, s);
       },
       [&](cudaStream_t s) {
         return launch_tc_single<TC_EPI_F16, OP_F16, false>(h, w2h, a, 255, num_sms - sp, s);

@@ -37,8 +37,9 @@ struct Tc2Layout {
   static constexpr int GRP_OFF = MISC_OFF + 16;
   static constexpr int TOTAL = GRP_OFF + (int)sizeof(GroupTable);
   static constexpr int ALLOC = TOTAL + 1024;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;  // BN in {128, 256}
-  static_assert(BN == 128 || BN == 256, "pair tiles are 128 or 256 wide");
+  // two accumulators of BN columns in a power-of-two allocation
+  static constexpr uint32_t TMEM_COLS = BN == 192 ? 512 : 2 * BN;
+  static_assert(BN == 128 || BN == 192 || BN == 256, "pair tiles are 128, 192 or 256 wide");
 };
 
 // Time an aborting CTA gives copies it cannot observe (they signal the other CTA's
@@ -279,14 +280,17 @@ static cudaError_t launch_tc2(const void* A, const void* B, const TcArgs& a, int
 
 // First expert Linear on CTA pairs, bf16 in, GELU fused, fp16 out, over the rows that
 // `row_part` selects; with `gather_src` the A rows are gathered from the token matrix.
+// `bn`: tile width, 256 or (without a gather) 192.
 cudaError_t launch_tc2_up(const void* a_in, const int32_t* gather_src, int gather_k,
                           int64_t gather_rows, const void* w1, void* h, const int32_t* offsets,
-                          int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
-                          int num_sms, cudaStream_t st) {
+                          int G, int N, int Kd, int64_t rows_cap, int row_part, int bn,
+                          uint32_t* hdr, int num_sms, cudaStream_t st) {
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, h, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            row_part, gather_src, gather_k, gather_rows};
   if (gather_src != nullptr)
     return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_BF16, true>(a_in, w1, a, num_sms, st);
+  if (bn == 192)
+    return launch_tc2<192, 7, TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, num_sms, st);
   return launch_tc2<256, 6, TC_EPI_GELU_F16, OP_BF16, false>(a_in, w1, a, num_sms, st);
 }
 
@@ -315,12 +319,13 @@ cudaError_t launch_tc2_down_e4m3(const void* hq, const float* sh, const void* w2
   return launch_tc2<256, 6, TC_EPI_F16, OP_E4M3, false>(hq, w2q, a, num_sms, st);
 }
 
-// Second expert Linear on CTA pairs, fp16 in, fp16 out.
+// Second expert Linear on CTA pairs, fp16 in, fp16 out; `bn` as for the first.
 cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const int32_t* offsets,
-                            int G, int N, int Kd, int64_t rows_cap, int row_part, uint32_t* hdr,
-                            int num_sms, cudaStream_t st) {
+                            int G, int N, int Kd, int64_t rows_cap, int row_part, int bn,
+                            uint32_t* hdr, int num_sms, cudaStream_t st) {
   TcArgs a{offsets, G, 0, N, Kd, rows_cap, y_perm, N, nullptr, hdr, 1, (Kd + TC_BK - 1) / TC_BK, 0,
            row_part};
+  if (bn == 192) return launch_tc2<192, 7, TC_EPI_F16, OP_F16, false>(h, w2h, a, num_sms, st);
   return launch_tc2<256, 6, TC_EPI_F16, OP_F16, false>(h, w2h, a, num_sms, st);
 }
 

@@ -249,7 +249,8 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
   if (!PLAN) return;
 
   // ---- dispatch plan: exclusive prefix of the warps' counts per expert (the warps hold
-  // consecutive tokens), the block's count, then the look-back over the blocks
+  // consecutive tokens), the block's count, then the two-level look-back over the blocks
+  // (groups of PLAN_GROUP blocks, then the groups)
   const int nblk = gridDim.x;
   const unsigned long long tag = epoch_tag(s_epoch);
   const int e = threadIdx.x;  // E <= 256 = blockDim
@@ -261,8 +262,9 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
       s_wcnt[w][e] = agg;
       agg += c;
     }
-    s_excl[e] = lookback_exclusive<16>(plan.desc + e, E, blk, agg, tag, blk != plan.skip_block,
-                                   plan.spin_limit, plan.hdr);
+    s_excl[e] = grouped_lookback_exclusive<PLAN_GROUP, 16>(
+        plan.desc + e, plan.desc + (size_t)nblk * E + e, E, blk, nblk, agg, tag,
+        blk != plan.skip_block, plan.spin_limit, plan.hdr);
   }
   __syncthreads();
 #pragma unroll

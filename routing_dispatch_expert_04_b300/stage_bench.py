@@ -19,7 +19,9 @@ with the median time, the stage's algorithmic bytes and the achieved GB/s (and T
 for the GEMMs).  With ``--profile-range`` one more launch of the stage runs between
 cudaProfilerStart and cudaProfilerStop, for a profiler's range replay: the counters then
 cover the whole stage, for the split plan both of its GEMM kernels (launched concurrently
-as in the layer; whether a profiler lets them overlap is the profiler's choice).
+as in the layer; whether a profiler lets them overlap is the profiler's choice).  With
+``--graph`` the stage is captured in a CUDA graph after the warm-up, and the timed and
+profiled launches are replays of it, as in the layer's step.
 """
 
 from __future__ import annotations
@@ -74,6 +76,9 @@ def main():
                          "its mean time and the memory controller's busy fraction (nvidia-smi)")
     ap.add_argument("--profile-range", action="store_true",
                     help="run one more launch between cudaProfilerStart/Stop")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the stage in a CUDA graph after the warm-up and time (and "
+                         "profile) its replays, as the layer's step runs it")
     ap.add_argument("--workload", default="long", choices=sorted(WORKLOADS))
     ap.add_argument("--tokens", type=int, default=0, help="override the token count T")
     ap.add_argument("--iters", type=int, default=20)
@@ -147,6 +152,13 @@ def main():
         flush.zero_()
         run()
     torch.cuda.synchronize()
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run()
+        run = graph.replay
+        run()
+        torch.cuda.synchronize()
     ms = []
     stream = torch.cuda.current_stream()
     for _ in range(args.iters):
