@@ -129,21 +129,24 @@ moe_status_t moe_route_select_bias(const moe_config* cfg, const void* x, const v
  * MOE_DROP_TOKEN_MAJOR, else MOE_ERR_UNSUPPORTED): moe_route -- or, with sel_bias given,
  * moe_route_select_bias -- followed in the same kernel by the histogram, capacity and
  * positions of moe_dispatch ("Top-K Routing and Capacity Factor"): each block of the
- * routing kernel ranks its tokens' assignments per expert, and a decoupled look-back over
- * the blocks gives every assignment its position in its expert.
+ * routing kernel ranks its tokens' assignments per expert and records its count per
+ * expert, and a second kernel (one block per expert) turns the counts into each block's
+ * count in the blocks before it and writes counts and offsets.  No kernel of this call
+ * waits for another block.
  *   x, w_r, b_r, sel_bias (nullable), logits, topk_ids, topk_w: as moe_route /
  *     moe_route_select_bias;
  *   counts [E], offsets [E+1]: as moe_dispatch;
- *   ws: receives the positions, read by moe_dispatch_planned (and the probability sums
- *     moe_aux_stats reduces).
+ *   ws: receives the ranks and per-block bases, read by moe_dispatch_planned (and the
+ *     probability sums moe_aux_stats reduces).
  * Results are those of moe_route (or moe_route_select_bias) followed by moe_dispatch. */
 moe_status_t moe_route_plan(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
                             const float* sel_bias, float* logits, int32_t* topk_ids, float* topk_w,
                             int32_t* counts, int32_t* offsets, void* ws, void* stream);
 
 /* Step 2's permutation after moe_route_plan on the same ws and topk_ids: slot, src and
- * (x and x_perm given) the row copy x_perm[r] = x[src[r] / K], from the positions
- * moe_route_plan left in ws.  Arguments and results as moe_dispatch; offsets is an input
+ * (x and x_perm given) the row copy x_perm[r] = x[src[r] / K]; an assignment's position
+ * in its expert is its rank plus its routing block's base, both left in ws by
+ * moe_route_plan.  Arguments and results as moe_dispatch; offsets is an input
  * here (as moe_route_plan wrote it).  Token-major arrival order only. */
 moe_status_t moe_dispatch_planned(const moe_config* cfg, const void* x, const int32_t* topk_ids,
                                   const int32_t* offsets, int32_t* slot, int32_t* src,
@@ -386,7 +389,7 @@ const char* moe_status_string(moe_status_t status);
 uint64_t moe_launch_count(void);
 
 /* Test hook for the bounded wait of the dispatch scan.  When skip_block >= 0, the next
- * moe_dispatch, moe_dispatch_noalloc or moe_route_plan call makes block `skip_block` of
+ * moe_dispatch or moe_dispatch_noalloc call makes block `skip_block` of
  * its look-back withhold its published counts, so its
  * successor's wait runs out after `spin_limit` polls and records MOE_ERR_TIMEOUT in
  * the device status word; every block still terminates.  Results of that call are

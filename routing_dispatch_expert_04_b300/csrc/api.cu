@@ -19,9 +19,12 @@ cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsig
                         int skip_block, int spin_limit, int slot_major, int Tn, int K,
                         cudaStream_t st);
 cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const int32_t* pos,
-                            const int32_t* offsets, int Tn, int d, int E, int K, int C,
-                            int32_t* slot, int32_t* src, void* xp, int64_t rows_cap, uint32_t* hdr,
-                            int num_sms, cudaStream_t st);
+                            const int32_t* base, int nbase, int tpb, const int32_t* offsets,
+                            int Tn, int d, int E, int K, int C, int32_t* slot, int32_t* src,
+                            void* xp, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                            cudaStream_t st);
+cudaError_t launch_plan_scan(int32_t* pcnt, int nblk, int E, int C, int32_t* ptot, int32_t* counts,
+                             int32_t* offsets, uint32_t* hdr, cudaStream_t st);
 cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const float* w,
                            const void* ys, void* y, int Tn, int d, int K, int num_sms,
                            cudaStream_t st);
@@ -190,15 +193,13 @@ static moe_status_t route_impl(const moe_config* cfg, const void* x, const void*
   }
   RoutePlan plan{};
   plan.hdr = hdr;
-  if (planned) {
-    int skip = -1, spin = 0;
-    take_scan_test_hook(&skip, &spin);
-    plan = RoutePlan{(int32_t*)((char*)ws + L.pos), counts, offsets,
-                     (unsigned long long*)((char*)ws + L.rdesc), hdr, c.capacity, skip, spin};
-  }
-  return cuda_status(launch_softmax_topk(logits, c.T, c.E, c.K, c.renormalize, topk_ids, topk_w,
-                                         (float*)((char*)ws + L.ppart), lpart, L.router_splits,
-                                         b_r, sel_bias, plan, st));
+  if (planned) plan = RoutePlan{(int32_t*)((char*)ws + L.pos), (int32_t*)((char*)ws + L.pcnt), hdr};
+  s = cuda_status(launch_softmax_topk(logits, c.T, c.E, c.K, c.renormalize, topk_ids, topk_w,
+                                      (float*)((char*)ws + L.ppart), lpart, L.router_splits, b_r,
+                                      sel_bias, plan, st));
+  if (s != MOE_OK || !planned) return s;
+  return cuda_status(launch_plan_scan(plan.pcnt, L.nblk_plan, c.E, c.capacity,
+                                      (int32_t*)((char*)ws + L.ptot), counts, offsets, hdr, st));
 }
 
 moe_status_t moe_route(const moe_config* cfg, const void* x, const void* w_r, const float* b_r,
@@ -242,9 +243,10 @@ moe_status_t moe_dispatch_planned(const moe_config* cfg, const void* x, const in
   if (x != nullptr && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID;
   const WsLayout L = ws_layout(c);
   return cuda_status(launch_dispatch(c.dtype, x, topk_ids, (const int32_t*)((char*)ws + L.pos),
-                                     offsets, c.T, c.d, c.E, c.K, c.capacity, slot, src, x_perm,
-                                     rows_capacity(c), (uint32_t*)ws, num_sms(),
-                                     (cudaStream_t)stream));
+                                     (const int32_t*)((char*)ws + L.pcnt), L.nblk_plan,
+                                     ROUTE_WARPS * route_plan_tpw(c.T), offsets, c.T, c.d, c.E,
+                                     c.K, c.capacity, slot, src, x_perm, rows_capacity(c),
+                                     (uint32_t*)ws, num_sms(), (cudaStream_t)stream));
 }
 
 moe_status_t moe_adjust_select_bias(const moe_config* cfg, const int32_t* counts, float* sel_bias,
@@ -289,9 +291,9 @@ moe_status_t moe_dispatch(const moe_config* cfg, const void* x, const int32_t* t
                               (unsigned long long*)((char*)ws + L.desc), pos, counts, offsets, hdr,
                               skip, spin, c.drop_order, c.T, c.K, st));
   if (s != MOE_OK) return s;
-  return cuda_status(launch_dispatch(c.dtype, x, topk_ids, pos, offsets, c.T, c.d, c.E, c.K,
-                                     c.capacity, slot, src, x_perm, rows_capacity(c), hdr,
-                                     num_sms(), st));
+  return cuda_status(launch_dispatch(c.dtype, x, topk_ids, pos, nullptr, 0, 1, offsets, c.T, c.d,
+                                     c.E, c.K, c.capacity, slot, src, x_perm, rows_capacity(c),
+                                     hdr, num_sms(), st));
 }
 
 static moe_status_t check_ffn_args(const moe_config* cfg, const void* in, const int32_t* offsets,

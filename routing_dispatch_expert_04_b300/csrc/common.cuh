@@ -25,19 +25,20 @@ __device__ __forceinline__ void raise_error(uint32_t* status, uint32_t bit) {
 // ------------------------------------------------------------------ workspace layout
 // [0, 256)        header: u32 status, u32 scan ticket, u32 aux ticket, u32 scan blocks
 //                 finished, u32 scan epoch (the look-back descriptors of one dispatch call
-//                 carry its epoch, so no call has to clear those of the previous one), the
-//                 same three words of the routing kernel's plan, u32 routing blocks of the
+//                 carry its epoch, so no call has to clear those of the previous one), two
+//                 unused words, u32 plan-scan blocks finished, u32 routing blocks of the
 //                 last routing call; bytes 64..79 clock telemetry
 // desc            scan descriptors, nblk_scan * E * u64 (flag << 32 | value)
-// pos             A * i32, position of each assignment inside its expert (pre-drop)
+// pos             A * i32, position of each assignment inside its expert (pre-drop); with
+//                 the plan in the routing kernel, its rank inside its routing block
 // ppart           E * nblk * f32, per-block sums of softmax probabilities (nblk = the
 //                 routing grid of the last routing call, which it records in header word 8)
 // auxfp           E * f64, per-expert f_i * P_i for the final fixed-order sum
 // lpart           router_splits * T * E * f32, partial router logits (split-K router only)
-// rdesc           (nblk_plan + ceil(nblk_plan / PLAN_GROUP)) * E * u64, look-back descriptors of
-//                 the routing kernel's plan: one row per routing block, then one per group
+// pcnt            E * nblk * i32, the routing kernel's plan: each routing block's count per
+//                 expert, replaced by the plan scan with the count in all earlier blocks
+// ptot            E * i32, each expert's total (plan scan)
 constexpr int SCAN_THREADS = 256;
-constexpr int PLAN_GROUP = 16;  // routing blocks per group of the plan's two-level look-back
 constexpr int SCAN_IPT = 16;
 constexpr int SCAN_ITEMS = SCAN_THREADS * SCAN_IPT;  // assignments per scan block
 constexpr int ROUTE_WARPS = 8;
@@ -49,14 +50,8 @@ constexpr int ROUTE_WARPS = 8;
 inline int route_tpw(int T) { return T >= 32768 ? 4 : 1; }
 
 // Tokens per warp of the routing kernel when it also computes the dispatch plan: the same
-// as without (so both paths sum the probabilities over the same token groups).  Larger
-// blocks for the plan's look-back measured no better: on the Qwen3 shape 512 blocks of 32
-// tokens took 70 us against 82 us for 2048 blocks of 8, both above the 39 + 8 us of the
-// unplanned routing plus the dispatch scan.
-inline int route_plan_tpw(int T, int E) {
-  (void)E;
-  return route_tpw(T);
-}
+// as without, so both paths sum the probabilities over the same token groups.
+inline int route_plan_tpw(int T) { return route_tpw(T); }
 inline int route_blocks(int T, int tpw) {
   const int per = ROUTE_WARPS * tpw;
   return (int)(((int64_t)T + per - 1) / per);
@@ -65,9 +60,11 @@ inline int route_blocks(int T, int tpw) {
 // Workspace header word holding the routing grid (blocks) of the last routing call: the
 // layout of the probability partial sums the aux statistics reduce.
 constexpr int HDR_ROUTE_NBLK = 8;
+// Header word counting the plan scan's finished blocks (reset by the last one).
+constexpr int HDR_PLAN_DONE = 7;
 
 struct WsLayout {
-  size_t desc, pos, ppart, auxfp, lpart, rdesc, total;
+  size_t desc, pos, ppart, auxfp, lpart, pcnt, ptot, total;
   int nblk_scan, nblk_route, nblk_plan, router_splits;
 };
 
@@ -99,9 +96,9 @@ inline WsLayout ws_layout(const moe_config& c) {
   int64_t A = (int64_t)c.T * c.K;
   L.nblk_scan = (int)((A + SCAN_ITEMS - 1) / SCAN_ITEMS);
   // the routing kernel runs route_blocks(T, route_tpw(T)) blocks, or with the dispatch plan
-  // route_blocks(T, route_plan_tpw(T, E)); the per-block buffers hold the larger count
+  // route_blocks(T, route_plan_tpw(T)); the per-block buffers hold the larger count
   L.nblk_route = route_blocks(c.T, route_tpw(c.T));
-  L.nblk_plan = route_blocks(c.T, route_plan_tpw(c.T, c.E));
+  L.nblk_plan = route_blocks(c.T, route_plan_tpw(c.T));
   const int nblk_rmax = L.nblk_route > L.nblk_plan ? L.nblk_route : L.nblk_plan;
   size_t off = 256;
   L.desc = off;
@@ -115,26 +112,22 @@ inline WsLayout ws_layout(const moe_config& c) {
   L.router_splits = router_splits(c);
   L.lpart = off;
   if (L.router_splits > 1) off = align_up(off + (size_t)L.router_splits * c.T * c.E * 4, 256);
-  L.rdesc = off;
-  const int ngroup_plan = (L.nblk_plan + PLAN_GROUP - 1) / PLAN_GROUP;
-  off = align_up(off + (size_t)(L.nblk_plan + ngroup_plan) * c.E * 8, 256);
+  L.pcnt = off;
+  off = align_up(off + (size_t)L.nblk_plan * c.E * 4, 256);
+  L.ptot = off;
+  off = align_up(off + (size_t)c.E * 4, 256);
   L.total = off;
   return L;
 }
 
-// The dispatch plan computed in the routing kernel's tail (token-major arrival order,
-// moe_route_plan): each routing block takes its tokens by ticket, ranks its assignments
-// per expert in arrival order, and a decoupled look-back over the blocks (lookback.cuh)
-// turns the ranks into each assignment's position in its expert; the last block writes
-// counts and offsets.
+// The dispatch plan computed with the routing (token-major arrival order, moe_route_plan):
+// the routing kernel ranks each block's assignments per expert in arrival order and
+// writes the block's count per expert; the plan scan turns the counts into each block's
+// count in all earlier blocks, and writes counts and offsets.  The dispatch adds the two.
 struct RoutePlan {
-  int32_t* pos;               // [T*K] position of each assignment in its expert
-  int32_t* counts;            // [E] assignments per expert before dropping
-  int32_t* offsets;           // [E+1] exclusive scan of the kept counts
-  unsigned long long* desc;   // [nblk_plan + groups, E] look-back descriptors (blocks, then groups)
-  uint32_t* hdr;              // workspace header (status, ticket, finished, epoch words)
-  int C;                      // capacity (< 0: no dropping)
-  int skip_block, spin_limit; // bounded-wait test hook
+  int32_t* pos;   // [T*K] rank of each assignment among its routing block's ones to its expert
+  int32_t* pcnt;  // [E, nblk] count of each expert in each routing block
+  uint32_t* hdr;  // workspace header
 };
 
 // ------------------------------------------------------------------ launch bookkeeping

@@ -1,8 +1,7 @@
 // The per-expert running count behind the capacity rule ("Top-K Routing and Capacity
 // Factor": an assignment is dropped when its expert already holds C assignments that
 // arrived before it), computed over chunks of the arrival-ordered assignment stream by
-// a single-pass decoupled look-back.  Shared by the dispatch scan (scan.cu) and the
-// routing kernel's plan tail (route.cu).
+// a single-pass decoupled look-back (the dispatch scan, scan.cu).
 //
 // Every chunk, in the order of an atomic ticket (so each chunk a block waits for is held
 // by a block that has already started), publishes per expert one descriptor word:
@@ -88,51 +87,6 @@ __device__ __forceinline__ int lookback_exclusive(unsigned long long* desc_e, in
   return excl;
 }
 
-// Two-level form for many chunks that publish at about the same time (one wave of
-// blocks, where the single-level walk would advance only W chunks per round trip).
-// Chunk b publishes its own count (level 0, desc0); the GS consecutive chunks of a group
-// read their group predecessors' counts; the group's last chunk publishes the group's
-// count and, after a look-back over the groups (level 1, desc1, the same protocol as
-// lookback_exclusive), the groups' inclusive total.  Returns the count of e in chunks
-// 0..b-1.  GS <= 32.
-template <int GS, int W>
-__device__ __forceinline__ int grouped_lookback_exclusive(unsigned long long* desc0_e,
-                                                          unsigned long long* desc1_e, int E,
-                                                          int b, int nchunk, int agg,
-                                                          unsigned long long tag, bool publish,
-                                                          int spin_limit, uint32_t* hdr) {
-  static_assert(GS >= 2 && GS <= 32, "group size");
-  if (publish) st_release_u64(desc0_e + (size_t)b * E, FLAG_AGG | tag | (uint32_t)agg);
-  const int g = b / GS, first = g * GS;
-  int intra = 0;
-  uint32_t pending = (b > first) ? (0xffffffffu >> (32 - (b - first))) : 0u;  // unread predecessors
-  int spins = 0;
-  while (pending) {
-    unsigned long long v[GS - 1];
-#pragma unroll
-    for (int j = 0; j < GS - 1; ++j)
-      v[j] = ((pending >> j) & 1u) ? ld_relaxed_u64(desc0_e + (size_t)(first + j) * E) : 0ull;
-#pragma unroll
-    for (int j = 0; j < GS - 1; ++j) {
-      if (((pending >> j) & 1u) && (v[j] & FLAG_MASK) != 0 &&
-          (v[j] & ~FLAG_MASK & ~0xffffffffull) == tag) {
-        intra += (int)(uint32_t)v[j];
-        pending &= ~(1u << j);
-      }
-    }
-    if (pending) {
-      if (++spins > spin_limit) {
-        raise_error(hdr, DEV_ERR_TIMEOUT);
-        break;
-      }
-      __nanosleep(64);
-    }
-  }
-  const bool last = (b - first == GS - 1) || (b == nchunk - 1);
-  return intra + lookback_exclusive<W>(desc1_e, E, g, intra + agg, tag, publish && last,
-                                       spin_limit, hdr);
-}
-
 // The last chunk's block: grand totals (counts, before dropping), kept = min(total, C)
 // (C < 0: all), and offsets = their exclusive scan over the experts (a warp scan of each
 // 32 experts, then the sums of the earlier warps).  `total` is expert tid's grand total
@@ -177,8 +131,7 @@ __device__ __forceinline__ void finish_lookback_call(uint32_t* hdr, int ticket, 
   }
 }
 
-// Workspace header words of the two look-back users.
+// Workspace header words of the dispatch scan's look-back.
 constexpr int HDR_SCAN_TICKET = 1, HDR_SCAN_DONE = 3, HDR_SCAN_EPOCH = 4;
-constexpr int HDR_PLAN_TICKET = 5, HDR_PLAN_DONE = 6, HDR_PLAN_EPOCH = 7;
 
 }  // namespace moe

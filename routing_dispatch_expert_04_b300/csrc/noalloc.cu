@@ -26,9 +26,10 @@ cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsig
                         int skip_block, int spin_limit, int slot_major, int Tn, int K,
                         cudaStream_t st);
 cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const int32_t* pos,
-                            const int32_t* offsets, int Tn, int d, int E, int K, int C,
-                            int32_t* slot, int32_t* src, void* xp, int64_t rows_cap, uint32_t* hdr,
-                            int num_sms, cudaStream_t st);
+                            const int32_t* base, int nbase, int tpb, const int32_t* offsets,
+                            int Tn, int d, int E, int K, int C, int32_t* slot, int32_t* src,
+                            void* xp, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                            cudaStream_t st);
 
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(4) << 20;
 
@@ -118,8 +119,8 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config* cfg, const void* 
   e = launch_scan(topk_ids, A, c.E, c.capacity, L.nblk_scan, (unsigned long long*)(base + L.desc),
                   pos, counts, offsets, hdr, skip, spin, c.drop_order, c.T, c.K, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_dispatch(c.dtype, x, topk_ids, pos, offsets, c.T, c.d, c.E, c.K, c.capacity, slot, src,
-                      x_perm, rows_capacity(c), hdr, sms, st);
+  e = launch_dispatch(c.dtype, x, topk_ids, pos, nullptr, 0, 1, offsets, c.T, c.d, c.E, c.K,
+                      c.capacity, slot, src, x_perm, rows_capacity(c), hdr, sms, st);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -13,11 +13,17 @@
 // The kernel also leaves, per block, the sum over its tokens of every expert's
 // probability; the aux-statistics kernel reduces those partial sums in a fixed order
 // to P_i, so the result is deterministic without floating-point atomics.
+//
+// With the dispatch plan (moe_route_plan) it also takes the capacity rule's first step
+// ("Top-K Routing and Capacity Factor": an expert keeps the first C assignments in
+// arrival order): every assignment's rank among its block's assignments to the same
+// expert, and the block's count per expert.  The plan scan (one block per expert) turns
+// the counts into each block's count in all earlier blocks and writes counts and
+// offsets; the dispatch adds the two.  No block waits for another.
 #include <math.h>
 #include <limits.h>
 
 #include "common.cuh"
-#include "lookback.cuh"
 
 namespace moe {
 
@@ -38,26 +44,16 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
                     const RoutePlan plan) {
   __shared__ float s_p[ROUTE_WARPS][VPT * 32];
   __shared__ int s_wcnt[PLAN ? ROUTE_WARPS : 1][PLAN ? 256 : 1];  // per-warp running counts
-  __shared__ int s_excl[PLAN ? 256 : 1];
-  __shared__ int s_blk;
-  __shared__ uint32_t s_epoch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the dispatch scan, launched as a programmatic dependent, may be scheduled as soon as
   // every block of this grid has started; it waits for this grid's results
   griddep_launch();
   // the aux statistics read the layout of the partial sums (this grid's size) from here
   if (blockIdx.x == 0 && threadIdx.x == 0) plan.hdr[HDR_ROUTE_NBLK] = gridDim.x;
-  int blk = blockIdx.x;
+  const int blk = blockIdx.x;
   if (PLAN) {
-    // tokens go to blocks in ticket order, so every chunk the look-back waits for belongs
-    // to a block that has started
-    if (threadIdx.x == 0) {
-      s_blk = (int)atomicAdd(&plan.hdr[HDR_PLAN_TICKET], 1u);
-      s_epoch = *(volatile uint32_t*)&plan.hdr[HDR_PLAN_EPOCH];
-    }
     for (int i = threadIdx.x; i < ROUTE_WARPS * 256; i += blockDim.x) (&s_wcnt[0][0])[i] = 0;
     __syncthreads();
-    blk = s_blk;
   }
   int my_rank[TPW];  // PLAN: rank of this lane's assignment among the warp's earlier ones
   int my_pick[TPW];  //   and its expert (-1: no assignment)
@@ -249,36 +245,112 @@ softmax_topk_kernel(float* __restrict__ logits, int T, int E, int K, int renorm,
   if (!PLAN) return;
 
   // ---- dispatch plan: exclusive prefix of the warps' counts per expert (the warps hold
-  // consecutive tokens), the block's count, then the two-level look-back over the blocks
-  // (groups of PLAN_GROUP blocks, then the groups)
+  // consecutive tokens), the block's count per expert, and each assignment's rank in
+  // the block
   const int nblk = gridDim.x;
-  const unsigned long long tag = epoch_tag(s_epoch);
-  const int e = threadIdx.x;  // E <= 256 = blockDim
-  int agg = 0;
-  if (e < E) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int agg = 0;
 #pragma unroll
     for (int w = 0; w < ROUTE_WARPS; ++w) {
       const int c = s_wcnt[w][e];
       s_wcnt[w][e] = agg;
       agg += c;
     }
-    s_excl[e] = grouped_lookback_exclusive<PLAN_GROUP, 16>(
-        plan.desc + e, plan.desc + (size_t)nblk * E + e, E, blk, nblk, agg, tag,
-        blk != plan.skip_block, plan.spin_limit, plan.hdr);
+    plan.pcnt[(size_t)e * nblk + blk] = agg;
   }
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < TPW; ++i) {
     const int t = t0 + i;
     if (t < T && my_pick[i] >= 0)
-      plan.pos[(size_t)t * K + lane] = s_excl[my_pick[i]] + s_wcnt[warp][my_pick[i]] + my_rank[i];
+      plan.pos[(size_t)t * K + lane] = s_wcnt[warp][my_pick[i]] + my_rank[i];
   }
-  if (blk == nblk - 1) {  // block-uniform
+}
+
+// Plan scan: block e replaces the counts of expert e in the routing blocks (pcnt row e)
+// by their exclusive prefix sums and records the total; the last block to finish writes
+// counts (the totals, before dropping) and offsets (the exclusive scan over the experts
+// of min(total, C), or of the totals when C < 0), and resets the finished counter.
+constexpr int PLAN_SCAN_THREADS = 256;
+constexpr int PLAN_SCAN_PER = 8;  // consecutive counts per thread in one pass
+
+__global__ void __launch_bounds__(PLAN_SCAN_THREADS)
+plan_scan_kernel(int32_t* __restrict__ pcnt, int nblk, int E, int C, int32_t* __restrict__ ptot,
+                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets, uint32_t* hdr) {
+  __shared__ int s_warp[PLAN_SCAN_THREADS / 32];
+  __shared__ bool s_last;
+  griddep_wait();    // the counts come from the routing kernel
+  griddep_launch();  // the dispatch may be scheduled; it waits for this grid
+  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t* row = pcnt + (size_t)e * nblk;
+  int carry = 0;
+  for (int b0 = 0; b0 < nblk; b0 += PLAN_SCAN_THREADS * PLAN_SCAN_PER) {
+    const int first = b0 + tid * PLAN_SCAN_PER;
+    int v[PLAN_SCAN_PER];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < PLAN_SCAN_PER; ++j) {
+      v[j] = first + j < nblk ? row[first + j] : 0;
+      sum += v[j];
+    }
+    // exclusive scan of the threads' sums: within the warp, then over the warps
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    write_counts_offsets(e < E ? s_excl[e] + agg : 0, E, plan.C, plan.counts, plan.offsets,
-                         &s_wcnt[0][0]);
+    int before = carry;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    int chunk = 0;
+    for (int w = 0; w < PLAN_SCAN_THREADS / 32; ++w) chunk += s_warp[w];
+    __syncthreads();  // s_warp is rewritten by the next pass
+    int run = before + incl - sum;
+#pragma unroll
+    for (int j = 0; j < PLAN_SCAN_PER; ++j) {
+      if (first + j < nblk) row[first + j] = run;
+      run += v[j];
+    }
+    carry += chunk;
   }
-  finish_lookback_call(plan.hdr, HDR_PLAN_TICKET, HDR_PLAN_DONE, HDR_PLAN_EPOCH, s_epoch, nblk);
+  if (tid == 0) {
+    ptot[e] = carry;
+    __threadfence();
+    s_last = atomicAdd(&hdr[HDR_PLAN_DONE], 1u) == (uint32_t)(gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;  // block-uniform
+  __threadfence();
+  int total = 0;
+  if (tid < E) total = *(volatile int32_t*)&ptot[tid];
+  // E <= 256 = blockDim: one thread per expert
+  int kept = tid < E ? ((C < 0) ? total : min(total, C)) : 0;
+  if (tid < E) counts[tid] = total;
+  int incl = kept;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += s_warp[w];
+  if (tid < E) offsets[tid + 1] = before + incl;
+  if (tid == 0) {
+    offsets[0] = 0;
+    hdr[HDR_PLAN_DONE] = 0u;
+  }
+}
+
+cudaError_t launch_plan_scan(int32_t* pcnt, int nblk, int E, int C, int32_t* ptot, int32_t* counts,
+                             int32_t* offsets, uint32_t* hdr, cudaStream_t st) {
+  const cudaError_t e = launch_dependent(plan_scan_kernel, dim3(E), dim3(PLAN_SCAN_THREADS), 0,
+                                         st, pcnt, nblk, E, C, ptot, counts, offsets, hdr);
+  count_launch();
+  return e;
 }
 
 // lpart == nullptr: `logits` is the input.  Otherwise the logits are the sum of nsplit
@@ -289,7 +361,7 @@ cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, 
                                 const float* bias, const float* sel_bias, const RoutePlan& plan,
                                 cudaStream_t st) {
   const bool planned = plan.pos != nullptr;
-  const int tpw = planned ? route_plan_tpw(T, E) : route_tpw(T);
+  const int tpw = planned ? route_plan_tpw(T) : route_tpw(T);
   const dim3 grid(route_blocks(T, tpw)), block(ROUTE_WARPS * 32);
 #define MOE_SOFTMAX_TOPK(V, P, PL)                                                                \
   softmax_topk_kernel<V, P, PL><<<grid, block, 0, st>>>(logits, T, E, K, renorm, ids, w, ppart,    \
@@ -298,14 +370,8 @@ cudaError_t launch_softmax_topk(float* logits, int T, int E, int K, int renorm, 
   do {                                                                                           \
     if (!planned) {                                                                              \
       if (tpw == 4) MOE_SOFTMAX_TOPK(V, 4, false); else MOE_SOFTMAX_TOPK(V, 1, false);           \
-    } else if (tpw == 16) {                                                                      \
-      if constexpr (V <= 2) MOE_SOFTMAX_TOPK(V, 16, true);                                       \
-    } else if (tpw == 8) {                                                                       \
-      if constexpr (V <= 4) MOE_SOFTMAX_TOPK(V, 8, true);                                        \
-    } else if (tpw == 4) {                                                                       \
-      MOE_SOFTMAX_TOPK(V, 4, true);                                                              \
     } else {                                                                                     \
-      MOE_SOFTMAX_TOPK(V, 1, true);                                                              \
+      if (tpw == 4) MOE_SOFTMAX_TOPK(V, 4, true); else MOE_SOFTMAX_TOPK(V, 1, true);             \
     }                                                                                            \
   } while (0)
   if (E <= 32) MOE_SOFTMAX_TOPK_TPW(1);

@@ -153,9 +153,10 @@ scan_kernel(const int32_t* __restrict__ ids, int A, int E, int C, int nblk,
 template <typename T>
 __global__ void __launch_bounds__(256)
 dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids,
-                const int32_t* __restrict__ pos, const int32_t* __restrict__ offsets, int Tn, int d,
-                int E, int K, int C, int32_t* __restrict__ slot, int32_t* __restrict__ src,
-                T* __restrict__ xp, int64_t rows_cap, uint32_t* hdr) {
+                const int32_t* __restrict__ pos, const int32_t* __restrict__ base, int nbase,
+                int tpb, const int32_t* __restrict__ offsets, int Tn, int d, int E, int K, int C,
+                int32_t* __restrict__ slot, int32_t* __restrict__ src, T* __restrict__ xp,
+                int64_t rows_cap, uint32_t* hdr) {
   __shared__ int s_slot[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = d / Elem<T>::PER16;
@@ -166,7 +167,9 @@ dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids,
       const int e = ids[a];
       int s = -1;
       if (e >= 0 && e < E) {
-        const int p = pos[a];
+        // with a per-block base (the plan from the routing kernel), pos is the rank inside
+        // the token's routing block of tpb tokens
+        const int p = pos[a] + (base != nullptr ? base[(size_t)e * nbase + t / tpb] : 0);
         if (C < 0 || p < C) s = offsets[e] + p;
       }
       if (s >= rows_cap) {
@@ -219,19 +222,21 @@ cudaError_t launch_scan(const int32_t* ids, int A, int E, int C, int nblk, unsig
 }
 
 cudaError_t launch_dispatch(int dtype, const void* x, const int32_t* ids, const int32_t* pos,
-                            const int32_t* offsets, int Tn, int d, int E, int K, int C,
-                            int32_t* slot, int32_t* src, void* xp, int64_t rows_cap, uint32_t* hdr,
-                            int num_sms, cudaStream_t st) {
+                            const int32_t* base, int nbase, int tpb, const int32_t* offsets,
+                            int Tn, int d, int E, int K, int C, int32_t* slot, int32_t* src,
+                            void* xp, int64_t rows_cap, uint32_t* hdr, int num_sms,
+                            cudaStream_t st) {
   const int want = (Tn + 7) / 8;
   const int grid = want < num_sms * 16 ? want : num_sms * 16;
   cudaError_t e;
   if (dtype == MOE_BF16)
     e = launch_dependent(dispatch_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
-                         (const __nv_bfloat16*)x, ids, pos, offsets, Tn, d, E, K, C, slot, src,
-                         (__nv_bfloat16*)xp, rows_cap, hdr);
+                         (const __nv_bfloat16*)x, ids, pos, base, nbase, tpb, offsets, Tn, d, E,
+                         K, C, slot, src, (__nv_bfloat16*)xp, rows_cap, hdr);
   else
     e = launch_dependent(dispatch_kernel<float>, dim3(grid), dim3(256), 0, st, (const float*)x, ids,
-                         pos, offsets, Tn, d, E, K, C, slot, src, (float*)xp, rows_cap, hdr);
+                         pos, base, nbase, tpb, offsets, Tn, d, E, K, C, slot, src, (float*)xp,
+                         rows_cap, hdr);
   count_launch();
   return e;
 }
