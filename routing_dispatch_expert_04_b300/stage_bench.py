@@ -76,6 +76,9 @@ def main():
                          "its mean time and the memory controller's busy fraction (nvidia-smi)")
     ap.add_argument("--profile-range", action="store_true",
                     help="run one more launch between cudaProfilerStart/Stop")
+    ap.add_argument("--library", action="store_true",
+                    help="GEMM stages: time cuBLAS (torch.bmm) on the same expert GEMMs instead "
+                         "of this library's kernels; needs equal rows in every expert")
     ap.add_argument("--graph", action="store_true",
                     help="capture the stage in a CUDA graph after the warm-up and time (and "
                          "profile) its replays, as the layer's step runs it")
@@ -145,7 +148,7 @@ def main():
             N.combine(cfg, y_perm, slot, w, None, y)
     else:
         run = _gemm_stage(args.stage, args.experts, wl, cfg, x, ids, counts, offsets, slot,
-                          src, ws, rows_cap, dev)
+                          src, ws, rows_cap, dev, args.library)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -191,7 +194,8 @@ def main():
         line.update(sustained)
     if args.stage in ("expert_up", "expert_down"):
         flops = 2.0 * R * wl.d * wl.F
-        line.update({"experts": args.experts, "gemm": args.gemm, "flops": flops,
+        line.update({"experts": args.experts, "gemm": "cublas bmm" if args.library else args.gemm,
+                     "flops": flops,
                      "tflops": round(flops / (med * 1e-3) / 1e12, 1)})
     print(json.dumps(line), flush=True)
 
@@ -241,11 +245,15 @@ def _sustain(run, seconds):
             "mem_mhz_median": median(2), "mem_busy_samples": len(rows)}
 
 
-def _gemm_stage(stage, experts, wl, cfg, x, ids, counts, offsets, slot, src, ws, rows_cap, dev):
+def _gemm_stage(stage, experts, wl, cfg, x, ids, counts, offsets, slot, src, ws, rows_cap, dev,
+                library=False):
     """Buffers and launch of one expert-GEMM stage over the workload's kept rows: A is the
     dispatched token rows (expert_up) or seeded fp16 rows of the scale of h (expert_down);
     the weights are seeded N(0, 1/fan_in) values (W2 in fp16, as the layer stores it for
-    bf16 layers).  E4M3 stages quantise A and the weights once, outside the timed launch."""
+    bf16 layers).  E4M3 stages quantise A and the weights once, outside the timed launch.
+    ``library``: the same GEMMs (same operands, flops and bytes, no GELU) as one cuBLAS
+    batched GEMM, torch.bmm over the experts, for comparison; every expert must hold the
+    same number of rows."""
     E, d, F = wl.E, wl.d, wl.F
     g = torch.Generator(device=dev)
     g.manual_seed(2)
@@ -260,6 +268,18 @@ def _gemm_stage(stage, experts, wl, cfg, x, ids, counts, offsets, slot, src, ws,
         w = (torch.randn((E, d, F), generator=g, device=dev) * F ** -0.5).half()
         out = torch.empty((rows_cap, d), dtype=torch.float16, device=dev)
         n_in, n_out = F, d
+    if library:
+        cnt = torch.diff(offsets)
+        per = int(cnt[0].item())
+        if experts != "bf16" or not bool((cnt == per).all().item()) or per == 0:
+            raise SystemExit("--library needs bf16 experts with equal rows per expert")
+        a3 = a[:E * per].view(E, per, n_in)
+        wt = w.transpose(1, 2)
+        o3 = torch.empty((E, per, n_out), dtype=a.dtype, device=dev)
+
+        def run():
+            torch.bmm(a3, wt, out=o3)
+        return run
     if experts == "bf16":
         fn = N.expert_up if stage == "expert_up" else N.expert_down
 
