@@ -353,11 +353,10 @@ cudaError_t launch_tc2_down(const void* h, const void* w2h, void* y_perm, const 
 
 // How the expert GEMM's rows are split between the kernels: one CTA per 128-row tile
 // for all rows, CTA pairs per 256-row tile for all rows, or pairs for each group's whole
-// 256-row tiles and one CTA per 128-row tile for the rest.  A one-CTA 128x256 MMA reads
-// 96 B/clk of operands from shared memory and its TMA stages write as much again, more
-// than the SM's shared memory delivers, which caps the tensor pipe near two thirds; a
-// pair MMA reads and stages half of B per SM.  But pairs pad a group to a multiple of
-// 256 rows.  The split runs pairs on each group's whole 256-row tiles and, at the same
+// 256-row tiles and one CTA per 128-row tile for the rest.  Measured on B300, the
+// one-CTA 128x256 tiles keep the tensor pipe about two thirds busy and the pair tiles
+// (which stage and read half of B per SM) 85-93%.  But pairs pad a group to a multiple
+// of 256 rows.  The split runs pairs on each group's whole 256-row tiles and, at the same
 // time on the remaining SMs, one CTA per tile on the rest.  Measured on the layer shapes
 // (B300), MOE_GEMM_AUTO takes pairs when their padding is at most 5% (judged from the
 // per-group row bound, and with N filling 256-wide tiles), the split when groups are
