@@ -22,8 +22,9 @@
 namespace moe {
 
 // Expert outputs (yp, ys) are fp16 for bf16 layers and fp32 for fp32 layers.  Each
-// lane handles two 16-byte slots per pass (j and j + 32: 8 fp16 or 4 fp32 columns each),
-// so that up to 2 x 4 row loads are in flight per lane; k is summed in order, in fp32.
+// lane handles JV 16-byte slots of a row per pass (j, j + 32, ...: 8 fp16 or 4 fp32
+// columns each) for 8 / JV rows at a time, so that 8 row loads are in flight per lane; k
+// is summed in order, in fp32.
 template <typename Tin> struct CombineIn;
 template <> struct CombineIn<float> {
   static constexpr int P = 4;
@@ -56,12 +57,14 @@ __device__ __forceinline__ void store_slot<__nv_bfloat16, 8>(__nv_bfloat16* out,
   st_v4(out, Elem<__nv_bfloat16>::pack(acc));
 }
 
-template <typename Tout, typename Tin>
-__global__ void __launch_bounds__(256)
+template <typename Tout, typename Tin, int JV>
+__global__ void __launch_bounds__(256, JV == 2 ? 4 : 3)  // two slots: four blocks per SM
 combine_kernel(const Tin* __restrict__ yp, const int32_t* __restrict__ slot,
                const float* __restrict__ w, const Tin* __restrict__ ys, Tout* __restrict__ y,
                int Tn, int d, int K) {
-  constexpr int P = CombineIn<Tin>::P, KC = 4;
+  // JV 16-byte slots of each row per lane and pass, KC rows per batch of loads: 8 loads
+  // in flight per lane either way
+  constexpr int P = CombineIn<Tin>::P, KC = 8 / JV;
   __shared__ int s_slot[8][32];
   __shared__ float s_w[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -72,52 +75,57 @@ combine_kernel(const Tin* __restrict__ yp, const int32_t* __restrict__ slot,
       s_w[warp][lane] = w[(size_t)t * K + lane];
     }
     __syncwarp();
-    for (int j0 = lane; j0 < nvec; j0 += 64) {
-      const int j1 = j0 + 32;
-      const bool two = j1 < nvec;
-      float acc0[P], acc1[P];
+    for (int j0 = lane; j0 < nvec; j0 += 32 * JV) {
+      float acc[JV][P];
 #pragma unroll
-      for (int i = 0; i < P; ++i) acc0[i] = acc1[i] = 0.f;
+      for (int v = 0; v < JV; ++v)
+#pragma unroll
+        for (int i = 0; i < P; ++i) acc[v][i] = 0.f;
       for (int k0 = 0; k0 < K; k0 += KC) {
-        uint4 v0[KC], v1[KC];
+        uint4 ld[KC][JV];
 #pragma unroll
         for (int u = 0; u < KC; ++u) {
           const int k = k0 + u;
           const int s = (k < K) ? s_slot[warp][k] : -1;
           const uint4* rowp = reinterpret_cast<const uint4*>(yp + (size_t)(s < 0 ? 0 : s) * d);
-          v0[u] = (s >= 0) ? ld_nc_v4(rowp + j0) : make_uint4(0u, 0u, 0u, 0u);
-          v1[u] = (s >= 0 && two) ? ld_nc_v4(rowp + j1) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int v = 0; v < JV; ++v) {
+            const int j = j0 + 32 * v;
+            ld[u][v] = (s >= 0 && j < nvec) ? ld_nc_v4(rowp + j) : make_uint4(0u, 0u, 0u, 0u);
+          }
         }
 #pragma unroll
         for (int u = 0; u < KC; ++u) {
           const int k = k0 + u;
           if (k < K && s_slot[warp][k] >= 0) {
-            float f0[P], f1[P];
-            CombineIn<Tin>::unpack(v0[u], f0);
-            CombineIn<Tin>::unpack(v1[u], f1);
             const float wk = s_w[warp][k];
 #pragma unroll
-            for (int i = 0; i < P; ++i) {
-              acc0[i] = fmaf(wk, f0[i], acc0[i]);
-              acc1[i] = fmaf(wk, f1[i], acc1[i]);
+            for (int v = 0; v < JV; ++v) {
+              float f[P];
+              CombineIn<Tin>::unpack(ld[u][v], f);
+#pragma unroll
+              for (int i = 0; i < P; ++i) acc[v][i] = fmaf(wk, f[i], acc[v][i]);
             }
           }
         }
       }
       if (ys != nullptr) {
         const uint4* rs = reinterpret_cast<const uint4*>(ys + (size_t)t * d);
-        float f0[P], f1[P];
-        CombineIn<Tin>::unpack(ld_nc_v4(rs + j0), f0);
-        CombineIn<Tin>::unpack(two ? ld_nc_v4(rs + j1) : make_uint4(0u, 0u, 0u, 0u), f1);
 #pragma unroll
-        for (int i = 0; i < P; ++i) {
-          acc0[i] += f0[i];
-          acc1[i] += f1[i];
+        for (int v = 0; v < JV; ++v) {
+          const int j = j0 + 32 * v;
+          float f[P];
+          CombineIn<Tin>::unpack(j < nvec ? ld_nc_v4(rs + j) : make_uint4(0u, 0u, 0u, 0u), f);
+#pragma unroll
+          for (int i = 0; i < P; ++i) acc[v][i] += f[i];
         }
       }
       Tout* out = y + (size_t)t * d;
-      store_slot<Tout, P>(out + (size_t)j0 * P, acc0);
-      if (two) store_slot<Tout, P>(out + (size_t)j1 * P, acc1);
+#pragma unroll
+      for (int v = 0; v < JV; ++v) {
+        const int j = j0 + 32 * v;
+        if (j < nvec) store_slot<Tout, P>(out + (size_t)j * P, acc[v]);
+      }
     }
     __syncwarp();
   }
@@ -249,12 +257,24 @@ cudaError_t launch_combine(int dtype, const void* yp, const int32_t* slot, const
                            cudaStream_t st) {
   const int want = (Tn + 7) / 8;
   const int grid = want < num_sms * 16 ? want : num_sms * 16;
-  if (dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16, __half><<<grid, 256, 0, st>>>(
-        (const __half*)yp, slot, w, (const __half*)ys, (__nv_bfloat16*)y, Tn, d, K);
-  else
-    combine_kernel<float, float><<<grid, 256, 0, st>>>((const float*)yp, slot, w, (const float*)ys,
-                                                       (float*)y, Tn, d, K);
+  // with one or two rows per token, four slots of each row per lane keep 8 loads in
+  // flight; with more rows, two slots of four rows
+  const bool wide = K <= 2;
+  if (dtype == MOE_BF16) {
+    if (wide)
+      combine_kernel<__nv_bfloat16, __half, 4><<<grid, 256, 0, st>>>(
+          (const __half*)yp, slot, w, (const __half*)ys, (__nv_bfloat16*)y, Tn, d, K);
+    else
+      combine_kernel<__nv_bfloat16, __half, 2><<<grid, 256, 0, st>>>(
+          (const __half*)yp, slot, w, (const __half*)ys, (__nv_bfloat16*)y, Tn, d, K);
+  } else {
+    if (wide)
+      combine_kernel<float, float, 4><<<grid, 256, 0, st>>>((const float*)yp, slot, w,
+                                                            (const float*)ys, (float*)y, Tn, d, K);
+    else
+      combine_kernel<float, float, 2><<<grid, 256, 0, st>>>((const float*)yp, slot, w,
+                                                            (const float*)ys, (float*)y, Tn, d, K);
+  }
   count_launch();
   return cudaGetLastError();
 }
