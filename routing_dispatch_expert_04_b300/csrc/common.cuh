@@ -74,15 +74,15 @@ struct WsLayout {
 // 3-stage CTAs per SM measured slower than one 6-stage CTA).
 inline int router_ctas_per_sm(int E) { return E <= 64 ? 2 : 1; }
 
-// K splits of the tensor-core router: enough CTAs to cover the SMs when T/128 row tiles
-// alone would not (planned for 148 SMs; a smaller GPU just runs more waves).  Every
-// slice keeps at least one 64-wide k-block.
+// K splits of the tensor-core router: enough CTAs to fill the SMs' CTA slots when T/128
+// row tiles alone would not (planned for 148 SMs; a smaller GPU just runs more waves),
+// at most 8.  Every slice keeps at least one 64-wide k-block.
 inline int router_splits(const moe_config& c) {
   if (c.dtype != MOE_BF16 || c.T <= 0) return 1;
   const int mt = (c.T + 127) / 128;
   const int nkb = (c.d + 63) / 64;
-  int s = 148 / mt;
-  if (s > 4) s = 4;
+  int s = 148 * router_ctas_per_sm(c.E) / mt;
+  if (s > 8) s = 8;
   if (s > nkb) s = nkb;
   if (s < 2) return 1;
   const int kpb = (nkb + s - 1) / s;
