@@ -13,11 +13,15 @@
 //               STAGES-deep ring of 128-byte-swizzled shared-memory stages;
 //   warp 1      owns TMEM (2 x BN fp32 columns: double-buffered accumulators) and one
 //               elected thread issues tcgen05.mma (M=128, N=BN; kind::f16 with K=16 or
-//               kind::f8f6f4 with K=32) and commits;
+//               kind::f8f6f4 with K=32) and commits; the warp learns that a stage holds
+//               its data from a named barrier, not from the stage's mbarrier;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, E4M3 row/column scales,
 //               fused GELU (the normal-tail form in tc_common.cuh) or plain/bias,
 //               conversion and masked stores.  Overlaps the next tile's main loop through
-//               the second accumulator.
+//               the second accumulator;
+//   warp 6      stage watcher: waits on each stage's mbarrier and arrives on its named
+//               barrier (the stage gate in tc_common.cuh), so the MMA thread touches no
+//               shared memory per k-block.
 // Tiles are (group, n-tile, m-tile) with m fastest, so CTAs running at the same time
 // share one weight box through L2.  The per-group row ranges are read from `offsets` on
 // the device (no host synchronisation); the last m-tile of a group may run past the
@@ -51,7 +55,7 @@ struct TcLayout {
 };
 
 template <int BN, int STAGES, int EPI, int KIND, bool GATHER>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(TC_THREADS_GATED, 1)
 tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, const TcArgs args) {
   using Lay = TcLayout<BN, STAGES>;
@@ -65,6 +69,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint64_t* done = bars + 2 * STAGES + 4;
   uint32_t* s_tmem = (uint32_t*)(smem + Lay::MISC_OFF);
   volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
+  volatile int* s_mma_left = (volatile int*)(smem + Lay::MISC_OFF + 8);
   GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
 
   const long long clk0 = clock64();
@@ -86,6 +91,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
     mbar_init(done, 1);
     *s_abort = 0;
+    *s_mma_left = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
@@ -161,24 +167,22 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t IDESC = KIND == OP_BF16 ? idesc_bf16_f32(TC_BM, BN)
-                                                : idesc_fmt0_f32(TC_BM, BN);
-      int s = 0;
-      uint32_t ph = 0, acc = 0, aph = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        if (!wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        const int kb0 = (t % ksplit) * args.kpb;
-        const int kb1 = min(nkb, kb0 + args.kpb);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_phase(&full[s], ph, s_abort, args.hdr)) {
-            ok = false;
-            break;
-          }
+    // ---------------------------------------------------------------- MMA issuer
+    // lane 0 issues; the whole warp waits on the stage gate (named barriers)
+    constexpr uint32_t IDESC = KIND == OP_BF16 ? idesc_bf16_f32(TC_BM, BN)
+                                              : idesc_fmt0_f32(TC_BM, BN);
+    int s = 0;
+    uint32_t acc = 0, aph = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int ok = 1;
+      if (lane == 0) ok = wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      const int kb0 = (t % ksplit) * args.kpb;
+      const int kb1 = min(nkb, kb0 + args.kpb);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        named_sync(TC_GATE_BAR0 + s, TC_GATE_THREADS);
+        if (lane == 0) {
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
           const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
@@ -192,21 +196,38 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        (kb != kb0 || k != 0) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
         }
-        if (!ok) break;
-        mma_commit(&tfull[acc]);
-        acc ^= 1u;
-        if (acc == 0) aph ^= 1u;
+        __syncwarp();
+        if (++s == STAGES) s = 0;
       }
+      if (lane == 0) mma_commit(&tfull[acc]);
+      __syncwarp();
+      acc ^= 1u;
+      if (acc == 0) aph ^= 1u;
+    }
+    if (lane == 0) {
+      *s_mma_left = 1;  // the watcher stops arriving
       // every MMA issued by this thread has completed once `done` flips
       mma_commit(done);
       drain_wait(done, 0);
     }
     __syncwarp();
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- stage watcher
+    int s = 0;
+    uint32_t ph = 0;
+    bool gave_up = false, go = true;
+    for (int t = blockIdx.x; t < total && go; t += gridDim.x) {
+      const int kb0 = (t % ksplit) * args.kpb;
+      const int kb1 = min(nkb, kb0 + args.kpb);
+      for (int kb = kb0; kb < kb1 && go; ++kb) {
+        go = gate_arrive(s, full, empty, ph, gave_up, s_abort, s_mma_left, args.hdr, lane);
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
@@ -307,7 +328,7 @@ static cudaError_t launch_tc(const void* A, const void* B, const TcArgs& a, int 
   int64_t grid = m_bound * n_tiles * a.ksplit;
   if (grid > (int64_t)num_sms * ctas_per_sm) grid = (int64_t)num_sms * ctas_per_sm;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, TC_THREADS, Lay::ALLOC, st>>>(ma, mb, a);
+  kern<<<(unsigned)grid, TC_THREADS_GATED, Lay::ALLOC, st>>>(ma, mb, a);
   count_launch();
   return cudaGetLastError();
 }
@@ -425,18 +446,18 @@ static cudaError_t split_streams(SplitStreams** out) {
 }
 
 // SMs given to the pair kernel in the split plan: its share of the rows, weighted by
-// the one-CTA kernel taking ~1.25x as long per row, so that both finish together; an even
+// the one-CTA kernel taking ~1.4x as long per row, so that both finish together; an even
 // count (whole pairs), leaving the one-CTA kernel some.  Measured on the Mixtral shape
 // (640-row groups: 512 on pairs, 128 on one CTA), GEMM1 / GEMM2 ms by pair SMs: 106
-// 0.496 / 0.482, 110 0.471 / 0.492, 112 0.469 / 0.475, 114 0.466 / 0.491, 116 0.521 /
-// 0.498, 118 0.563 / 0.569; the weighting gives 112.  Past the optimum the one-CTA kernel's
-// share of the tiles finishes last, and the time rises steeply.
+// 0.471 / 0.477, 108 0.451 / 0.473, 112 0.512 / 0.473, 114+ 0.51 / 0.55; the weighting
+// gives 108.  Past the optimum the one-CTA kernel's share of the tiles finishes last, and
+// the time rises steeply.
 static int split_pair_sms(int64_t cap_per_group, int num_sms) {
   double frac = 0.75;  // groups of unknown size
   if (cap_per_group > 0) {
     const double whole = (double)(cap_per_group / 256 * 256);
     const double rest = (double)(cap_per_group - cap_per_group / 256 * 256);
-    frac = whole / (whole + 1.25 * rest);
+    frac = whole / (whole + 1.4 * rest);
   }
   int sp = ((int)(num_sms * frac)) & ~1;
   if (sp > num_sms - 2) sp = (num_sms - 2) & ~1;

@@ -13,7 +13,8 @@
 //     both CTAs; both CTAs' epilogue warps arrive on the even CTA's "accumulator empty"
 //     barrier, which therefore counts 8 warps.
 // Roles per CTA: warp 0 TMA producer, warp 1 TMEM owner (+ MMA issuer in the even CTA),
-// warps 2..5 epilogue (same fused GELU / fp32 epilogues as the one-CTA kernel).
+// warps 2..5 epilogue (same fused GELU / fp32 epilogues as the one-CTA kernel), warp 6
+// (even CTA) the stage watcher of the one-CTA kernel's stage gate.
 // Every mbarrier wait is bounded (the CTA records a timeout and leaves its loops); the
 // pair meets at a cluster barrier before TMEM is freed, so neither CTA exits while the
 // other's MMAs or copies may still touch its shared memory or TMEM.
@@ -47,7 +48,7 @@ struct Tc2Layout {
 constexpr uint64_t PAIR_ABORT_SETTLE_NS = 200000ull;
 
 template <int BN, int STAGES, int EPI, int KIND, bool GATHER>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS_GATED, 1)
 tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const TcArgs args) {
   using Lay = Tc2Layout<BN, STAGES>;
@@ -61,6 +62,7 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
   uint64_t* done = bars + 2 * STAGES + 4;
   uint32_t* s_tmem = (uint32_t*)(smem + Lay::MISC_OFF);
   volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
+  volatile int* s_mma_left = (volatile int*)(smem + Lay::MISC_OFF + 8);
   GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
 
   const long long clk0 = clock64();
@@ -84,6 +86,7 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
     mbar_init(done, 1);
     *s_abort = 0;
+    *s_mma_left = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
@@ -165,48 +168,66 @@ tc2_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
       // ---------------------------------------------------------------- MMA issuer
+      // lane 0 issues; the whole warp waits on the stage gate (named barriers)
       constexpr uint32_t IDESC = KIND == OP_BF16 ? idesc_bf16_f32(TC2_BM, BN)
                                                 : idesc_fmt0_f32(TC2_BM, BN);
       int s = 0;
-      uint32_t ph = 0, acc = 0, aph = 0;
-      bool ok = true;
-      for (int t = cluster; t < total && ok; t += n_clusters) {
-        if (!wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr)) break;
-        tc_fence_after();
+      uint32_t acc = 0, aph = 0;
+      for (int t = cluster; t < total; t += n_clusters) {
+        int ok = 1;
+        if (lane == 0) ok = wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_phase(&full[s], ph, s_abort, args.hdr)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
-          const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
+          named_sync(TC_GATE_BAR0 + s, TC_GATE_THREADS);
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
+            const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
-            if (KIND == OP_E4M3)
-              mma_e4m3_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
-                            IDESC, (kb != 0 || k != 0) ? 1u : 0u);
-            else
-              mma_f16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
-                           IDESC, (kb != 0 || k != 0) ? 1u : 0u);
+            for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
+              if (KIND == OP_E4M3)
+                mma_e4m3_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
+                              IDESC, (kb != 0 || k != 0) ? 1u : 0u);
+              else
+                mma_f16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
+                             IDESC, (kb != 0 || k != 0) ? 1u : 0u);
+            }
+            mma_commit_pair_mc(&empty[s], (uint16_t)3);
           }
-          mma_commit_pair_mc(&empty[s], (uint16_t)3);
+          __syncwarp();
+          if (++s == STAGES) s = 0;
+        }
+        if (lane == 0) mma_commit_pair_mc(&tfull[acc], (uint16_t)3);
+        __syncwarp();
+        acc ^= 1u;
+        if (acc == 0) aph ^= 1u;
+      }
+      if (lane == 0) {
+        *s_mma_left = 1;  // the watcher stops arriving
+        // every MMA issued by this thread has completed once `done` flips
+        mma_commit_pair_local(done);
+        drain_wait(done, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    if (rank == 0) {
+      // -------------------------------------------------------------- stage watcher
+      int s = 0;
+      uint32_t ph = 0;
+      bool gave_up = false, go = true;
+      for (int t = cluster; t < total && go; t += n_clusters) {
+        for (int kb = 0; kb < nkb && go; ++kb) {
+          go = gate_arrive(s, full, empty, ph, gave_up, s_abort, s_mma_left, args.hdr, lane);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if (!ok) break;
-        mma_commit_pair_mc(&tfull[acc], (uint16_t)3);
-        acc ^= 1u;
-        if (acc == 0) aph ^= 1u;
       }
-      // every MMA issued by this thread has completed once `done` flips
-      mma_commit_pair_local(done);
-      drain_wait(done, 0);
     }
     __syncwarp();
   } else {
@@ -273,7 +294,7 @@ static cudaError_t launch_tc2(const void* A, const void* B, const TcArgs& a, int
   int64_t clusters = m_bound * n_tiles;
   if (clusters > num_sms / 2) clusters = num_sms / 2;
   if (clusters < 1) clusters = 1;
-  kern<<<(unsigned)(2 * clusters), TC_THREADS, Lay::ALLOC, st>>>(ma, mb, a);
+  kern<<<(unsigned)(2 * clusters), TC_THREADS_GATED, Lay::ALLOC, st>>>(ma, mb, a);
   count_launch();
   return cudaGetLastError();
 }

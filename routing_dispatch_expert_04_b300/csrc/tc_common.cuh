@@ -28,6 +28,7 @@ template <int KIND> struct OpKind {
   static constexpr int BK = TC_ROW_BYTES / BYTES;  // K elements per stage
 };
 constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS_GATED = 224;  // + the watcher warp (warp 6)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 constexpr int TC_MAX_GROUPS = 256;
@@ -90,6 +91,36 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
       return false;
     }
   }
+}
+
+// Stage gate between a watcher warp and the MMA warp: named barrier TC_GATE_BAR0 + s means
+// "stage s holds its data".  A shared-memory access by the thread that issues the MMAs
+// stalls while its MMAs are in flight (an mbarrier wait or a plain load, about 230 cycles
+// each on B300), so the MMA warp waits on a named barrier and the watcher warp, which
+// issues no MMAs, does the mbarrier waits.  The watcher arrives exactly once per stage
+// the MMA warp syncs, in the same order, and never more than one round ahead of it: it
+// waits for the stage's data, or, after a wait has given up, for the MMA warp's commit of
+// the stage's previous round (or for the MMA warp to have left its loop, after which it
+// stops arriving).
+constexpr int TC_GATE_BAR0 = 1;
+constexpr int TC_GATE_THREADS = 64;  // watcher warp + MMA warp
+
+__device__ __forceinline__ bool gate_arrive(int s, uint64_t* full, uint64_t* empty, uint32_t ph,
+                                            bool& gave_up, volatile int* abort_flag,
+                                            volatile int* mma_left, uint32_t* hdr, int lane) {
+  if (lane == 0) {
+    if (!gave_up && !wait_phase(&full[s], ph, abort_flag, hdr)) gave_up = true;
+    if (gave_up) {
+      const uint64_t t0 = tc::globaltimer_ns();
+      while (!tc::mbar_try_wait(&empty[s], ph ^ 1u) && !*mma_left) {
+        if (tc::globaltimer_ns() - t0 > DRAIN_LIMIT_NS) break;
+      }
+    }
+  }
+  __syncwarp();
+  if (*mma_left) return false;
+  tc::named_arrive(TC_GATE_BAR0 + s, TC_GATE_THREADS);
+  return true;
 }
 
 // Wait used only while draining after an abort: ignores the abort flag, shorter limit.
