@@ -18,7 +18,8 @@
 //     tokens; for fp16 outputs the warp's 32 x 32 block goes through a shared-memory
 //     buffer, token-major, and each lane then stores 16 contiguous bytes of a token row.
 // Pipeline, barriers, bounded waits and teardown as in gemm_tc2.cu: warp 0 TMA producer,
-// warp 1 TMEM owner + MMA issuer (even CTA), warps 2..5 epilogue; both CTAs' copies
+// warp 1 TMEM owner + MMA issuer (even CTA), warps 2..5 epilogue, warp 6 stage watcher
+// (even CTA; the stage gate of tc_common.cuh); both CTAs' copies
 // signal the even CTA's "full" barrier, its commits arrive on both CTAs' "empty" and
 // "accumulator full" barriers, both CTAs' epilogues arrive on its "accumulator empty".
 // Tiles are (group, weight tile, token tile) with token tiles fastest, so the pairs that
@@ -115,7 +116,7 @@ __device__ __forceinline__ TTile decode_ttile(int t, int G, const GroupTable* ta
 }
 
 template <int STAGES, int EPI, int KIND>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS_GATED, 1)
 tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
                          const __grid_constant__ CUtensorMap tmap_x64,
                          const __grid_constant__ CUtensorMap tmap_x32,
@@ -131,6 +132,7 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
   uint64_t* done = bars + 2 * STAGES + 4;
   uint32_t* s_tmem = (uint32_t*)(smem + Lay::MISC_OFF);
   volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
+  volatile int* s_mma_left = (volatile int*)(smem + Lay::MISC_OFF + 8);
   GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
 
   const long long clk0 = clock64();
@@ -154,6 +156,7 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
     }
     mbar_init(done, 1);
     *s_abort = 0;
+    *s_mma_left = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_x128);
     tma_prefetch_desc(&tmap_x64);
@@ -221,49 +224,67 @@ tc2t_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x128,
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
       // ---------------------------------------------------------------- MMA issuer
+      // lane 0 issues; the whole warp waits on the stage gate (named barriers)
       const uint32_t idesc0 =
           KIND == OP_BF16 ? idesc_bf16_f32(T2T_TILE, 0) : idesc_fmt0_f32(T2T_TILE, 0);
       int s = 0;
-      uint32_t ph = 0, acc = 0, aph = 0;
-      bool ok = true;
-      for (int t = cluster; t < total && ok; t += n_clusters) {
+      uint32_t acc = 0, aph = 0;
+      for (int t = cluster; t < total; t += n_clusters) {
         const TTile ti = decode_ttile(t, G, tab);
         const uint32_t idesc = idesc0 | ((uint32_t)(ti.ninst >> 3) << 17);
-        if (!wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr)) break;
-        tc_fence_after();
+        int ok = 1;
+        if (lane == 0) ok = wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         const uint32_t d_tmem = tmem_base + acc * T2T_TILE;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_phase(&full[s], ph, s_abort, args.hdr)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t w_addr = smem_u32(smem + s * Lay::W_BYTES);
-          const uint32_t x_addr = smem_u32(smem + Lay::X_OFF + s * Lay::X_BYTES);
+          named_sync(TC_GATE_BAR0 + s, TC_GATE_THREADS);
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t w_addr = smem_u32(smem + s * Lay::W_BYTES);
+            const uint32_t x_addr = smem_u32(smem + Lay::X_OFF + s * Lay::X_BYTES);
 #pragma unroll
-          for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
-            if (KIND == OP_E4M3)
-              mma_e4m3_pair(d_tmem, sdesc_sw128(w_addr + k * 32), sdesc_sw128(x_addr + k * 32),
-                            idesc, (kb != 0 || k != 0) ? 1u : 0u);
-            else
-              mma_f16_pair(d_tmem, sdesc_sw128(w_addr + k * 32), sdesc_sw128(x_addr + k * 32),
-                           idesc, (kb != 0 || k != 0) ? 1u : 0u);
+            for (int k = 0; k < TC_ROW_BYTES / 32; ++k) {  // 32 bytes of K per MMA
+              if (KIND == OP_E4M3)
+                mma_e4m3_pair(d_tmem, sdesc_sw128(w_addr + k * 32), sdesc_sw128(x_addr + k * 32),
+                              idesc, (kb != 0 || k != 0) ? 1u : 0u);
+              else
+                mma_f16_pair(d_tmem, sdesc_sw128(w_addr + k * 32), sdesc_sw128(x_addr + k * 32),
+                             idesc, (kb != 0 || k != 0) ? 1u : 0u);
+            }
+            mma_commit_pair_mc(&empty[s], (uint16_t)3);
           }
-          mma_commit_pair_mc(&empty[s], (uint16_t)3);
+          __syncwarp();
+          if (++s == STAGES) s = 0;
+        }
+        if (lane == 0) mma_commit_pair_mc(&tfull[acc], (uint16_t)3);
+        __syncwarp();
+        acc ^= 1u;
+        if (acc == 0) aph ^= 1u;
+      }
+      if (lane == 0) {
+        *s_mma_left = 1;  // the watcher stops arriving
+        mma_commit_pair_local(done);
+        drain_wait(done, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    if (rank == 0) {
+      // -------------------------------------------------------------- stage watcher
+      int s = 0;
+      uint32_t ph = 0;
+      bool gave_up = false, go = true;
+      for (int t = cluster; t < total && go; t += n_clusters) {
+        for (int kb = 0; kb < nkb && go; ++kb) {
+          go = gate_arrive(s, full, empty, ph, gave_up, s_abort, s_mma_left, args.hdr, lane);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if (!ok) break;
-        mma_commit_pair_mc(&tfull[acc], (uint16_t)3);
-        acc ^= 1u;
-        if (acc == 0) aph ^= 1u;
       }
-      mma_commit_pair_local(done);
-      drain_wait(done, 0);
     }
     __syncwarp();
   } else {
@@ -335,7 +356,7 @@ static cudaError_t launch_tc2t(const void* X, const void* W, const TcArgs& a, in
   int64_t clusters = w_tiles * t_bound;
   if (clusters > num_sms / 2) clusters = num_sms / 2;
   if (clusters < 1) clusters = 1;
-  kern<<<(unsigned)(2 * clusters), TC_THREADS, Lay::ALLOC, st>>>(mx128, mx64, mx32, mw, a);
+  kern<<<(unsigned)(2 * clusters), TC_THREADS_GATED, Lay::ALLOC, st>>>(mx128, mx64, mx32, mw, a);
   count_launch();
   return cudaGetLastError();
 }
