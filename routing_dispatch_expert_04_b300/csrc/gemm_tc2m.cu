@@ -17,7 +17,8 @@
 // m-tile of its slab, so the pairs that run together walk each weight slab once between
 // them (the split plan instead ran the remainders as a second kernel on other SMs).
 // Pipeline, barriers, bounded waits and teardown as in gemm_tc2.cu: warp 0 TMA producer,
-// warp 1 TMEM owner + MMA issuer (even CTA), warps 2..5 epilogue; both CTAs' copies
+// warp 1 TMEM owner + MMA issuer (even CTA), warps 2..5 epilogue, warp 6 stage watcher
+// (even CTA; the stage gate of tc_common.cuh); both CTAs' copies
 // signal the even CTA's "full" barrier, its commits arrive on both CTAs' "empty" and
 // "accumulator full" barriers, both CTAs' epilogues arrive on its "accumulator empty".
 #include "tc_common.cuh"
@@ -116,7 +117,7 @@ __device__ __forceinline__ MTile decode_mtile(int t, int G, const GroupTable* ta
 }
 
 template <int STAGES, int EPI, int KIND>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS_GATED, 1)
 tc2m_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a128,
                          const __grid_constant__ CUtensorMap tmap_a64,
                          const __grid_constant__ CUtensorMap tmap_a32,
@@ -134,6 +135,7 @@ tc2m_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a128,
   uint64_t* done = bars + 2 * STAGES + 4;
   uint32_t* s_tmem = (uint32_t*)(smem + Lay::MISC_OFF);
   volatile int* s_abort = (volatile int*)(smem + Lay::MISC_OFF + 4);
+  volatile int* s_mma_left = (volatile int*)(smem + Lay::MISC_OFF + 8);
   GroupTable* tab = (GroupTable*)(smem + Lay::GRP_OFF);
 
   const long long clk0 = clock64();
@@ -157,6 +159,7 @@ tc2m_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a128,
     }
     mbar_init(done, 1);
     *s_abort = 0;
+    *s_mma_left = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a128);
     tma_prefetch_desc(&tmap_a64);
@@ -234,51 +237,69 @@ tc2m_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a128,
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    if (rank == 0) {
       // ---------------------------------------------------------------- MMA issuer
       // Whole tile: D[rows, cols] += A(rows) . B(cols)^T, M=256, N=256.
       // Remainder tile: D[cols, rows] += B(cols) . A(rows)^T, M=256, N = its rows.
+      // lane 0 issues; the whole warp waits on the stage gate (named barriers)
       const uint32_t idesc_whole =
           KIND == OP_BF16 ? idesc_bf16_f32(TM_TILE, TM_TILE) : idesc_fmt0_f32(TM_TILE, TM_TILE);
       const uint32_t idesc_tr0 =
           KIND == OP_BF16 ? idesc_bf16_f32(TM_TILE, 0) : idesc_fmt0_f32(TM_TILE, 0);
       int s = 0;
-      uint32_t ph = 0, acc = 0, aph = 0;
-      bool ok = true;
-      for (int t = cluster; t < total && ok; t += n_clusters) {
+      uint32_t acc = 0, aph = 0;
+      for (int t = cluster; t < total; t += n_clusters) {
         const MTile ti = decode_mtile(t, G, tab);
         const uint32_t idesc = ti.tr ? (idesc_tr0 | ((uint32_t)(ti.ninst >> 3) << 17)) : idesc_whole;
-        if (!wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr)) break;
-        tc_fence_after();
+        int ok = 1;
+        if (lane == 0) ok = wait_phase(&tempty[acc], aph ^ 1u, s_abort, args.hdr) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         const uint32_t d_tmem = tmem_base + acc * TM_TILE;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_phase(&full[s], ph, s_abort, args.hdr)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
-          const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
-          const uint32_t m_addr = ti.tr ? b_addr : a_addr;  // operand on the MMA's M side
-          const uint32_t n_addr = ti.tr ? a_addr : b_addr;  // and on its N side
+          named_sync(TC_GATE_BAR0 + s, TC_GATE_THREADS);
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + s * Lay::A_BYTES);
+            const uint32_t b_addr = smem_u32(smem + Lay::B_OFF + s * Lay::B_BYTES);
+            const uint32_t m_addr = ti.tr ? b_addr : a_addr;  // operand on the MMA's M side
+            const uint32_t n_addr = ti.tr ? a_addr : b_addr;  // and on its N side
 #pragma unroll
-          for (int k = 0; k < TC_ROW_BYTES / 32; ++k)  // 32 bytes of K per MMA
-            mma_f16_pair(d_tmem, sdesc_sw128(m_addr + k * 32), sdesc_sw128(n_addr + k * 32), idesc,
-                         (kb != 0 || k != 0) ? 1u : 0u);
-          mma_commit_pair_mc(&empty[s], (uint16_t)3);
+            for (int k = 0; k < TC_ROW_BYTES / 32; ++k)  // 32 bytes of K per MMA
+              mma_f16_pair(d_tmem, sdesc_sw128(m_addr + k * 32), sdesc_sw128(n_addr + k * 32),
+                           idesc, (kb != 0 || k != 0) ? 1u : 0u);
+            mma_commit_pair_mc(&empty[s], (uint16_t)3);
+          }
+          __syncwarp();
+          if (++s == STAGES) s = 0;
+        }
+        if (lane == 0) mma_commit_pair_mc(&tfull[acc], (uint16_t)3);
+        __syncwarp();
+        acc ^= 1u;
+        if (acc == 0) aph ^= 1u;
+      }
+      if (lane == 0) {
+        *s_mma_left = 1;  // the watcher stops arriving
+        // every MMA issued by this thread has completed once `done` flips
+        mma_commit_pair_local(done);
+        drain_wait(done, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    if (rank == 0) {
+      // -------------------------------------------------------------- stage watcher
+      int s = 0;
+      uint32_t ph = 0;
+      bool gave_up = false, go = true;
+      for (int t = cluster; t < total && go; t += n_clusters) {
+        for (int kb = 0; kb < nkb && go; ++kb) {
+          go = gate_arrive(s, full, empty, ph, gave_up, s_abort, s_mma_left, args.hdr, lane);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
-        if (!ok) break;
-        mma_commit_pair_mc(&tfull[acc], (uint16_t)3);
-        acc ^= 1u;
-        if (acc == 0) aph ^= 1u;
       }
-      // every MMA issued by this thread has completed once `done` flips
-      mma_commit_pair_local(done);
-      drain_wait(done, 0);
     }
     __syncwarp();
   } else {
@@ -359,7 +380,7 @@ static cudaError_t launch_tc2m(const void* X, const void* W, const TcArgs& a, in
   int64_t clusters = slabs * t_bound;
   if (clusters > num_sms / 2) clusters = num_sms / 2;
   if (clusters < 1) clusters = 1;
-  kern<<<(unsigned)(2 * clusters), TC_THREADS, Lay::ALLOC, st>>>(m128, m64, m32, mw, a);
+  kern<<<(unsigned)(2 * clusters), TC_THREADS_GATED, Lay::ALLOC, st>>>(m128, m64, m32, mw, a);
   count_launch();
   return cudaGetLastError();
 }
