@@ -98,8 +98,13 @@ def test_expert_down_f16(name, offs, Kd, Nn, pairing):
 
 
 @pytest.mark.parametrize("T,E,d,bias", [(300, 8, 256, False), (257, 128, 512, True),
-                                        (130, 256, 1024, True), (64, 5, 64, True)])
+                                        (130, 256, 1024, True), (64, 5, 64, True),
+                                        (512, 8, 1024, True), (600, 8, 832, False)])
 def test_tensor_core_router(T, E, d, bias):
+    """Router logits against the fp64 oracle.  The cases cover one K slice (64, 5, 64),
+    4 slices, 8 slices of one k-block each (257, 128, 512), 8 slices of two (130, 256,
+    1024 and 512, 8, 1024: two CTAs per SM) and 7 slices whose last one is shorter
+    (600, 8, 832: 13 k-blocks in slices of two)."""
     cfg = N.make_config(T, d, E, min(2, E), 64, "bf16", -1)
     ws = torch.zeros(N.workspace_size(cfg), dtype=torch.uint8, device="cuda")
     x = _gen((T, d), 1.0, 5, torch.bfloat16)
