@@ -27,6 +27,7 @@ profiled launches are replays of it, as in the layer's step.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import statistics
 import time
@@ -84,6 +85,9 @@ def main():
                          "profile) its replays, as the layer's step runs it")
     ap.add_argument("--workload", default="long", choices=sorted(WORKLOADS))
     ap.add_argument("--tokens", type=int, default=0, help="override the token count T")
+    ap.add_argument("--num-experts", type=int, default=0,
+                    help="override the routed expert count E (a smaller case of the same "
+                         "layer, e.g. for a profiler capture that must stay a few GB)")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args()
@@ -94,6 +98,10 @@ def main():
     wl = WORKLOADS[args.workload]
     if args.tokens > 0:
         wl = wl.scaled(args.tokens)
+    if args.num_experts > 0:
+        if args.num_experts < wl.K:
+            raise SystemExit(f"--num-experts must be at least K = {wl.K}")
+        wl = dataclasses.replace(wl, name=f"{wl.name}_E{args.num_experts}", E=args.num_experts)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     inp = make_inputs(wl, dev, seed=0, weights=False)
