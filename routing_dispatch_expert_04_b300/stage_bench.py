@@ -21,7 +21,9 @@ cudaProfilerStart and cudaProfilerStop, for a profiler's range replay: the count
 cover the whole stage, for the split plan both of its GEMM kernels (launched concurrently
 as in the layer; whether a profiler lets them overlap is the profiler's choice).  With
 ``--graph`` the stage is captured in a CUDA graph after the warm-up, and the timed and
-profiled launches are replays of it, as in the layer's step.
+profiled launches are replays of it, as in the layer's step.  ``--tokens`` and
+``--num-experts`` shrink the workload (same d, F, K and routing recipe) for profiler
+captures that must stay a few GB on the device.
 """
 
 from __future__ import annotations
